@@ -1,0 +1,148 @@
+"""fp64 CPU oracle for the monolithic LM-head loss -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The library path never does, and this
+package imports nothing from the library.
+
+The arithmetic lives in ``headloss_oracle.c`` (plain C, fp64, one row at a
+time); this module builds it with gcc on first use and marshals numpy arrays
+through ctypes.  Inputs are passed as fp64 arrays that are exact upcasts of
+the logits the library sees.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "headloss_oracle.c")
+_LIB = os.path.join(_HERE, "libheadloss_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# Loss / metric bits, defined here independently of the library.
+CE, Z, DIST_CE, FKL, RKL, GRPO, GRPO_STATS, ENTROPY = (1 << i for i in range(8))
+DIST_ANY = DIST_CE | FKL | RKL
+
+# Per-row record fields (headloss_oracle.c, enum RF_*).
+RF = dict(valid=0, ce=1, z=2, dist_ce=3, fkl=4, rkl=5, grpo=6, logprob=7, ratio=8,
+          clipped=9, kl3=10, adv=11, adv2=12, entropy=13, ambiguous=14, act=15, lse=16)
+N_RF = 17
+
+# Scalar slots of a call.
+SLOTS = ("total", "ce", "z", "dist_ce", "fkl", "rkl", "grpo_loss", "new_logprob_mean",
+         "ratio_mean", "clip_frac", "kl_k3", "adv_mean", "adv_std", "entropy_mean",
+         "n_valid", "n_clipped")
+
+
+class _Cfg(ctypes.Structure):
+    _fields_ = [("flags", ctypes.c_uint32)] + [
+        (n, ctypes.c_double)
+        for n in ("w_ce", "w_z", "w_dist_ce", "w_fkl", "w_rkl", "w_grpo", "w_entropy",
+                  "grad_scale", "temperature", "clip_eps", "softcap", "logits_scale")
+    ]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP, -O2, no fast-math)."""
+    with _lock:
+        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+            tmp = _LIB + f".tmp{os.getpid()}"
+            subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+                                   "-o", tmp, _SRC, "-lm"])
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        dp = ctypes.POINTER(ctypes.c_double)
+        ip = ctypes.POINTER(ctypes.c_int64)
+        lib.oracle_rows.argtypes = [ctypes.POINTER(_Cfg), ctypes.c_int64, ctypes.c_int64, dp, ip,
+                                    dp, dp, dp, ctypes.c_int64, dp, dp, dp, ctypes.c_int]
+        lib.oracle_rows.restype = ctypes.c_int
+        lib.oracle_reduce.argtypes = [ctypes.POINTER(_Cfg), dp, ctypes.c_int64, dp]
+        lib.oracle_reduce.restype = None
+        lib.oracle_count_valid.argtypes = [ip, ctypes.c_int64]
+        lib.oracle_count_valid.restype = ctypes.c_int64
+        lib.oracle_row_fields.restype = ctypes.c_int
+        assert lib.oracle_row_fields() == N_RF
+        _lib = lib
+    return _lib
+
+
+def make_cfg(flags: int, weights: dict | None = None, temperature: float = 1.0,
+             clip_eps: float = 0.2, softcap: float = 0.0, logits_scale: float = 1.0,
+             grad_scale: float = 1.0) -> _Cfg:
+    w = dict(ce=1.0, z=0.0, dist_ce=0.0, fkl=0.0, rkl=0.0, grpo=1.0, entropy=0.0)
+    if weights:
+        w.update(weights)
+    return _Cfg(flags, w["ce"], w["z"], w["dist_ce"], w["fkl"], w["rkl"], w["grpo"],
+                w["entropy"], grad_scale, temperature, clip_eps, softcap, logits_scale)
+
+
+def _ptr(a, ctype):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _f64(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float64)
+
+
+def count_valid(labels, n_rows: int) -> int:
+    if labels is None:
+        return int(n_rows)
+    lab = np.ascontiguousarray(labels, dtype=np.int64)
+    return int(_load().oracle_count_valid(_ptr(lab, ctypes.c_int64), lab.shape[0]))
+
+
+def rows(cfg: _Cfg, x, labels=None, teacher=None, old_logprobs=None, advantages=None,
+         n_valid_total: int | None = None, want_grad: bool = True, want_gmag: bool = False,
+         n_threads: int = 0):
+    """Per-row records (n x 17) and, optionally, gradient / term magnitude (n x V)."""
+    lib = _load()
+    x = _f64(x)
+    n, V = x.shape
+    lab = None if labels is None else np.ascontiguousarray(labels, dtype=np.int64)
+    t = _f64(teacher)
+    o = _f64(old_logprobs)
+    a = _f64(advantages)
+    if n_valid_total is None:
+        n_valid_total = count_valid(lab, n)
+    rec = np.zeros((n, N_RF), np.float64)
+    grad = np.empty((n, V), np.float64) if want_grad else None
+    gmag = np.empty((n, V), np.float64) if want_gmag else None
+    rc = lib.oracle_rows(ctypes.byref(cfg), n, V, _ptr(x, ctypes.c_double),
+                         _ptr(lab, ctypes.c_int64), _ptr(t, ctypes.c_double),
+                         _ptr(o, ctypes.c_double), _ptr(a, ctypes.c_double), int(n_valid_total),
+                         _ptr(rec, ctypes.c_double), _ptr(grad, ctypes.c_double),
+                         _ptr(gmag, ctypes.c_double), int(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_rows rejected its arguments")
+    return rec, grad, gmag
+
+
+def reduce(cfg: _Cfg, rec) -> np.ndarray:
+    """The sixteen scalars of a call from its per-row records."""
+    rec = _f64(rec)
+    out = np.zeros(16, np.float64)
+    _load().oracle_reduce(ctypes.byref(cfg), _ptr(rec, ctypes.c_double), rec.shape[0],
+                          _ptr(out, ctypes.c_double))
+    return out
+
+
+def forward_backward(cfg: _Cfg, x, labels=None, teacher=None, old_logprobs=None,
+                     advantages=None, want_grad: bool = True, want_gmag: bool = False,
+                     n_threads: int = 0):
+    """A whole call: (scalars[16], per-row records, grad or None, gmag or None)."""
+    rec, grad, gmag = rows(cfg, x, labels, teacher, old_logprobs, advantages, None, want_grad,
+                           want_gmag, n_threads)
+    return reduce(cfg, rec), rec, grad, gmag
