@@ -1,0 +1,449 @@
+"""Benchmark of the fused LM-head loss (one JSON line on stdout).
+
+A step is one headloss_forward_backward call over the whole batch of the
+workload (default: the all-in combined loss set, 65536 tokens x 128256 vocab,
+bf16): every loss scalar plus the one combined logits gradient.  Inputs are
+seeded synthetic tensors larger than L2, resident in HBM before timing.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Under torchrun each rank runs its own batch on its own GPU (rows are
+independent: weak scaling, no data-path collective); the time is the max over
+ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused head-loss tokens/s and HBM GB/s (% of GB300 peak) per loss set, 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="all_in_bf16")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-loss-sets", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="wall time the CPU-baseline sample is sized for")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for fn in sorted(glob.glob(os.path.join(ROOT, "gradient_row_online_gb300", "csrc", "*"))):
+        with open(fn, "rb") as f:
+            h.update(os.path.basename(fn).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the row kernel from a committed ncu summary,
+    if it was taken on the current kernel sources (else None)."""
+    fn = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(fn) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.out,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- our arm
+
+def time_calls(fn, stream, steps):
+    """Per-call durations (ms) by CUDA events on `stream`, synchronised around."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def run_ours(args, rank, world, local):
+    import gradient_row_online_gb300 as pkg
+    from gradient_row_online_gb300 import headloss as hlb
+    from gradient_row_online_gb300 import workloads as W
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    wl = W.WORKLOADS[args.workload].replace(seed=rank)  # each rank its own batch
+    hlb.load_library()
+    h = pkg.headloss_for(wl)
+    inp = W.make_inputs(wl, dev)
+    grad = torch.empty_like(inp["logits"])
+    out = torch.empty(16, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    dcode = hlb.dtype_code(wl.dtype)
+
+    def step():
+        hlb.headloss_forward_backward(h.h, inp["logits"], wl.N, wl.V, dcode, inp["labels"],
+                                      inp["teacher"], inp["old_logprobs"], inp["advantages"],
+                                      grad, out, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        per_call = []
+        # per-call events inside the timed region (same stream)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, b in evs:
+            a.record(stream)
+            step()
+            b.record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        total_ms = t0.elapsed_time(t1)
+        per_call = [a.elapsed_time(b) for a, b in evs]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+    scal = out.double().cpu().numpy()
+    err = h.device_error()
+    if err != hlb.HEADLOSS_OK:
+        raise RuntimeError(hlb.STATUS[err])
+
+    ms_per_step = total_ms / args.steps
+    tokens_per_s = wl.N * world * args.steps / (total_ms / 1e3)
+    bytes_per_launch = wl.min_bytes_per_row() * wl.N
+    call_ms = statistics.mean(per_call)
+    achieved = bytes_per_launch / (call_ms / 1e3) / 1e9
+    peak, peak_kind = peaks()
+    plan = h.plan(wl.V, dcode)
+    clocks = clk.summary()
+
+    line = {
+        "metric": METRIC,
+        "value": tokens_per_s,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded N(0,3^2) logits; see workloads.py)",
+        "config": {
+            "workload": wl.name, "N_tokens": wl.N, "V": wl.V, "io_dtype": str(wl.dtype)[6:],
+            "losses": list(wl.losses), "temperature": wl.temperature, "softcap": wl.softcap,
+            "logits_scale": wl.logits_scale, "clip_eps": wl.clip_eps,
+            "parallelism": f"rows sharded over {world} GPU(s), no collective",
+            "l2": f"inputs larger than L2 ({bytes_per_launch / 1e9:.1f} GB per step)",
+            "plan": plan,
+        },
+        "roofline": {
+            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_kind": peak_kind,
+            "traffic": recorded_traffic(wl.name),
+            "algorithmic_bytes_per_launch": bytes_per_launch,
+            "kernel": "hl::rows_kernel (timed as the whole call: count + rows + finalize)",
+        },
+        "gpu_launches": args.steps * hlb.headloss_launches_per_call(),
+        "clocks": clocks,
+        "scalars": {n: float(v) for n, v in zip(hlb.SLOTS, scal)},
+    }
+    if not args.no_loss_sets and world == 1:
+        line["loss_sets"] = loss_sets(args, dev, exclude=wl.name, peak=peak)
+    if not args.no_e2e:
+        del grad
+        line["e2e"] = e2e(wl, h, inp, args, dev, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return line
+
+
+def loss_sets(args, dev, exclude, peak):
+    """Short measurement of the other full-size loss sets (same call, same clock)."""
+    import gradient_row_online_gb300 as pkg
+    from gradient_row_online_gb300 import headloss as hlb
+    from gradient_row_online_gb300 import workloads as W
+
+    res = {}
+    for name in W.ORDER[1:]:
+        if name == exclude:
+            continue
+        wl = W.WORKLOADS[name]
+        inp = W.make_inputs(wl, dev)
+        g = torch.empty_like(inp["logits"])
+        out = torch.empty(16, dtype=torch.float32, device=dev)
+        h = pkg.headloss_for(wl)
+        s = torch.cuda.current_stream(dev)
+        fn = lambda: h(inp["logits"], inp["labels"], inp["teacher"], inp["old_logprobs"],
+                       inp["advantages"], g, out, s)
+        for _ in range(3):
+            fn()
+        ms = statistics.mean(time_calls(fn, s, 10))
+        gbs = wl.min_bytes_per_row() * wl.N / (ms / 1e3) / 1e9
+        res[name] = {"tokens_per_s": wl.N / (ms / 1e3), "ms_per_call": ms, "gbs": gbs,
+                     "frac_of_measured_peak": gbs / peak, "plan": h.plan(wl.V, hlb.dtype_code(wl.dtype))}
+        del inp, g
+        h.close()
+        torch.cuda.empty_cache()
+    return res
+
+
+def e2e(wl, h, inp, args, dev, world):
+    """The same metric through the public call with pinned HOST buffers: every
+    step copies its inputs host->device and reads the gradient and scalars back."""
+    from gradient_row_online_gb300 import headloss as hlb
+
+    names = ["logits", "labels", "teacher", "old_logprobs", "advantages"]
+    host = {k: (None if inp[k] is None else torch.empty(inp[k].shape, dtype=inp[k].dtype,
+                                                        pin_memory=True)) for k in names}
+    for k in names:
+        if host[k] is not None:
+            host[k].copy_(inp[k])
+    h_grad = torch.empty(inp["logits"].shape, dtype=inp["logits"].dtype, pin_memory=True)
+    h_out = torch.empty(16, dtype=torch.float32, pin_memory=True)
+    d_grad = torch.empty_like(inp["logits"])
+    d_out = torch.empty(16, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names if host[k] is not None)
+    d2h = h_grad.numel() * h_grad.element_size() + 64
+
+    def step():
+        for k in names:
+            if host[k] is not None:
+                inp[k].copy_(host[k], non_blocking=True)
+        hlb.headloss_forward_backward(h.h, inp["logits"], wl.N, wl.V, hlb.dtype_code(wl.dtype),
+                                      inp["labels"], inp["teacher"], inp["old_logprobs"],
+                                      inp["advantages"], d_grad, d_out, stream)
+        h_grad.copy_(d_grad, non_blocking=True)
+        h_out.copy_(d_out, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    ms = time_calls(step, stream, args.e2e_steps)
+    total = sum(ms)
+    return {"value": wl.N * world * len(ms) / (total / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": len(ms),
+            "ms_per_step": total / len(ms)}
+
+
+def cpu_rows_per_s(wl, x, lab, t, old, adv, n_valid, threads):
+    import oracle as orc
+    from tests import _harness as H
+    cfg = H.oracle_cfg(wl)
+    t0 = time.perf_counter()
+    orc.rows(cfg, x, lab, t, old, adv, n_valid, True, False, threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, inp, seconds, reps=1):
+    """The fp64 oracle, as it stands, on this host's cores, on a bounded row
+    sample of the same workload (rows sized for about `seconds` of wall time)."""
+    import numpy as np
+
+    import oracle as orc
+    from tests import _harness as H
+
+    cores = len(os.sched_getaffinity(0))
+    n_valid = orc.count_valid(H.host_i64(inp["labels"]), inp["labels"].shape[0])
+
+    def sample(r):
+        pick = lambda k: None if inp[k] is None else inp[k][:r]
+        return (H.host64(pick("logits")), H.host_i64(pick("labels")), H.host64(pick("teacher")),
+                H.host64(pick("old_logprobs")), H.host64(pick("advantages")))
+
+    probe = min(wl.N, max(cores, 16))
+    s = sample(probe)
+    dt = cpu_rows_per_s(wl, *s, n_valid, cores)
+    rows = int(min(wl.N, max(probe, probe * seconds / max(dt, 1e-6))))
+    s = sample(rows)
+    dt = cpu_rows_per_s(wl, *s, n_valid, cores)
+    return {"value": rows / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {rows} of {wl.N} rows of {wl.name} (gradient + all scalars, fp64, "
+                      f"{cores} OpenMP threads), {dt:.1f} s"}
+
+
+# ---------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: fp64 CPU, bounded row sample per step."""
+    import oracle as orc
+    from gradient_row_online_gb300 import workloads as W
+    from tests import _harness as H
+
+    wl = W.WORKLOADS[args.workload]
+    cores = len(os.sched_getaffinity(0))
+    # size one step: probe, then rows for ~(150 s / (steps + warmup)) per step
+    budget = max(1.0, 150.0 / (args.steps + max(3, args.warmup)))
+    probe = 16
+    inp = W.make_inputs(wl, "cpu", rows=probe)
+    cfg = H.oracle_cfg(wl)
+    nv = orc.count_valid(H.host_i64(inp["labels"]), probe)
+    args_h = lambda d: (H.host64(d["logits"]), H.host_i64(d["labels"]), H.host64(d["teacher"]),
+                        H.host64(d["old_logprobs"]), H.host64(d["advantages"]))
+    t0 = time.perf_counter()
+    orc.rows(cfg, *args_h(inp), nv, True, False, cores)
+    dt = time.perf_counter() - t0
+    rows = int(max(probe, min(wl.N, probe * budget / max(dt, 1e-6))))
+    inp = W.make_inputs(wl, "cpu", rows=rows)
+    a = args_h(inp)
+    nv = orc.count_valid(a[1], rows)
+    for _ in range(max(3, args.warmup)):
+        orc.rows(cfg, *a, nv, True, False, cores)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        rec, _, _ = orc.rows(cfg, *a, nv, True, False, cores)
+        orc.reduce(cfg, rec)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = rows * len(times) / total
+    sample = (f"first {rows} of {wl.N} rows of {wl.name} per step (gradient + all scalars, "
+              f"fp64, {cores} OpenMP threads)")
+    return {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; see workloads.py)", "impl": "reference",
+        "config": {"workload": wl.name, "N_tokens": wl.N, "V": wl.V, "losses": list(wl.losses),
+                   "rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return 0
+    line = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,458 @@
+// headloss_api.cu -- the C ABI (include/headloss.h): argument checks, the
+// launch planner, and the two small kernels around the row kernel (valid-row
+// count before it, deterministic scalar finalize after it).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "headloss.h"
+#include "hl_params.h"
+#include "hl_rows.cuh"
+
+namespace hl {
+const void* rows_kernel_bf16(int feat);
+const void* rows_kernel_fp16(int feat);
+const void* rows_kernel_fp32(int feat);
+
+// Valid rows of the call (0 <= label < V); a label >= V raises E_LABEL.
+// One block: the count is an exact integer whatever the order.
+__global__ void __launch_bounds__(1024) count_valid_kernel(const int64_t* labels, int64_t N,
+                                                           int64_t V, long long* out, int* err) {
+    __shared__ long long part[32];
+    long long c = 0;
+    int bad = 0;
+    if (labels) {
+        for (int64_t i = threadIdx.x; i < N; i += blockDim.x) {
+            const int64_t y = labels[i];
+            if (y >= 0 && y < V) ++c;
+            else if (y >= V) bad = 1;
+        }
+    } else if (threadIdx.x == 0) {
+        c = N;
+    }
+    for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = c;
+    if (bad) atomicOr(err, E_LABEL);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        long long tot = 0;
+        for (int w = 0; w < int(blockDim.x >> 5); ++w) tot += part[w];
+        *out = tot;
+    }
+}
+
+struct FinalizeArgs {
+    uint32_t flags;
+    float w_ce, w_z, w_dce, w_fkl, w_rkl, w_grpo, w_ent;
+};
+
+// Sums the per-cluster partials in cluster order (fp64) and writes the
+// sixteen scalars (means over valid rows; unselected slots 0).
+__global__ void finalize_kernel(const double* partials, int nclusters, const long long* n_valid,
+                                FinalizeArgs a, float* out) {
+    __shared__ double tot[NACC];
+    const int t = threadIdx.x;
+    if (t < NACC) {
+        double s = 0.0;
+        for (int c = 0; c < nclusters; ++c) s += partials[size_t(c) * NACC + t];
+        tot[t] = s;
+    }
+    __syncthreads();
+    if (t != 0) return;
+    double o[16];
+    for (int i = 0; i < 16; ++i) o[i] = 0.0;
+    const double n = double(*n_valid);
+    o[HEADLOSS_SLOT_N_VALID] = n;
+    if (n > 0.0) {
+        const uint32_t f = a.flags;
+        if (f & L_CE) o[HEADLOSS_SLOT_CE] = tot[A_CE] / n;
+        if (f & L_Z) o[HEADLOSS_SLOT_Z] = tot[A_Z] / n;
+        if (f & L_DIST_CE) o[HEADLOSS_SLOT_DIST_CE] = tot[A_DCE] / n;
+        if (f & L_FKL) o[HEADLOSS_SLOT_FKL] = tot[A_FKL] / n;
+        if (f & L_RKL) o[HEADLOSS_SLOT_RKL] = tot[A_RKL] / n;
+        if (f & L_GRPO) o[HEADLOSS_SLOT_GRPO] = tot[A_GRPO] / n;
+        if (f & L_GRPO_STATS) {
+            o[HEADLOSS_SLOT_NEW_LOGPROB] = tot[A_LP] / n;
+            o[HEADLOSS_SLOT_RATIO] = tot[A_RATIO] / n;
+            o[HEADLOSS_SLOT_CLIP_FRAC] = tot[A_NCLIP] / n;
+            o[HEADLOSS_SLOT_KL_K3] = tot[A_KL3] / n;
+            const double am = tot[A_ADV] / n;
+            const double var = tot[A_ADV2] / n - am * am;
+            o[HEADLOSS_SLOT_ADV_MEAN] = am;
+            o[HEADLOSS_SLOT_ADV_STD] = var > 0.0 ? sqrt(var) : 0.0;
+            o[HEADLOSS_SLOT_N_CLIPPED] = tot[A_NCLIP];
+        }
+        if (f & L_ENTROPY) o[HEADLOSS_SLOT_ENTROPY] = tot[A_ENT] / n;
+        double total = 0.0;
+        if (f & L_CE) total += double(a.w_ce) * o[HEADLOSS_SLOT_CE];
+        if (f & L_Z) total += double(a.w_z) * o[HEADLOSS_SLOT_Z];
+        if (f & L_DIST_CE) total += double(a.w_dce) * o[HEADLOSS_SLOT_DIST_CE];
+        if (f & L_FKL) total += double(a.w_fkl) * o[HEADLOSS_SLOT_FKL];
+        if (f & L_RKL) total += double(a.w_rkl) * o[HEADLOSS_SLOT_RKL];
+        if (f & L_GRPO) total += double(a.w_grpo) * o[HEADLOSS_SLOT_GRPO];
+        if (f & L_ENTROPY) total += double(a.w_ent) * o[HEADLOSS_SLOT_ENTROPY];
+        o[HEADLOSS_SLOT_TOTAL] = total;
+    }
+    for (int i = 0; i < 16; ++i) out[i] = float(o[i]);
+}
+
+}  // namespace hl
+
+using namespace hl;
+
+namespace {
+
+constexpr uint32_t kAllFlags = 0xffu;
+constexpr int kLaunchesPerCall = 3;
+
+struct Plan {
+    int64_t V = -1;
+    int dtype = -1, feat = -1;
+    int C = 0, nbuf = 0, words = 0, smem = 0, ncl = 0;
+    int64_t L = 0;
+    const void* kernel = nullptr;
+};
+
+}  // namespace
+
+struct headloss {
+    uint32_t flags;
+    headloss_weights w;
+    float T, eps, softcap, s;
+    int device, num_sms, smem_optin;
+    void* ws;
+    double* partials;
+    int partials_cap;  // clusters
+    long long* n_valid;
+    int* err;
+    int forced_C, forced_nbuf;
+    Plan plan;  // cache of the last plan
+    std::mutex mu;
+};
+
+namespace {
+
+int elem_size(int dtype) { return dtype == HEADLOSS_FP32 ? 4 : 2; }
+
+int feature_set(const headloss* h) {
+    int f = 0;
+    if (h->flags & (L_DIST_CE | L_FKL | L_RKL)) f |= F_TEACH;
+    if (h->flags & L_RKL) f |= F_RKL;
+    if (h->flags & L_ENTROPY) f |= F_ENT;
+    if (h->softcap > 0.f) f |= F_SOFTCAP;
+    return f;
+}
+
+const void* kernel_for(int dtype, int feat) {
+    switch (dtype) {
+        case HEADLOSS_BF16: return rows_kernel_bf16(feat);
+        case HEADLOSS_FP16: return rows_kernel_fp16(feat);
+        case HEADLOSS_FP32: return rows_kernel_fp32(feat);
+        default: return nullptr;
+    }
+}
+
+// Chooses the cluster size C (CTAs sharing one row), the column slice per
+// CTA, the number of row stages each CTA buffers, and the persistent grid.
+// Preference: the smallest cluster whose slice leaves room for at least two
+// stages (one computing, one or more in flight).
+int make_plan(headloss* h, int64_t V, int dtype, Plan* out) {
+    const int feat = feature_set(h);
+    if (h->plan.V == V && h->plan.dtype == dtype && h->plan.feat == feat &&
+        (h->forced_C == 0 || h->forced_C == h->plan.C) &&
+        (h->forced_nbuf == 0 || h->forced_nbuf == h->plan.nbuf)) {
+        *out = h->plan;
+        return HEADLOSS_OK;
+    }
+    const void* kernel = kernel_for(dtype, feat);
+    if (!kernel) return HEADLOSS_ERR_DTYPE;
+    const int es = elem_size(dtype);
+    const int epw = 16 / es;
+    const int ops = (feat & F_TEACH) ? 2 : 1;
+    const int acc_bytes = dtype == HEADLOSS_FP32 ? 8 : 4;
+    const int budget = h->smem_optin - smem_fixed_bytes(acc_bytes);
+    static const int kClusters[] = {1, 2, 4, 8};
+    Plan pl;
+    for (int ci = 0; ci < 4 && pl.C == 0; ++ci) {
+        const int C = kClusters[ci];
+        if (h->forced_C && C != h->forced_C) continue;
+        int64_t L = (V + C - 1) / C;
+        L = (L + epw - 1) / epw * epw;
+        if (C > 1 && (C - 1) * L >= V && !h->forced_C) continue;  // an idle CTA: take a smaller C
+        const int64_t words = L / epw + 2;
+        const int64_t stage = words * 16 * ops;
+        int64_t nbuf = budget / stage;
+        if (nbuf > MAX_STAGES) nbuf = MAX_STAGES;
+        if (h->forced_nbuf) {
+            if (nbuf < h->forced_nbuf) continue;
+            nbuf = h->forced_nbuf;
+        }
+        if (nbuf < 2) continue;
+        pl.C = C;
+        pl.L = L;
+        pl.words = int(words);
+        pl.nbuf = int(nbuf);
+        pl.smem = int(stage * nbuf) + smem_fixed_bytes(acc_bytes);
+    }
+    if (pl.C == 0) return HEADLOSS_ERR_SIZE;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem) !=
+        cudaSuccess)
+        return HEADLOSS_ERR_CUDA;
+    int ncl = 0;
+    if (pl.C == 1) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, THREADS, pl.smem) !=
+            cudaSuccess)
+            return HEADLOSS_ERR_CUDA;
+        ncl = per_sm * h->num_sms;
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = pl.C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(pl.C * h->num_sms, 1, 1);
+        cfg.blockDim = dim3(THREADS, 1, 1);
+        cfg.dynamicSmemBytes = pl.smem;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&ncl, kernel, &cfg) != cudaSuccess)
+            return HEADLOSS_ERR_CUDA;
+    }
+    if (ncl < 1) return HEADLOSS_ERR_SIZE;
+    if (ncl > h->partials_cap) ncl = h->partials_cap;
+    pl.ncl = ncl;
+    pl.V = V;
+    pl.dtype = dtype;
+    pl.feat = feat;
+    pl.kernel = kernel;
+    h->plan = pl;
+    *out = pl;
+    return HEADLOSS_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int headloss_version(void) { return 1; }
+
+int headloss_launches_per_call(void) { return kLaunchesPerCall; }
+
+const char* headloss_strerror(int status) {
+    switch (status) {
+        case HEADLOSS_OK: return "ok";
+        case HEADLOSS_ERR_ARG: return "invalid argument";
+        case HEADLOSS_ERR_DTYPE: return "unsupported dtype";
+        case HEADLOSS_ERR_ALIGN: return "logits, teacher or gradient base is not 16-byte aligned";
+        case HEADLOSS_ERR_MISSING_INPUT: return "a selected loss is missing a required input";
+        case HEADLOSS_ERR_CUDA: return "CUDA runtime error";
+        case HEADLOSS_ERR_TIMEOUT: return "device: a bounded wait for a row copy gave up";
+        case HEADLOSS_ERR_LABEL_RANGE: return "device: label >= V (row treated as masked)";
+        case HEADLOSS_ERR_SIZE: return "vocabulary row too large for the on-chip plan";
+        default: return "unknown status";
+    }
+}
+
+int headloss_create(uint32_t flags, const headloss_weights* w, float temperature, float clip_eps,
+                    float softcap, float logits_scale, headloss_t* out) {
+    if (!out) return HEADLOSS_ERR_ARG;
+    *out = nullptr;
+    if (flags == 0 || (flags & ~kAllFlags)) return HEADLOSS_ERR_ARG;
+    if (!(temperature > 0.f) || !isfinite(temperature)) return HEADLOSS_ERR_ARG;
+    if (!(clip_eps >= 0.f) || !isfinite(clip_eps)) return HEADLOSS_ERR_ARG;
+    if (!(softcap >= 0.f) || !isfinite(softcap)) return HEADLOSS_ERR_ARG;
+    if (!(logits_scale > 0.f) || !isfinite(logits_scale)) return HEADLOSS_ERR_ARG;
+    headloss_weights ww = {0.f, 0.f, 0.f, 0.f, 0.f, 1.f, 0.f, 1.f};
+    ww.ce = 1.f;
+    if (w) ww = *w;
+    const float wl[8] = {ww.ce, ww.z, ww.dist_ce, ww.fkl, ww.rkl, ww.grpo, ww.entropy, ww.grad_scale};
+    for (float v : wl)
+        if (!isfinite(v)) return HEADLOSS_ERR_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return HEADLOSS_ERR_CUDA;
+    int sms = 0, optin = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return HEADLOSS_ERR_CUDA;
+    headloss* h = new (std::nothrow) headloss();
+    if (!h) return HEADLOSS_ERR_ARG;
+    h->flags = flags;
+    h->w = ww;
+    h->T = temperature;
+    h->eps = clip_eps;
+    h->softcap = softcap;
+    h->s = logits_scale;
+    h->device = dev;
+    h->num_sms = sms;
+    h->smem_optin = optin;
+    h->partials_cap = 4 * sms;
+    const size_t pbytes = size_t(h->partials_cap) * NACC * sizeof(double);
+    if (cudaMalloc(&h->ws, pbytes + 256) != cudaSuccess) {
+        delete h;
+        return HEADLOSS_ERR_CUDA;
+    }
+    h->partials = static_cast<double*>(h->ws);
+    h->n_valid = reinterpret_cast<long long*>(static_cast<char*>(h->ws) + pbytes);
+    h->err = reinterpret_cast<int*>(static_cast<char*>(h->ws) + pbytes + 64);
+    if (cudaMemset(h->ws, 0, pbytes + 256) != cudaSuccess) {
+        cudaFree(h->ws);
+        delete h;
+        return HEADLOSS_ERR_CUDA;
+    }
+    *out = h;
+    return HEADLOSS_OK;
+}
+
+void headloss_destroy(headloss_t h) {
+    if (!h) return;
+    cudaFree(h->ws);
+    delete h;
+}
+
+int headloss_force_plan(headloss_t h, int cluster, int stages) {
+    if (!h) return HEADLOSS_ERR_ARG;
+    if (!(cluster == 0 || cluster == 1 || cluster == 2 || cluster == 4 || cluster == 8))
+        return HEADLOSS_ERR_ARG;
+    if (!(stages == 0 || (stages >= 2 && stages <= MAX_STAGES))) return HEADLOSS_ERR_ARG;
+    std::lock_guard<std::mutex> g(h->mu);
+    h->forced_C = cluster;
+    h->forced_nbuf = stages;
+    h->plan = Plan();
+    return HEADLOSS_OK;
+}
+
+int headloss_plan(headloss_t h, int64_t V, int dtype, int* cluster, int* stages, int* ctas,
+                  int* threads, int* smem_bytes) {
+    if (!h || V < 1 || V >= (int64_t(1) << 31)) return HEADLOSS_ERR_ARG;
+    if (dtype < 0 || dtype > 2) return HEADLOSS_ERR_DTYPE;
+    std::lock_guard<std::mutex> g(h->mu);
+    Plan pl;
+    const int rc = make_plan(h, V, dtype, &pl);
+    if (rc) return rc;
+    if (cluster) *cluster = pl.C;
+    if (stages) *stages = pl.nbuf;
+    if (ctas) *ctas = pl.ncl * pl.C;
+    if (threads) *threads = THREADS;
+    if (smem_bytes) *smem_bytes = pl.smem;
+    return HEADLOSS_OK;
+}
+
+int headloss_forward_backward(headloss_t h, const void* logits, int64_t N, int64_t V, int dtype,
+                              const int64_t* labels, const void* teacher_logits,
+                              const float* old_logprobs, const float* advantages, void* grad_out,
+                              float* scalars_out, headloss_stream_t stream) {
+    if (!h || !scalars_out || N < 0 || V < 1 || V >= (int64_t(1) << 31)) return HEADLOSS_ERR_ARG;
+    if (N > 0 && !logits) return HEADLOSS_ERR_ARG;
+    if (dtype < 0 || dtype > 2) return HEADLOSS_ERR_DTYPE;
+    const uint32_t f = h->flags;
+    if (N > 0) {  // an empty batch reads no input
+        if ((f & (L_CE | L_GRPO | L_GRPO_STATS)) && !labels) return HEADLOSS_ERR_MISSING_INPUT;
+        if ((f & (L_DIST_CE | L_FKL | L_RKL)) && !teacher_logits)
+            return HEADLOSS_ERR_MISSING_INPUT;
+        if ((f & (L_GRPO | L_GRPO_STATS)) && (!old_logprobs || !advantages))
+            return HEADLOSS_ERR_MISSING_INPUT;
+    }
+    const bool teach = (f & (L_DIST_CE | L_FKL | L_RKL)) != 0;
+    if (!aligned16(logits) || (teach && !aligned16(teacher_logits)) ||
+        (grad_out && !aligned16(grad_out)))
+        return HEADLOSS_ERR_ALIGN;
+    if (teach && grad_out) {  // the gradient may alias the logits, never the teacher
+        const char* g0 = static_cast<const char*>(grad_out);
+        const char* t0 = static_cast<const char*>(teacher_logits);
+        const int64_t bytes = N * V * elem_size(dtype);
+        if (g0 < t0 + bytes && t0 < g0 + bytes) return HEADLOSS_ERR_ARG;
+    }
+    std::lock_guard<std::mutex> g(h->mu);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return HEADLOSS_ERR_CUDA;
+    if (dev != h->device) return HEADLOSS_ERR_ARG;
+    Plan pl;
+    const int rc = make_plan(h, V, dtype, &pl);
+    if (rc) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    count_valid_kernel<<<1, 1024, 0, s>>>(labels, N, V, h->n_valid, h->err);
+
+    int ncl = 0;
+    if (N > 0) {
+        ncl = int(N < pl.ncl ? N : pl.ncl);
+        Params p;
+        p.x = logits;
+        p.t = teach ? teacher_logits : nullptr;
+        p.g = grad_out;
+        p.labels = labels;
+        p.old_lp = (f & (L_GRPO | L_GRPO_STATS)) ? old_logprobs : nullptr;
+        p.adv = (f & (L_GRPO | L_GRPO_STATS)) ? advantages : nullptr;
+        p.N = N;
+        p.V = V;
+        p.L = pl.L;
+        p.C = pl.C;
+        p.nbuf = pl.nbuf;
+        p.words = pl.words;
+        p.flags = f;
+        p.s = h->s;
+        p.softcap = h->softcap;
+        p.T = h->T;
+        p.eps = h->eps;
+        p.w_ce = h->w.ce;
+        p.w_z = h->w.z;
+        p.w_dce = h->w.dist_ce;
+        p.w_fkl = h->w.fkl;
+        p.w_rkl = h->w.rkl;
+        p.w_grpo = h->w.grpo;
+        p.w_ent = h->w.entropy;
+        p.grad_scale = h->w.grad_scale;
+        p.partials = h->partials;
+        p.n_valid = h->n_valid;
+        p.err = h->err;
+
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = pl.C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(ncl * pl.C, 1, 1);
+        cfg.blockDim = dim3(THREADS, 1, 1);
+        cfg.dynamicSmemBytes = pl.smem;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = pl.C > 1 ? 1 : 0;
+        void* args[] = {&p};
+        if (cudaLaunchKernelExC(&cfg, pl.kernel, args) != cudaSuccess) return HEADLOSS_ERR_CUDA;
+    }
+    FinalizeArgs fa;
+    fa.flags = f;
+    fa.w_ce = h->w.ce;
+    fa.w_z = h->w.z;
+    fa.w_dce = h->w.dist_ce;
+    fa.w_fkl = h->w.fkl;
+    fa.w_rkl = h->w.rkl;
+    fa.w_grpo = h->w.grpo;
+    fa.w_ent = h->w.entropy;
+    finalize_kernel<<<1, 32, 0, s>>>(h->partials, ncl, h->n_valid, fa, scalars_out);
+    if (cudaGetLastError() != cudaSuccess) return HEADLOSS_ERR_CUDA;
+    return HEADLOSS_OK;
+}
+
+int headloss_get_device_error(headloss_t h, headloss_stream_t stream, int* err) {
+    if (!h || !err) return HEADLOSS_ERR_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return HEADLOSS_ERR_CUDA;
+    if (cudaMemcpy(&v, h->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return HEADLOSS_ERR_CUDA;
+    if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess) return HEADLOSS_ERR_CUDA;
+    *err = (v & E_LABEL) ? HEADLOSS_ERR_LABEL_RANGE
+                         : ((v & E_TIMEOUT) ? HEADLOSS_ERR_TIMEOUT : HEADLOSS_OK);
+    return HEADLOSS_OK;
+}
+
+}  // extern "C"

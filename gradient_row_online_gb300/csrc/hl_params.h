@@ -1,0 +1,60 @@
+// hl_params.h -- launch parameters shared by the host planner and the kernels.
+#pragma once
+#include <stdint.h>
+
+namespace hl {
+
+// Compile-time feature set of one row-kernel instantiation.
+enum : int {
+    F_TEACH = 1,    // teacher row + student-at-temperature sums (DIST_CE / FKL / RKL)
+    F_RKL = 2,      // reverse-KL sum and its log-ratio gradient term
+    F_ENT = 4,      // entropy sum (metric and/or gradient)
+    F_SOFTCAP = 8,  // z = s * c * tanh(x / c)
+};
+
+// Loss / metric bits (values match enum headloss_flag).
+enum : uint32_t {
+    L_CE = 1u, L_Z = 2u, L_DIST_CE = 4u, L_FKL = 8u, L_RKL = 16u,
+    L_GRPO = 32u, L_GRPO_STATS = 64u, L_ENTROPY = 128u,
+};
+
+// Device error bits (read back by headloss_get_device_error).
+enum : int { E_LABEL = 1, E_TIMEOUT = 2 };
+
+constexpr int THREADS = 512;
+constexpr int NWARPS = THREADS / 32;
+constexpr int MAX_CLUSTER = 8;
+constexpr int MAX_STAGES = 4;
+
+// Partial-statistics record one CTA contributes for one row (all base-2
+// units; see the row kernel for definitions).
+enum Rec { R_ZM, R_UM, R_S, R_E, R_ST, R_SQ, R_EQ, R_XP, R_Y, R_ZY, R_HASY, NREC };
+
+// Per-cluster partial sums over its rows (fp64), reduced by the finalize kernel.
+enum Acc {
+    A_CE, A_Z, A_DCE, A_FKL, A_RKL, A_GRPO, A_LP, A_RATIO, A_KL3, A_ADV, A_ADV2,
+    A_ENT, A_NVALID, A_NCLIP, NACC_USED
+};
+constexpr int NACC = 16;
+
+struct Params {
+    const void* x;         // N x V logits
+    const void* t;         // N x V teacher logits (or null)
+    void* g;               // N x V gradient (or null)
+    const int64_t* labels; // N (or null)
+    const float* old_lp;   // N (or null)
+    const float* adv;      // N (or null)
+    int64_t N, V;
+    int64_t L;             // columns per CTA slice (multiple of 16 bytes' worth)
+    int C;                 // CTAs per cluster (one row per cluster)
+    int nbuf;              // row stages buffered per CTA
+    int words;             // 16-byte words per operand stage buffer
+    uint32_t flags;
+    float s, softcap, T, eps;
+    float w_ce, w_z, w_dce, w_fkl, w_rkl, w_grpo, w_ent, grad_scale;
+    double* partials;              // [clusters][NACC]
+    const long long* n_valid;      // valid-row count of this call
+    int* err;                      // device error word
+};
+
+}  // namespace hl

@@ -1,0 +1,29 @@
+// hl_rows_bf16.cu -- row-kernel instantiations for bf16 logits (one per feature set).
+#include "hl_rows_kernel.cuh"
+
+namespace hl {
+
+#define HL_CASE(F) \
+    case F: return reinterpret_cast<const void*>(&rows_kernel<__nv_bfloat16, F>);
+
+const void* rows_kernel_bf16(int feat) {
+    switch (feat) {
+        HL_CASE(0)
+        HL_CASE(F_ENT)
+        HL_CASE(F_TEACH)
+        HL_CASE(F_TEACH | F_ENT)
+        HL_CASE(F_TEACH | F_RKL)
+        HL_CASE(F_TEACH | F_RKL | F_ENT)
+        HL_CASE(F_SOFTCAP)
+        HL_CASE(F_SOFTCAP | F_ENT)
+        HL_CASE(F_SOFTCAP | F_TEACH)
+        HL_CASE(F_SOFTCAP | F_TEACH | F_ENT)
+        HL_CASE(F_SOFTCAP | F_TEACH | F_RKL)
+        HL_CASE(F_SOFTCAP | F_TEACH | F_RKL | F_ENT)
+        default: return nullptr;
+    }
+}
+
+#undef HL_CASE
+
+}  // namespace hl

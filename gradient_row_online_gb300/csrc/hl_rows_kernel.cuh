@@ -1,0 +1,340 @@
+// hl_rows_kernel.cuh -- the persistent cluster-per-row kernel (see hl_rows.cuh
+// for the row pipeline and the sources it follows).
+#pragma once
+#include "hl_rows.cuh"
+
+namespace hl {
+
+template <typename DT, int FEAT>
+__global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant__ Params p) {
+    using Tr = DTraits<DT>;
+    using A = typename Tr::acc;
+    constexpr int EPW = Tr::EPW;
+    constexpr int ES = Tr::ES;
+    constexpr bool TEACH = (FEAT & F_TEACH) != 0;
+    constexpr bool RKL = (FEAT & F_RKL) != 0;
+    constexpr bool ENT = (FEAT & F_ENT) != 0;
+    constexpr bool CAP = (FEAT & F_SOFTCAP) != 0;
+    constexpr int OPS = TEACH ? 2 : 1;
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int W = p.words;
+    const uint32_t opbytes = uint32_t(W) * 16u;
+    const uint32_t stage_bytes = opbytes * OPS;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(stage_bytes) * p.nbuf);
+    double* acc = reinterpret_cast<double*>(bars + MAX_STAGES);  // [NACC], thread 0 of rank 0
+    A* xch = reinterpret_cast<A*>(acc + NACC);          // [2][MAX_CLUSTER][NREC]
+    A* red = xch + 2 * MAX_CLUSTER * NREC;              // [NWARPS][NREC]
+    A* coef = red + NWARPS * NREC;                      // [16]
+
+    const int C = p.C;
+    uint32_t rank, cid, ncl;
+    if (C > 1) {
+        rank = cluster_ctarank();
+        cid = cluster_id_x();
+        ncl = ncluster_x();
+    } else {
+        rank = 0;
+        cid = blockIdx.x;
+        ncl = gridDim.x;
+    }
+    const int64_t N = p.N, V = p.V;
+    const int64_t col0 = int64_t(rank) * p.L;
+    const int64_t col1 = col0 + p.L < V ? col0 + p.L : V;
+    const DT* __restrict__ xg = static_cast<const DT*>(p.x);
+    const DT* __restrict__ tg = static_cast<const DT*>(p.t);
+    DT* gg = static_cast<DT*>(p.g);
+
+    const A LOG2E = A(1.4426950408889634);
+    const A s = A(p.s);
+    const A K = s * LOG2E;                                 // zs = x * K (no softcap)
+    const A invc = CAP ? A(1) / A(p.softcap) : A(0);
+    const A Kc = CAP ? s * A(p.softcap) * LOG2E : A(0);    // zs = tanh(x / c) * Kc
+    const A invT = A(1) / A(p.T);
+    const A KT = LOG2E * invT;                             // us = t * KT
+
+    auto zs_of = [&](A v) -> A { return CAP ? mul_rn(tnh(v * invc), Kc) : mul_rn(v, K); };
+
+    if (tid == 0) {
+        for (int b = 0; b < p.nbuf; ++b) mbar_init(smem_addr(&bars[b]), 1);
+        fence_mbar_init();
+        for (int i = 0; i < NACC; ++i) acc[i] = 0.0;
+    }
+    __syncthreads();
+    if (C > 1) cluster_barrier();  // every peer has started before any DSMEM store
+
+    // Producer (thread 0): start the copies of local iteration `it` into its stage.
+    auto issue = [&](int it) {
+        const int64_t r = int64_t(cid) + int64_t(it) * ncl;
+        if (r >= N) return;
+        const int st = it % p.nbuf;
+        const uint32_t bar = smem_addr(&bars[st]);
+        const int64_t e0 = r * V + col0, e1 = r * V + col1;
+        int64_t f0 = (e0 + EPW - 1) / EPW * EPW, f1 = e1 / EPW * EPW;
+        const uint32_t bytes = (e1 > e0 && f1 > f0) ? uint32_t((f1 - f0) * ES) : 0u;
+        fence_proxy_async();  // order earlier generic stores to this stage before the copy
+        mbar_arrive_expect_tx(bar, bytes * OPS);
+        if (bytes) {
+            const uint32_t dst = smem_addr(smem + size_t(st) * stage_bytes) +
+                                 uint32_t((f0 / EPW - e0 / EPW) * 16);
+            bulk_g2s(dst, xg + f0, bytes, bar);
+            if (TEACH) bulk_g2s(dst + opbytes, tg + f0, bytes, bar);
+        }
+    };
+    if (tid == 0)
+        for (int it = 0; it < p.nbuf; ++it) issue(it);
+
+    const bool has_labels = p.labels != nullptr;
+    const bool need_side = (p.flags & (L_GRPO | L_GRPO_STATS)) != 0;
+    int xc = 0;             // exchanges done (parity of the exchange buffer)
+    uint32_t lost = 0, lost_par = 0;  // stages (and phase parities) whose wait gave up
+
+    // Side inputs of the next row are loaded one iteration ahead.
+    int64_t y_next = 0;
+    float o_next = 0.f, a_next = 0.f;
+    if (int64_t(cid) < N) {
+        if (has_labels) y_next = p.labels[cid];
+        if (need_side) {
+            o_next = p.old_lp[cid];
+            a_next = p.adv[cid];
+        }
+    }
+
+    for (int it = 0;; ++it) {
+        const int64_t r = int64_t(cid) + int64_t(it) * ncl;
+        if (r >= N) break;
+        const int64_t y = y_next;
+        const float old_lp = o_next, adv = a_next;
+        {
+            const int64_t rn = r + ncl;
+            if (rn < N) {
+                if (has_labels) y_next = p.labels[rn];
+                if (need_side) {
+                    o_next = p.old_lp[rn];
+                    a_next = p.adv[rn];
+                }
+            }
+        }
+        const bool valid = !has_labels || (y >= 0 && y < V);
+        if (has_labels && y >= V && rank == 0 && tid == 0) atomicOr(p.err, E_LABEL);
+
+        const int st = it % p.nbuf;
+        const uint32_t par = uint32_t(it / p.nbuf) & 1u;
+        if (!mbar_wait_bounded(smem_addr(&bars[st]), par)) {
+            lost |= 1u << st;
+            lost_par = (lost_par & ~(1u << st)) | (par << st);
+            if (tid == 0) atomicOr(p.err, E_TIMEOUT);
+        }
+        unsigned char* xs_b = smem + size_t(st) * stage_bytes;
+        DT* xs = reinterpret_cast<DT*>(xs_b);
+        DT* ts = reinterpret_cast<DT*>(xs_b + opbytes);
+
+        const int64_t e0 = r * V + col0, e1 = r * V + col1;
+        const bool nonempty = e1 > e0;
+        const int64_t wf = e0 / EPW;
+        const int nw = nonempty ? int((e1 + EPW - 1) / EPW - wf) : 0;
+
+        if (valid && nonempty) {
+            // Elements of partial 16-byte words at the slice ends (rows whose
+            // byte length is not a multiple of 16) come in with plain loads.
+            const int64_t f0 = (e0 + EPW - 1) / EPW * EPW, f1 = e1 / EPW * EPW;
+            const int64_t head_end = e1 < f0 ? e1 : f0;
+            const int64_t tail_start = f1 > head_end ? f1 : head_end;
+            const int nh = int(head_end - e0), nt = int(e1 - tail_start);
+            if (nh + nt > 0) {
+                if (tid < nh + nt) {
+                    const int64_t e = tid < nh ? e0 + tid : tail_start + (tid - nh);
+                    xs[e - wf * EPW] = xg[e];
+                    if (TEACH) ts[e - wf * EPW] = tg[e];
+                }
+                __syncthreads();
+            }
+        }
+
+        if (valid) {
+            // ---- pass A: slice max of raw student / teacher logits ----
+            A mx[2] = {A(-CUDART_INF), A(-CUDART_INF)};
+            for (int w = tid; w < nw; w += THREADS) {
+                const int64_t eb = (wf + w) * EPW;
+                const bool full = eb >= e0 && eb + EPW <= e1;
+                A v[EPW];
+                Tr::unpack(*reinterpret_cast<const uint4*>(xs_b + size_t(w) * 16), v);
+#pragma unroll
+                for (int i = 0; i < EPW; ++i)
+                    if (full || (eb + i >= e0 && eb + i < e1)) mx[0] = amax(mx[0], v[i]);
+                if (TEACH) {
+                    Tr::unpack(*reinterpret_cast<const uint4*>(xs_b + opbytes + size_t(w) * 16), v);
+#pragma unroll
+                    for (int i = 0; i < EPW; ++i)
+                        if (full || (eb + i >= e0 && eb + i < e1)) mx[1] = amax(mx[1], v[i]);
+                }
+            }
+            block_max<A, 2>(mx, red, lane, warp);
+            if (tid == 0) {
+                coef[0] = nonempty ? zs_of(mx[0]) : A(-CUDART_INF);
+                coef[1] = (TEACH && nonempty) ? mul_rn(mx[1], KT) : A(-CUDART_INF);
+            }
+            __syncthreads();
+            const A zm = coef[0], um = coef[1];
+
+            // ---- pass B: exponent sums relative to the slice max ----
+            // S = sum 2^d, E = sum 2^d d (d = zs - zm); ST = sum 2^(d/T);
+            // Sq = sum 2^du, Eq = sum 2^du du (du = us - um);
+            // Xp = sum 2^du (du - d/T);  Y = -sum 2^(d/T) (du - d/T).
+            A sm[7] = {A(0), A(0), A(0), A(0), A(0), A(0), A(0)};
+            for (int w = tid; w < nw; w += THREADS) {
+                const int64_t eb = (wf + w) * EPW;
+                const bool full = eb >= e0 && eb + EPW <= e1;
+                A v[EPW], u[EPW];
+                Tr::unpack(*reinterpret_cast<const uint4*>(xs_b + size_t(w) * 16), v);
+                if (TEACH)
+                    Tr::unpack(*reinterpret_cast<const uint4*>(xs_b + opbytes + size_t(w) * 16), u);
+#pragma unroll
+                for (int i = 0; i < EPW; ++i) {
+                    if (!(full || (eb + i >= e0 && eb + i < e1))) continue;
+                    const A d = sub_rn(zs_of(v[i]), zm);
+                    const A e = ex2(d);
+                    sm[0] += e;
+                    if (ENT) sm[1] += e * d;
+                    if (TEACH) {
+                        const A dT = d * invT;
+                        const A eT = ex2(dT);
+                        const A du = sub_rn(mul_rn(u[i], KT), um);
+                        const A eq = ex2(du);
+                        const A wd = du - dT;
+                        sm[2] += eT;
+                        sm[3] += eq;
+                        sm[4] += eq * du;
+                        sm[5] += eq * wd;
+                        if (RKL) sm[6] -= eT * wd;
+                    }
+                }
+            }
+            block_sum<A, 7>(sm, red, lane, warp);
+            A* myrec = xch + ((xc & 1) * MAX_CLUSTER + rank) * NREC;
+            if (tid == 0) {
+                A rec[NREC];
+                rec[R_ZM] = zm;
+                rec[R_UM] = um;
+                rec[R_S] = sm[0];
+                rec[R_E] = sm[1];
+                rec[R_ST] = sm[2];
+                rec[R_SQ] = sm[3];
+                rec[R_EQ] = sm[4];
+                rec[R_XP] = sm[5];
+                rec[R_Y] = sm[6];
+                rec[R_ZY] = A(0);
+                rec[R_HASY] = A(0);
+                if (has_labels && y >= col0 && y < col1) {
+                    const int64_t ey = r * V + y;
+                    rec[R_ZY] = zs_of(Tr::to_acc(xs[ey - wf * EPW]));
+                    rec[R_HASY] = A(1);
+                }
+                if (C > 1) {
+                    const uint32_t a0 = smem_addr(myrec);
+                    for (int k = 0; k < C; ++k) {
+                        const uint32_t ra = map_peer(a0, uint32_t(k));
+#pragma unroll
+                        for (int i = 0; i < NREC; ++i) st_peer(ra + i * sizeof(A), rec[i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < NREC; ++i) myrec[i] = rec[i];
+                }
+            }
+            if (C > 1) cluster_barrier();
+            if (tid == 0) {
+                row_epilogue<A, TEACH, RKL, ENT, CAP>(p, xch + (xc & 1) * MAX_CLUSTER * NREC, C,
+                                                      rank == 0, old_lp, adv, acc, coef);
+            }
+            ++xc;
+            __syncthreads();
+        }
+
+        // ---- pass C: the combined gradient, written once ----
+        if (gg != nullptr) {
+            A lse2 = 0, lseT2 = 0, lsq2 = 0, pc = 0, ps = 0, tc = 0, ts_ = 0, qc = 0, bc = 0;
+            if (valid) {
+                lse2 = coef[K_LSE2];
+                lseT2 = coef[K_LSET2];
+                lsq2 = coef[K_LSQ2];
+                pc = coef[K_PC];
+                ps = coef[K_PS];
+                tc = coef[K_TC];
+                ts_ = coef[K_TS];
+                qc = coef[K_QC];
+                bc = coef[K_BC];
+            }
+            const A dlse = lseT2 - lsq2;
+            const int64_t ey = (has_labels && valid && y >= col0 && y < col1) ? r * V + y : -1;
+            for (int w = tid; w < nw; w += THREADS) {
+                const int64_t eb = (wf + w) * EPW;
+                const bool full = eb >= e0 && eb + EPW <= e1;
+                A gv[EPW];
+                if (valid) {
+                    A v[EPW], u[EPW];
+                    Tr::unpack(*reinterpret_cast<const uint4*>(xs_b + size_t(w) * 16), v);
+                    if (TEACH)
+                        Tr::unpack(*reinterpret_cast<const uint4*>(xs_b + opbytes + size_t(w) * 16),
+                                   u);
+#pragma unroll
+                    for (int i = 0; i < EPW; ++i) {
+                        A zs, dz = A(1);
+                        if (CAP) {
+                            const A th = tnh(v[i] * invc);
+                            zs = th * Kc;
+                            dz = s - s * th * th;
+                        } else {
+                            zs = v[i] * K;
+                        }
+                        const A arg = zs - lse2;
+                        A gz = ex2(arg) * (ENT ? pc + ps * arg : pc);
+                        if (TEACH) {
+                            const A argT = zs * invT - lseT2;
+                            const A argq = u[i] * KT - lsq2;
+                            A tcoef = tc;
+                            if (RKL) {
+                                // log2 pT - log2 q from the logit difference,
+                                // one rounding at its own scale
+                                const A dxu = CAP ? (zs - u[i] * LOG2E) * invT
+                                                  : fma(v[i], s, -u[i]) * KT;
+                                tcoef = fma(ts_, dxu - dlse, tc);
+                            }
+                            gz += ex2(argT) * tcoef + qc * ex2(argq);
+                        }
+                        if (eb + i == ey) gz -= bc;
+                        gv[i] = CAP ? gz * dz : gz;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < EPW; ++i) gv[i] = A(0);
+                }
+                if (full) {
+                    *reinterpret_cast<uint4*>(gg + eb) = Tr::pack(gv);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < EPW; ++i)
+                        if (eb + i >= e0 && eb + i < e1) gg[eb + i] = Tr::from_acc(gv[i]);
+                }
+            }
+        }
+        __syncthreads();  // every thread is done with this stage
+        if (tid == 0) issue(it + p.nbuf);
+    }
+
+    // A stage whose wait gave up may still receive its copy: wait for it once
+    // more (bounded) before the CTA's shared memory goes away.
+    if (lost && tid == 0) {
+        for (int b = 0; b < p.nbuf; ++b)
+            if (lost & (1u << b)) (void)mbar_wait_bounded(smem_addr(&bars[b]), (lost_par >> b) & 1u);
+    }
+    if (rank == 0 && tid == 0) {
+        double* out = p.partials + size_t(cid) * NACC;
+#pragma unroll
+        for (int i = 0; i < NACC; ++i) out[i] = acc[i];
+    }
+    if (C > 1) cluster_barrier();  // no CTA leaves while a peer may still address it
+}
+
+}  // namespace hl

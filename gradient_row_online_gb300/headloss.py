@@ -1,0 +1,243 @@
+"""Thin Python binding of the C ABI in include/headloss.h (ctypes).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libheadloss.so.  Tensors are passed as raw device pointers; torch
+is used for device memory and streams.  There is no fallback: if the library
+is not built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libheadloss.so")
+
+# enum headloss_flag
+HEADLOSS_CE = 1 << 0
+HEADLOSS_Z = 1 << 1
+HEADLOSS_DIST_CE = 1 << 2
+HEADLOSS_FKL = 1 << 3
+HEADLOSS_RKL = 1 << 4
+HEADLOSS_GRPO = 1 << 5
+HEADLOSS_GRPO_STATS = 1 << 6
+HEADLOSS_ENTROPY = 1 << 7
+
+# enum headloss_dtype
+HEADLOSS_FP32, HEADLOSS_BF16, HEADLOSS_FP16 = 0, 1, 2
+
+# enum headloss_status
+STATUS = {0: "HEADLOSS_OK", 1: "HEADLOSS_ERR_ARG", 2: "HEADLOSS_ERR_DTYPE",
+          3: "HEADLOSS_ERR_ALIGN", 4: "HEADLOSS_ERR_MISSING_INPUT", 5: "HEADLOSS_ERR_CUDA",
+          6: "HEADLOSS_ERR_TIMEOUT", 7: "HEADLOSS_ERR_LABEL_RANGE", 8: "HEADLOSS_ERR_SIZE"}
+HEADLOSS_OK = 0
+HEADLOSS_ERR_ARG = 1
+HEADLOSS_ERR_DTYPE = 2
+HEADLOSS_ERR_ALIGN = 3
+HEADLOSS_ERR_MISSING_INPUT = 4
+HEADLOSS_ERR_CUDA = 5
+HEADLOSS_ERR_TIMEOUT = 6
+HEADLOSS_ERR_LABEL_RANGE = 7
+HEADLOSS_ERR_SIZE = 8
+
+# enum headloss_slot
+SLOTS = ("total", "ce", "z", "dist_ce", "fkl", "rkl", "grpo_loss", "new_logprob_mean",
+         "ratio_mean", "clip_frac", "kl_k3", "adv_mean", "adv_std", "entropy_mean", "n_valid",
+         "n_clipped")
+
+# Every function declared in include/headloss.h.
+EXPORTS = ("headloss_create", "headloss_forward_backward", "headloss_get_device_error",
+           "headloss_plan", "headloss_force_plan", "headloss_launches_per_call",
+           "headloss_destroy", "headloss_strerror", "headloss_version")
+
+
+class headloss_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_float) for n in
+                ("ce", "z", "dist_ce", "fkl", "rkl", "grpo", "entropy", "grad_scale")]
+
+
+class HeadlossError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({_strerror(status)})")
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libheadloss.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with gradient_row_online_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.headloss_create.argtypes = [ctypes.c_uint32, ctypes.POINTER(headloss_weights),
+                                    ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                    ctypes.c_float, ctypes.POINTER(vp)]
+    lib.headloss_create.restype = i32
+    lib.headloss_forward_backward.argtypes = [vp, vp, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp]
+    lib.headloss_forward_backward.restype = i32
+    lib.headloss_get_device_error.argtypes = [vp, vp, ip]
+    lib.headloss_get_device_error.restype = i32
+    lib.headloss_plan.argtypes = [vp, i64, i32, ip, ip, ip, ip, ip]
+    lib.headloss_plan.restype = i32
+    lib.headloss_force_plan.argtypes = [vp, i32, i32]
+    lib.headloss_force_plan.restype = i32
+    lib.headloss_launches_per_call.argtypes = []
+    lib.headloss_launches_per_call.restype = i32
+    lib.headloss_destroy.argtypes = [vp]
+    lib.headloss_destroy.restype = None
+    lib.headloss_strerror.argtypes = [i32]
+    lib.headloss_strerror.restype = ctypes.c_char_p
+    lib.headloss_version.argtypes = []
+    lib.headloss_version.restype = i32
+    _lib = lib
+    return lib
+
+
+def _strerror(status: int) -> str:
+    try:
+        return load_library().headloss_strerror(status).decode()
+    except Exception:
+        return "?"
+
+
+def _check(status: int, where: str):
+    if status != HEADLOSS_OK:
+        raise HeadlossError(status, where)
+
+
+def _ptr(a):
+    """Device address of a tensor (or an int address, or None)."""
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    return a.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        try:
+            import torch
+            return torch.cuda.current_stream().cuda_stream
+        except Exception:
+            return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def dtype_code(torch_dtype) -> int:
+    import torch
+    return {torch.float32: HEADLOSS_FP32, torch.bfloat16: HEADLOSS_BF16,
+            torch.float16: HEADLOSS_FP16}[torch_dtype]
+
+
+def make_weights(ce=1.0, z=0.0, dist_ce=0.0, fkl=0.0, rkl=0.0, grpo=1.0, entropy=0.0,
+                 grad_scale=1.0) -> headloss_weights:
+    return headloss_weights(ce, z, dist_ce, fkl, rkl, grpo, entropy, grad_scale)
+
+
+def headloss_create(flags: int, weights=None, temperature: float = 1.0, clip_eps: float = 0.2,
+                    softcap: float = 0.0, logits_scale: float = 1.0) -> int:
+    lib = load_library()
+    if isinstance(weights, dict):
+        weights = make_weights(**weights)
+    h = ctypes.c_void_p()
+    w = ctypes.byref(weights) if weights is not None else None
+    _check(lib.headloss_create(flags, w, temperature, clip_eps, softcap, logits_scale,
+                               ctypes.byref(h)), "headloss_create")
+    return h.value
+
+
+def headloss_forward_backward(h, logits, N, V, dtype, labels, teacher_logits, old_logprobs,
+                              advantages, grad_out, scalars_out, stream=None) -> None:
+    lib = load_library()
+    _check(lib.headloss_forward_backward(h, _ptr(logits), int(N), int(V), int(dtype),
+                                         _ptr(labels), _ptr(teacher_logits), _ptr(old_logprobs),
+                                         _ptr(advantages), _ptr(grad_out), _ptr(scalars_out),
+                                         _stream(stream)), "headloss_forward_backward")
+
+
+def headloss_get_device_error(h, stream=None) -> int:
+    lib = load_library()
+    e = ctypes.c_int()
+    _check(lib.headloss_get_device_error(h, _stream(stream), ctypes.byref(e)),
+           "headloss_get_device_error")
+    return e.value
+
+
+def headloss_plan(h, V: int, dtype: int) -> dict:
+    lib = load_library()
+    vals = [ctypes.c_int() for _ in range(5)]
+    _check(lib.headloss_plan(h, int(V), int(dtype), *[ctypes.byref(v) for v in vals]),
+           "headloss_plan")
+    return dict(zip(("cluster", "stages", "ctas", "threads", "smem_bytes"),
+                    (v.value for v in vals)))
+
+
+def headloss_force_plan(h, cluster: int, stages: int) -> None:
+    _check(load_library().headloss_force_plan(h, int(cluster), int(stages)),
+           "headloss_force_plan")
+
+
+def headloss_launches_per_call() -> int:
+    return load_library().headloss_launches_per_call()
+
+
+def headloss_destroy(h) -> None:
+    if h:
+        load_library().headloss_destroy(h)
+
+
+def headloss_strerror(status: int) -> str:
+    return load_library().headloss_strerror(int(status)).decode()
+
+
+def headloss_version() -> int:
+    return load_library().headloss_version()
+
+
+class HeadLoss:
+    """A handle plus the call on torch tensors (same semantics as the C ABI)."""
+
+    def __init__(self, flags: int, weights=None, temperature: float = 1.0,
+                 clip_eps: float = 0.2, softcap: float = 0.0, logits_scale: float = 1.0):
+        self.flags = flags
+        self.h = headloss_create(flags, weights, temperature, clip_eps, softcap, logits_scale)
+
+    def __call__(self, logits, labels=None, teacher_logits=None, old_logprobs=None,
+                 advantages=None, grad_out=None, scalars_out=None, stream=None):
+        import torch
+        N, V = logits.shape
+        if scalars_out is None:
+            scalars_out = torch.empty(16, dtype=torch.float32, device=logits.device)
+        headloss_forward_backward(self.h, logits, N, V, dtype_code(logits.dtype), labels,
+                                  teacher_logits, old_logprobs, advantages, grad_out,
+                                  scalars_out, stream)
+        return scalars_out
+
+    def plan(self, V: int, dtype: int) -> dict:
+        return headloss_plan(self.h, V, dtype)
+
+    def force_plan(self, cluster: int, stages: int) -> None:
+        headloss_force_plan(self.h, cluster, stages)
+
+    def device_error(self, stream=None) -> int:
+        return headloss_get_device_error(self.h, stream)
+
+    def close(self):
+        if self.h:
+            headloss_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

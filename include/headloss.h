@@ -1,0 +1,194 @@
+/*
+ * headloss.h -- C ABI of the fused language-model head loss (GB300, sm_103a).
+ *
+ * One call reads each token row of vocabulary logits, computes its softmax
+ * statistics once, and shares them across every requested loss and metric:
+ * label cross-entropy, z-loss, distillation (from-distribution CE, forward KL,
+ * reverse KL, with temperature), the GRPO clipped objective with its
+ * ratio / KL / clamp / advantage statistics, and entropy.  In the same pass it
+ * writes one combined logits gradient and every requested scalar.
+ *
+ * Source of the operation (ServiceNow Fast-LLM pages):
+ *   - issue #507 "Monolithic fused head-loss kernel", Problem / Proposed
+ *     direction: a flag set of losses and metrics, one softmax, all scalars
+ *     and the combined gradient in one pass;
+ *   - PR #549 "Monolithic fused head-loss kernel (torch.compile)", Approach
+ *     and Loss coverage: the loss set, one logits scale per softmax, fp32
+ *     gradient accumulation cast to the logits dtype once;
+ *   - PR #558 "Triton monolithic kernel", Design: the gradient is a per-row
+ *     superposition  grad_j = prob_coeff * softmax_j - label_coeff * delta(j, label),
+ *     extended here by a teacher term and a reverse-KL log-ratio term;
+ *     Validation: masking, logit / gradient scaling, softcap, metrics without
+ *     gradient.
+ *
+ * Conventions shared by every entry point:
+ *   - Every call returns an int status (HEADLOSS_OK == 0).  On any error no
+ *     device work has been enqueued and no output was touched.
+ *   - The caller owns every buffer.  All data pointers are DEVICE pointers of
+ *     the current CUDA device.
+ *   - headloss_forward_backward is asynchronous on `stream`: it never
+ *     synchronises the host and never allocates.  Results are valid after the
+ *     stream is synchronised.
+ *   - One handle may be used by one stream at a time (it owns a small
+ *     workspace for per-cluster partial sums).
+ */
+#ifndef HEADLOSS_H
+#define HEADLOSS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same layout as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* headloss_stream_t;
+
+typedef struct headloss* headloss_t;
+
+/* Logits dtype: the teacher logits and the gradient have the same dtype. */
+enum headloss_dtype { HEADLOSS_FP32 = 0, HEADLOSS_BF16 = 1, HEADLOSS_FP16 = 2 };
+
+/* Loss / metric selection.  A flag selects EMISSION of the scalar; the
+ * matching weight selects its GRADIENT contribution (weight 0 = metric only,
+ * PR #558 "metrics-without-gradient"). */
+enum headloss_flag {
+    HEADLOSS_CE = 1u << 0,          /* label cross-entropy, lse - z[label] */
+    HEADLOSS_Z = 1u << 1,           /* z-loss, lse^2 */
+    HEADLOSS_DIST_CE = 1u << 2,     /* -sum_j q_j log pT_j (teacher q, student pT at T) */
+    HEADLOSS_FKL = 1u << 3,         /* KL(q || pT) */
+    HEADLOSS_RKL = 1u << 4,         /* KL(pT || q) */
+    HEADLOSS_GRPO = 1u << 5,        /* -min(rho A, clip(rho, 1-eps, 1+eps) A) */
+    HEADLOSS_GRPO_STATS = 1u << 6,  /* new_logprob / ratio / clip / KL / advantage stats */
+    HEADLOSS_ENTROPY = 1u << 7      /* H(p) of the student softmax */
+};
+
+enum headloss_status {
+    HEADLOSS_OK = 0,
+    HEADLOSS_ERR_ARG = 1,           /* bad size, flag, weight, temperature, ... */
+    HEADLOSS_ERR_DTYPE = 2,         /* dtype not one of enum headloss_dtype */
+    HEADLOSS_ERR_ALIGN = 3,         /* a logits / teacher / gradient base not 16-byte aligned */
+    HEADLOSS_ERR_MISSING_INPUT = 4, /* a flag's required input pointer is NULL */
+    HEADLOSS_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+    HEADLOSS_ERR_TIMEOUT = 6,       /* device: a bounded wait for a row copy gave up */
+    HEADLOSS_ERR_LABEL_RANGE = 7,   /* device: a label >= V (that row was treated as masked) */
+    HEADLOSS_ERR_SIZE = 8           /* V too large for the on-chip row plan of this dtype/flag set */
+};
+
+/* Loss weights.  grad_scale multiplies the whole gradient (the incoming
+ * gradient of the total loss); it does not scale the emitted scalars. */
+typedef struct {
+    float ce, z, dist_ce, fkl, rkl, grpo, entropy, grad_scale;
+} headloss_weights;
+
+/* Scalar slots of scalars_out (16 floats).  Means are over valid rows.
+ * Slots of losses / metrics not selected by the flags are written 0. */
+enum headloss_slot {
+    HEADLOSS_SLOT_TOTAL = 0,        /* sum over selected losses of weight * mean */
+    HEADLOSS_SLOT_CE = 1,
+    HEADLOSS_SLOT_Z = 2,
+    HEADLOSS_SLOT_DIST_CE = 3,
+    HEADLOSS_SLOT_FKL = 4,
+    HEADLOSS_SLOT_RKL = 5,
+    HEADLOSS_SLOT_GRPO = 6,
+    HEADLOSS_SLOT_NEW_LOGPROB = 7,  /* mean of z[label] - lse */
+    HEADLOSS_SLOT_RATIO = 8,        /* mean of rho = exp(new - old log-prob) */
+    HEADLOSS_SLOT_CLIP_FRAC = 9,    /* fraction of rows with |rho - 1| > eps */
+    HEADLOSS_SLOT_KL_K3 = 10,       /* mean of rho - 1 - log rho */
+    HEADLOSS_SLOT_ADV_MEAN = 11,
+    HEADLOSS_SLOT_ADV_STD = 12,     /* population standard deviation */
+    HEADLOSS_SLOT_ENTROPY = 13,
+    HEADLOSS_SLOT_N_VALID = 14,     /* exact integer (exact while < 2^24) */
+    HEADLOSS_SLOT_N_CLIPPED = 15    /* exact integer (exact while < 2^24) */
+};
+
+/*
+ * headloss_create -- validate a loss set and build a handle.
+ *
+ * flags:        OR of enum headloss_flag (at least one bit; unknown bits -> ERR_ARG).
+ * w:            weights (NULL = all loss weights 0 except ce = grpo = 1, grad_scale = 1).
+ *               A weight of a loss whose flag is not set is ignored.
+ * temperature:  T > 0, divides student AND teacher logits for the three
+ *               distillation losses only (PR #549 "Bundled fix": the
+ *               distillation temperature is honoured).
+ * clip_eps:     GRPO epsilon >= 0 (symmetric clip).
+ * softcap:      c >= 0; c > 0 applies z = c * tanh(x / c) before the scale.
+ * logits_scale: s > 0; the student softmax sees z = s * softcap(x) (PR #549
+ *               Approach: one softmax, one logits_scale_factor).
+ * out:          receives the handle.
+ *
+ * Allocates the handle's workspace on the current device (the only
+ * allocation this library makes).  Errors: ERR_ARG, ERR_CUDA.
+ */
+int headloss_create(uint32_t flags, const headloss_weights* w, float temperature,
+                    float clip_eps, float softcap, float logits_scale, headloss_t* out);
+
+/*
+ * headloss_forward_backward -- one fused pass over N rows of V logits.
+ *
+ * logits:         N x V, row-major, contiguous, `dtype`; base 16-byte aligned
+ *                 (rows need not be: a row whose bytes are not a multiple of 16
+ *                 is handled with element-wise edges).
+ * labels:         N int64 (NULL = no labels: every row valid; CE / GRPO /
+ *                 GRPO_STATS then return ERR_MISSING_INPUT).  label < 0 masks
+ *                 the row for every loss and metric: its gradient row is
+ *                 written as exact +0 and it is not counted.  label >= V is a
+ *                 device error (ERR_LABEL_RANGE via headloss_get_device_error)
+ *                 and that row is treated as masked.
+ * teacher_logits: N x V, same layout and dtype (required by DIST_CE / FKL /
+ *                 RKL, else ignored).
+ * old_logprobs:   N fp32 old-policy log-probs of the label (GRPO, GRPO_STATS).
+ * advantages:     N fp32 per-token advantages (GRPO, GRPO_STATS).
+ * grad_out:       N x V, `dtype`, 16-byte aligned, or NULL for metrics only.
+ *                 It may equal `logits` (in-place); it must not overlap the
+ *                 teacher.  Written: d(grad_scale * total) / d logits, where
+ *                 total = sum_k weight_k * mean_over_valid_rows(loss_k).
+ * scalars_out:    16 fp32 (enum headloss_slot).
+ * stream:         CUDA stream for all device work.
+ *
+ * N == 0 is valid (no input is read; every scalar is written 0).
+ *
+ * Errors (host-side, nothing enqueued): ERR_ARG (N < 0, V < 1, V >= 2^31,
+ * null handle / scalars_out, null logits with N > 0), ERR_DTYPE, ERR_ALIGN,
+ * ERR_MISSING_INPUT (N > 0 only), ERR_SIZE, ERR_CUDA (launch failure).
+ */
+int headloss_forward_backward(headloss_t h, const void* logits, int64_t N, int64_t V, int dtype,
+                              const int64_t* labels, const void* teacher_logits,
+                              const float* old_logprobs, const float* advantages,
+                              void* grad_out, float* scalars_out, headloss_stream_t stream);
+
+/*
+ * headloss_get_device_error -- synchronise `stream`, then read and clear the
+ * handle's device error word.  *err receives HEADLOSS_OK, ERR_LABEL_RANGE or
+ * ERR_TIMEOUT (the first of those raised since the last read).
+ */
+int headloss_get_device_error(headloss_t h, headloss_stream_t stream, int* err);
+
+/*
+ * headloss_plan -- the launch plan a call with (V, dtype) would use:
+ * cluster size (CTAs sharing one row), row stages buffered per CTA, CTAs
+ * launched, threads per CTA, dynamic shared memory per CTA.  Any pointer may
+ * be NULL.  Errors: ERR_ARG, ERR_DTYPE, ERR_SIZE, ERR_CUDA.
+ */
+int headloss_plan(headloss_t h, int64_t V, int dtype, int* cluster, int* stages, int* ctas,
+                  int* threads, int* smem_bytes);
+
+/*
+ * headloss_force_plan -- pin the cluster size (1, 2, 4 or 8) and the stage
+ * count (2..4) for later calls on this handle, or 0 / 0 for the automatic
+ * plan.  For tests and tuning.  A later call whose rows do not fit the pinned
+ * plan returns ERR_SIZE.
+ */
+int headloss_force_plan(headloss_t h, int cluster, int stages);
+
+/* Kernel launches one headloss_forward_backward call enqueues (constant). */
+int headloss_launches_per_call(void);
+
+void headloss_destroy(headloss_t h);
+const char* headloss_strerror(int status);
+int headloss_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HEADLOSS_H */

@@ -124,8 +124,9 @@ int64_t oracle_count_valid(const int64_t* labels, int64_t n_rows) {
  * masks the row.  inv_n = 1 / (valid rows of the whole call).
  * rec: RF_COUNT fields.  grad (nullable): dL/dx for this row, where
  * L = grad_scale * sum_k w_k * mean_over_valid_rows(loss_k).
- * gmag (nullable): sum over loss terms of |term| in dL/dx, the scale at which
- * a rounding error of a superposed gradient lives.
+ * gmag (nullable): the size of the quantities dL/dx is computed from (sum over
+ * loss terms of |term|, where a factor that is itself a difference counts its
+ * parts): the scale at which rounding error of a superposed gradient lives.
  */
 static void oracle_row(const oracle_cfg* cfg, int64_t V, const double* x, int64_t label,
                        int has_labels, const double* t, double old_lp, double adv,
@@ -228,33 +229,57 @@ static void oracle_row(const oracle_cfg* cfg, int64_t V, const double* x, int64_
     const double T = cfg->temperature;
     for (int64_t j = 0; j < V; ++j) {
         const double delta = (has_labels && j == label) ? 1.0 : 0.0;
-        double terms[8];
+        /* terms[i]: one loss's contribution; mags[i]: the size of the
+         * quantities it is computed from (a factor that is itself a
+         * difference, like log pT - log q - RKL, counts its parts) */
+        double terms[8], mags[8];
         int nt = 0;
         /* CE: d(lse - z_y)/dz_j = p_j - delta */
-        if (f & OR_CE) terms[nt++] = k * cfg->w_ce * (p[j] - delta);
+        if (f & OR_CE) {
+            terms[nt] = k * cfg->w_ce * (p[j] - delta);
+            mags[nt++] = fabs(k * cfg->w_ce) * (p[j] + delta);
+        }
         /* z-loss: d(lse^2)/dz_j = 2 lse p_j */
-        if (f & OR_Z) terms[nt++] = k * cfg->w_z * 2.0 * lse * p[j];
+        if (f & OR_Z) {
+            terms[nt] = k * cfg->w_z * 2.0 * lse * p[j];
+            mags[nt] = fabs(terms[nt]);
+            ++nt;
+        }
         /* from-distribution CE: d(-sum_i q_i log pT_i)/dz_j = (pT_j - q_j) / T */
-        if (f & OR_DIST_CE) terms[nt++] = k * cfg->w_dist_ce * (pT[j] - q[j]) / T;
+        if (f & OR_DIST_CE) {
+            terms[nt] = k * cfg->w_dist_ce * (pT[j] - q[j]) / T;
+            mags[nt++] = fabs(k * cfg->w_dist_ce / T) * (pT[j] + q[j]);
+        }
         /* forward KL: sum q log q does not depend on z, same derivative */
-        if (f & OR_FKL) terms[nt++] = k * cfg->w_fkl * (pT[j] - q[j]) / T;
+        if (f & OR_FKL) {
+            terms[nt] = k * cfg->w_fkl * (pT[j] - q[j]) / T;
+            mags[nt++] = fabs(k * cfg->w_fkl / T) * (pT[j] + q[j]);
+        }
         /* reverse KL: d/dz_j sum_i pT_i (log pT_i - log q_i)
          *           = pT_j (log pT_j - log q_j - RKL) / T */
         if (f & OR_RKL) {
             const double log_pT = zT[j] - lse_T, log_q = u[j] - lsq;
-            terms[nt++] = k * cfg->w_rkl * pT[j] * (log_pT - log_q - rkl) / T;
+            terms[nt] = k * cfg->w_rkl * pT[j] * (log_pT - log_q - rkl) / T;
+            mags[nt++] = fabs(k * cfg->w_rkl * pT[j] / T) *
+                         (fabs(log_pT) + fabs(log_q) + fabs(rkl));
         }
         /* GRPO: d loss/d rho = -A (unclipped branch) or 0; d rho/d lp = rho;
          * d lp/dz_j = delta - p_j */
-        if (f & OR_GRPO) terms[nt++] = k * cfg->w_grpo * (-adv * act) * rho * (delta - p[j]);
+        if (f & OR_GRPO) {
+            terms[nt] = k * cfg->w_grpo * (-adv * act) * rho * (delta - p[j]);
+            mags[nt++] = fabs(k * cfg->w_grpo * adv * act * rho) * (delta + p[j]);
+        }
         /* entropy: dH/dz_j = -p_j (log p_j + H) */
-        if (f & OR_ENTROPY) terms[nt++] = k * cfg->w_entropy * (-p[j] * ((z[j] - lse) + H));
+        if (f & OR_ENTROPY) {
+            terms[nt] = k * cfg->w_entropy * (-p[j] * ((z[j] - lse) + H));
+            mags[nt++] = fabs(k * cfg->w_entropy * p[j]) * (fabs(z[j] - lse) + fabs(H));
+        }
 
         const double dzdx = transform_deriv(cfg, x[j]);
         double g = 0.0, mag = 0.0;
         for (int i = 0; i < nt; ++i) {
             g += terms[i];
-            mag += fabs(terms[i]);
+            mag += mags[i];
         }
         if (grad) grad[j] = g * dzdx;
         if (gmag) gmag[j] = mag * fabs(dzdx);

@@ -1,0 +1,205 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs.  Small cases compare every output element; the full-size
+workloads compare every scalar over all rows and the gradient on sampled
+rows, in the launch configuration the benchmark times."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from gradient_row_online_gb300 import headloss as hlb
+from gradient_row_online_gb300 import workloads as W
+from tests import _harness as H
+
+pytestmark = pytest.mark.gpu
+
+ALL_LOSSES = ("ce", "z", "dist_ce", "fkl", "rkl", "grpo", "grpo_stats", "entropy")
+FULL_W = dict(ce=0.9, z=0.3, dist_ce=0.4, fkl=0.6, rkl=0.7, grpo=1.1, entropy=0.5,
+              grad_scale=1.3)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    hlb.load_library()
+
+
+def small(losses, N=33, V=257, dtype=torch.bfloat16, **kw):
+    base = W.Workload("small", N, V, dtype, tuple(losses), dict(FULL_W), sigma=3.0,
+                      mask_frac=0.2, teacher_noise=1.0, temperature=1.7, clip_eps=0.2)
+    return base.replace(**kw) if kw else base
+
+
+def full_check(wl, plan=None, inplace=False):
+    inp = W.make_inputs(wl, "cuda")
+    ref_inp = dict(inp, logits=inp["logits"].clone()) if inplace else inp
+    got, g, _ = H.run_gpu(wl, inp, plan=plan, inplace=inplace)
+    cfg, rec, ref, gmag = H.oracle_rows(wl, ref_inp)
+    H.check_scalars(wl, got, cfg, rec)
+    H.check_grad(wl, g, ref, gmag, rec)
+
+
+# ------------------------------------------------------------ small, every output
+
+def test_tiny_ce_z_fp32_workload():
+    full_check(W.WORKLOADS["tiny_ce_z_fp32"])
+
+
+SUBSETS = [c for r in range(1, 9) for c in itertools.combinations(ALL_LOSSES, r)]
+
+
+@pytest.mark.parametrize("softcap,scale", [(0.0, 1.0), (20.0, 0.6)])
+def test_every_loss_subset_bf16(softcap, scale):
+    for losses in SUBSETS:
+        full_check(small(losses, softcap=softcap, logits_scale=scale, seed=len(losses)))
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.float32])
+@pytest.mark.parametrize("losses", [("ce",), ("ce", "z"), ("grpo", "grpo_stats", "entropy"),
+                                    ("dist_ce", "fkl", "rkl"), ALL_LOSSES])
+def test_loss_sets_fp16_fp32(dtype, losses):
+    full_check(small(losses, dtype=dtype))
+    full_check(small(losses, dtype=dtype, softcap=15.0, logits_scale=1.3, seed=3))
+
+
+@pytest.mark.parametrize("V", [1, 2, 7, 8, 9, 1000, 1023, 1024, 32001])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_ragged_and_tiny_vocab(V, dtype):
+    full_check(small(ALL_LOSSES, N=19, V=V, dtype=dtype))
+
+
+@pytest.mark.parametrize("cluster,stages", [(1, 2), (2, 2), (2, 3), (4, 2), (8, 2), (8, 4)])
+def test_forced_cluster_plans(cluster, stages):
+    wl = small(ALL_LOSSES, N=40, V=20011, softcap=30.0, logits_scale=0.5)
+    full_check(wl, plan=(cluster, stages))
+    full_check(small(("ce", "z", "entropy"), N=40, V=8000, dtype=torch.float32),
+               plan=(cluster, stages))
+
+
+def test_large_logits_fp32():
+    wl = small(("ce", "z", "entropy", "fkl", "rkl"), N=8, V=513, dtype=torch.float32,
+               sigma=1e4)
+    full_check(wl)
+
+
+def test_in_place_gradient():
+    full_check(small(("ce", "z", "grpo", "grpo_stats", "entropy"), N=50, V=3000), inplace=True)
+
+
+def test_metrics_without_gradient_match_and_write_nothing():
+    wl = small(ALL_LOSSES, N=30, V=999, weights=dict(FULL_W, ce=0.0, grpo=0.0))
+    inp = W.make_inputs(wl, "cuda")
+    a, g, h = H.run_gpu(wl, inp, grad=True)
+    b, _, _ = H.run_gpu(wl, inp, grad=False, handle=h)
+    assert np.array_equal(a, b)
+    cfg, rec, ref, gmag = H.oracle_rows(wl, inp)
+    H.check_scalars(wl, b, cfg, rec)
+
+
+def test_deterministic_bitwise():
+    wl = small(ALL_LOSSES, N=300, V=4099, softcap=10.0)
+    inp = W.make_inputs(wl, "cuda")
+    a, ga, h = H.run_gpu(wl, inp)
+    b, gb, _ = H.run_gpu(wl, inp, handle=h)
+    assert np.array_equal(a, b)
+    assert torch.equal(ga.view(torch.int16), gb.view(torch.int16))
+
+
+def test_all_rows_masked_and_empty_batch():
+    wl = small(ALL_LOSSES, N=12, V=300, mask_frac=1.1)
+    inp = W.make_inputs(wl, "cuda")
+    got, g, h = H.run_gpu(wl, inp)
+    assert np.all(got == 0.0)
+    assert int(g.view(torch.int16).abs().max()) == 0
+    empty = {k: (None if v is None else v[:0]) for k, v in inp.items()}
+    out = torch.full((16,), 7.0, device="cuda")
+    h(empty["logits"], empty["labels"], empty["teacher"], empty["old_logprobs"],
+      empty["advantages"], empty["logits"], out)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0)
+
+
+def test_label_out_of_range_is_reported_and_masked():
+    wl = small(("ce", "z"), N=20, V=100, mask_frac=0.0)
+    inp = W.make_inputs(wl, "cuda")
+    inp["labels"][3] = 100
+    h = __import__("gradient_row_online_gb300").headloss_for(wl)
+    g = torch.empty_like(inp["logits"])
+    out = torch.empty(16, device="cuda")
+    h(inp["logits"], inp["labels"], None, None, None, g, out)
+    assert h.device_error() == hlb.HEADLOSS_ERR_LABEL_RANGE
+    assert h.device_error() == hlb.HEADLOSS_OK  # read clears it
+    assert int(g[3].view(torch.int16).abs().max()) == 0
+    assert out[14].item() == 19
+
+
+def test_host_side_argument_errors():
+    wl = small(ALL_LOSSES, N=4, V=64)
+    inp = W.make_inputs(wl, "cuda")
+    h = __import__("gradient_row_online_gb300").headloss_for(wl)
+    x, lab, t = inp["logits"], inp["labels"], inp["teacher"]
+    o, a = inp["old_logprobs"], inp["advantages"]
+    out = torch.empty(16, device="cuda")
+    fb = hlb.headloss_forward_backward
+    cases = [
+        (dict(teacher_logits=None), hlb.HEADLOSS_ERR_MISSING_INPUT),
+        (dict(labels=None), hlb.HEADLOSS_ERR_MISSING_INPUT),
+        (dict(old_logprobs=None), hlb.HEADLOSS_ERR_MISSING_INPUT),
+        (dict(logits=x.data_ptr() + 2), hlb.HEADLOSS_ERR_ALIGN),
+        (dict(grad_out=x.data_ptr() + 4), hlb.HEADLOSS_ERR_ALIGN),
+        (dict(grad_out=t), hlb.HEADLOSS_ERR_ARG),
+        (dict(dtype=7), hlb.HEADLOSS_ERR_DTYPE),
+        (dict(N=-1), hlb.HEADLOSS_ERR_ARG),
+        (dict(V=0), hlb.HEADLOSS_ERR_ARG),
+        (dict(scalars_out=None), hlb.HEADLOSS_ERR_ARG),
+    ]
+    for over, status in cases:
+        args = dict(h=h.h, logits=x, N=4, V=64, dtype=hlb.HEADLOSS_BF16, labels=lab,
+                    teacher_logits=t, old_logprobs=o, advantages=a, grad_out=None,
+                    scalars_out=out, stream=None)
+        args.update(over)
+        with pytest.raises(hlb.HeadlossError) as e:
+            fb(**args)
+        assert e.value.status == status, (over, e.value.status)
+
+
+def test_create_rejects_bad_configuration():
+    bad = [dict(flags=0), dict(flags=1 << 9), dict(temperature=0.0), dict(clip_eps=-1.0),
+           dict(softcap=-1.0), dict(logits_scale=0.0)]
+    for b in bad:
+        args = dict(flags=hlb.HEADLOSS_CE, weights=None, temperature=1.0, clip_eps=0.2,
+                    softcap=0.0, logits_scale=1.0)
+        args.update(b)
+        with pytest.raises(hlb.HeadlossError) as e:
+            hlb.headloss_create(**args)
+        assert e.value.status == hlb.HEADLOSS_ERR_ARG
+
+
+# ----------------------------------------------- full-size workloads (bench plan)
+
+FULL = ("ce_z_bf16", "ce_distill_bf16", "grpo_z_entropy_bf16", "all_in_bf16")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload(name):
+    wl = W.WORKLOADS[name]
+    inp = W.make_inputs(wl, "cuda")
+    got, g, h = H.run_gpu(wl, inp)
+    # every scalar over all rows (oracle without gradient)
+    cfg, rec, _, _ = H.oracle_rows(wl, inp, want_grad=False, want_gmag=False)
+    H.check_scalars(wl, got, cfg, rec)
+    # the gradient on sampled rows: first, last, masked, and a seeded spread
+    rng = np.random.default_rng(0)
+    labels = inp["labels"].cpu().numpy()
+    rows = set([0, 1, wl.N - 1]) | set(rng.choice(wl.N, 40, replace=False).tolist())
+    rows |= set(np.nonzero(labels < 0)[0][:4].tolist())
+    rows = np.array(sorted(rows))
+    _, srec, ref, gmag = H.oracle_rows(wl, inp, rows=rows)
+    sel = torch.as_tensor(rows, device="cuda")
+    H.check_grad(wl, g.index_select(0, sel), ref, gmag, srec)
+    del inp, g
+    torch.cuda.empty_cache()
