@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="all_in_bf16")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="use only the first ROWS tokens of the workload (profiling cases)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -175,6 +177,8 @@ def run_ours(args, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     wl = W.WORKLOADS[args.workload].replace(seed=rank)  # each rank its own batch
+    if args.rows:
+        wl = wl.replace(N=min(args.rows, wl.N))
     hlb.load_library()
     h = pkg.headloss_for(wl)
     inp = W.make_inputs(wl, dev)

@@ -155,10 +155,37 @@ const void* kernel_for(int dtype, int feat) {
     }
 }
 
+// Max co-resident clusters of `C` CTAs of `kernel` with `smem` bytes each.
+int active_clusters(const void* kernel, int C, int smem, int num_sms, int* out) {
+    if (C == 1) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, THREADS, smem) !=
+            cudaSuccess)
+            return HEADLOSS_ERR_CUDA;
+        *out = per_sm * num_sms;
+        return HEADLOSS_OK;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(C * num_sms, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(out, kernel, &cfg) != cudaSuccess) return HEADLOSS_ERR_CUDA;
+    return HEADLOSS_OK;
+}
+
 // Chooses the cluster size C (CTAs sharing one row), the column slice per
 // CTA, the number of row stages each CTA buffers, and the persistent grid.
-// Preference: the smallest cluster whose slice leaves room for at least two
-// stages (one computing, one or more in flight).
+// Every C in 1..8 whose slice leaves room for at least two stages (one
+// computing, one or more in flight) is a candidate; the plan with the most
+// co-resident CTAs wins (the GPCs of a GB300 fit 15 clusters of 8 but 28 of
+// 5), ties going to the smaller cluster.
 int make_plan(headloss* h, int64_t V, int dtype, Plan* out) {
     const int feat = feature_set(h);
     if (h->plan.V == V && h->plan.dtype == dtype && h->plan.feat == feat &&
@@ -174,14 +201,17 @@ int make_plan(headloss* h, int64_t V, int dtype, Plan* out) {
     const int ops = (feat & F_TEACH) ? 2 : 1;
     const int acc_bytes = dtype == HEADLOSS_FP32 ? 8 : 4;
     const int budget = h->smem_optin - smem_fixed_bytes(acc_bytes);
-    static const int kClusters[] = {1, 2, 4, 8};
-    Plan pl;
-    for (int ci = 0; ci < 4 && pl.C == 0; ++ci) {
-        const int C = kClusters[ci];
+    // the attribute is a per-kernel cap shared by every handle: always the device maximum
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             h->smem_optin) != cudaSuccess)
+        return HEADLOSS_ERR_CUDA;
+    Plan best;
+    int best_ctas = 0;
+    for (int C = 1; C <= MAX_CLUSTER; ++C) {
         if (h->forced_C && C != h->forced_C) continue;
         int64_t L = (V + C - 1) / C;
         L = (L + epw - 1) / epw * epw;
-        if (C > 1 && (C - 1) * L >= V && !h->forced_C) continue;  // an idle CTA: take a smaller C
+        if (C > 1 && (C - 1) * L >= V && !h->forced_C) continue;  // an idle CTA
         const int64_t words = L / epw + 2;
         const int64_t stage = words * 16 * ops;
         int64_t nbuf = budget / stage;
@@ -191,47 +221,30 @@ int make_plan(headloss* h, int64_t V, int dtype, Plan* out) {
             nbuf = h->forced_nbuf;
         }
         if (nbuf < 2) continue;
+        Plan pl;
         pl.C = C;
         pl.L = L;
         pl.words = int(words);
         pl.nbuf = int(nbuf);
         pl.smem = int(stage * nbuf) + smem_fixed_bytes(acc_bytes);
+        int ncl = 0;
+        const int rc = active_clusters(kernel, C, pl.smem, h->num_sms, &ncl);
+        if (rc) return rc;
+        if (ncl > h->partials_cap) ncl = h->partials_cap;
+        if (ncl < 1) continue;
+        pl.ncl = ncl;
+        if (ncl * C > best_ctas) {
+            best = pl;
+            best_ctas = ncl * C;
+        }
     }
-    if (pl.C == 0) return HEADLOSS_ERR_SIZE;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem) !=
-        cudaSuccess)
-        return HEADLOSS_ERR_CUDA;
-    int ncl = 0;
-    if (pl.C == 1) {
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, THREADS, pl.smem) !=
-            cudaSuccess)
-            return HEADLOSS_ERR_CUDA;
-        ncl = per_sm * h->num_sms;
-    } else {
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = pl.C;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(pl.C * h->num_sms, 1, 1);
-        cfg.blockDim = dim3(THREADS, 1, 1);
-        cfg.dynamicSmemBytes = pl.smem;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&ncl, kernel, &cfg) != cudaSuccess)
-            return HEADLOSS_ERR_CUDA;
-    }
-    if (ncl < 1) return HEADLOSS_ERR_SIZE;
-    if (ncl > h->partials_cap) ncl = h->partials_cap;
-    pl.ncl = ncl;
-    pl.V = V;
-    pl.dtype = dtype;
-    pl.feat = feat;
-    pl.kernel = kernel;
-    h->plan = pl;
-    *out = pl;
+    if (best.C == 0) return HEADLOSS_ERR_SIZE;
+    best.V = V;
+    best.dtype = dtype;
+    best.feat = feat;
+    best.kernel = kernel;
+    h->plan = best;
+    *out = best;
     return HEADLOSS_OK;
 }
 
@@ -318,8 +331,7 @@ void headloss_destroy(headloss_t h) {
 
 int headloss_force_plan(headloss_t h, int cluster, int stages) {
     if (!h) return HEADLOSS_ERR_ARG;
-    if (!(cluster == 0 || cluster == 1 || cluster == 2 || cluster == 4 || cluster == 8))
-        return HEADLOSS_ERR_ARG;
+    if (cluster < 0 || cluster > MAX_CLUSTER) return HEADLOSS_ERR_ARG;
     if (!(stages == 0 || (stages >= 2 && stages <= MAX_STAGES))) return HEADLOSS_ERR_ARG;
     std::lock_guard<std::mutex> g(h->mu);
     h->forced_C = cluster;

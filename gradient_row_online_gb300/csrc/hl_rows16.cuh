@@ -1,0 +1,582 @@
+// hl_rows16.cuh -- the row kernel for bf16 / fp16 logits (fp32 arithmetic).
+//
+// Same row pipeline as the generic kernel (hl_rows_kernel.cuh): a cluster
+// per row, each CTA a column slice resident in shared memory, the row read
+// from HBM once and the gradient written once.  This version is written for
+// issue throughput, which bounds the 16-bit path on GB300:
+//   - pass A takes the slice max on packed 16-bit pairs (one max per 2 elements);
+//   - passes B and C run on fp32 pairs (add / mul / fma .f32x2: one issued
+//     instruction per 2 elements) with single-instruction ex2 / rcp;
+//   - softcap's tanh comes from tanh(y) = 1 - 2 / (exp(2y) + 1) (ex2 + rcp),
+//   - 16-byte words wholly inside the slice take the packed path; only the
+//     (at most two) partial words at a ragged slice edge take a scalar path;
+//   - the C partial records of a row are merged by C lanes of warp 0 at once.
+#pragma once
+#include "hl_pack.cuh"
+#include "hl_rows.cuh"
+
+namespace hl {
+
+// Scalar twin of the packed element math, for the partial words.
+struct Scal {
+    __device__ static float tanh_a2x(float a2x) {
+        const float w = ex2f(a2x) + 1.f;
+        return fmaf(rcpf(w), -2.f, 1.f);
+    }
+};
+
+// Warp 0 merges the C records of a row (lane k holds record k), then lane 0
+// derives the row's losses and gradient coefficients.
+template <bool TEACH, bool RKL, bool ENT, bool CAP>
+__device__ void row_epilogue16(const Params& p, const float* recs, int C, bool accumulate,
+                               float old_lp, float adv, double* acc, float* coef, int lane) {
+    const float LN2 = 0.6931471805599453f;
+    const float invT = 1.f / p.T;
+    float r[NREC];
+    const bool have = lane < C;
+#pragma unroll
+    for (int i = 0; i < NREC; ++i) r[i] = have ? recs[lane * NREC + i] : 0.f;
+    const bool live = have && r[R_S] > 0.f;
+    float M = live ? r[R_ZM] : -CUDART_INF_F;
+    float Mu = (live && TEACH) ? r[R_UM] : -CUDART_INF_F;
+#pragma unroll
+    for (int o = 4; o; o >>= 1) {
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        if (TEACH) Mu = fmaxf(Mu, __shfl_xor_sync(0xffffffffu, Mu, o));
+    }
+    float c[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // S E ST Sq Eq Xp Y zy
+    if (live) {
+        const float d = r[R_ZM] - M;
+        const float al = exp2f(d);
+        c[0] = al * r[R_S];
+        if (ENT) c[1] = al * (r[R_E] + d * r[R_S]);
+        if (TEACH) {
+            const float dT = d * invT;
+            const float alT = exp2f(dT);
+            const float du = r[R_UM] - Mu;
+            const float be = exp2f(du);
+            c[2] = alT * r[R_ST];
+            c[3] = be * r[R_SQ];
+            c[4] = be * (r[R_EQ] + du * r[R_SQ]);
+            c[5] = be * (r[R_XP] + (du - dT) * r[R_SQ]);
+            if (RKL) c[6] = alT * (r[R_Y] - (du - dT) * r[R_ST]);
+        }
+    }
+    if (have && r[R_HASY] > 0.f) c[7] = r[R_ZY];
+#pragma unroll
+    for (int o = 4; o; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] += __shfl_xor_sync(0xffffffffu, c[i], o);
+    if (lane != 0) return;
+
+    const float S = c[0], E = c[1], ST = c[2], Sq = c[3], Eq = c[4], Xp = c[5], Y = c[6];
+    const float zy = c[7];
+    const uint32_t f = p.flags;
+    const float lS = log2f(S);
+    const float lse2 = M + lS;
+    const float lse = lse2 * LN2;
+    const float kk = float(double(p.grad_scale) / double(*p.n_valid));
+    float H = 0.f, lST = 0.f, lSq = 0.f, dce = 0.f, fkl = 0.f, rkl = 0.f;
+    if (ENT) H = LN2 * (lS - E / S);
+    if (TEACH) {
+        lST = log2f(ST);
+        lSq = log2f(Sq);
+        fkl = LN2 * (Xp / Sq - lSq + lST);
+        dce = LN2 * (Xp / Sq + lST - Eq / Sq);
+        if (RKL) rkl = LN2 * (Y / ST - lST + lSq);
+    }
+    float pc = 0.f, ps = 0.f, tc = 0.f, ts = 0.f, qc = 0.f, bc = 0.f;
+    if (f & L_CE) {
+        pc += kk * p.w_ce;
+        bc += kk * p.w_ce;
+    }
+    if (f & L_Z) pc += kk * p.w_z * 2.f * lse;
+    float lp = 0.f, rho = 0.f, grpo = 0.f, kl3 = 0.f;
+    bool clipped = false;
+    if (f & (L_GRPO | L_GRPO_STATS)) {
+        const float eps = p.eps;
+        lp = (zy - lse2) * LN2;
+        const float lr = lp - old_lp;
+        rho = expf(lr);
+        float rho_c = rho < 1.f - eps ? 1.f - eps : rho;
+        rho_c = rho_c > 1.f + eps ? 1.f + eps : rho_c;
+        const float unc = rho * adv, clp = rho_c * adv;
+        const float obj = unc < clp ? unc : clp;
+        const bool act = unc <= clp || (rho >= 1.f - eps && rho <= 1.f + eps);
+        grpo = -obj;
+        kl3 = rho - 1.f - lr;
+        clipped = fabsf(rho - 1.f) > eps;
+        if ((f & L_GRPO) && act) {
+            const float gco = kk * p.w_grpo * adv * rho;
+            pc += gco;
+            bc += gco;
+        }
+    }
+    if (ENT && (f & L_ENTROPY)) {
+        const float ec = kk * p.w_ent;
+        pc -= ec * H;
+        ps = -ec * LN2;
+    }
+    if (TEACH) {
+        float dc = 0.f;
+        if (f & L_DIST_CE) dc += p.w_dce;
+        if (f & L_FKL) dc += p.w_fkl;
+        dc *= kk * invT;
+        tc += dc;
+        qc -= dc;
+        if (RKL && (f & L_RKL)) {
+            const float rc = kk * invT * p.w_rkl;
+            tc -= rc * rkl;
+            ts = rc * LN2;
+        }
+    }
+    if (!CAP) {  // dz/dx = s: fold the chain rule into the coefficients
+        pc *= p.s;
+        ps *= p.s;
+        tc *= p.s;
+        ts *= p.s;
+        qc *= p.s;
+        bc *= p.s;
+    }
+    coef[K_LSE2] = lse2;
+    coef[K_LSET2] = TEACH ? M * invT + lST : 0.f;
+    coef[K_LSQ2] = TEACH ? Mu + lSq : 0.f;
+    coef[K_PC] = pc;
+    coef[K_PS] = ps;
+    coef[K_TC] = tc;
+    coef[K_TS] = ts;
+    coef[K_QC] = qc;
+    coef[K_BC] = bc;
+    if (accumulate) {
+        acc[A_NVALID] += 1.0;
+        if (f & L_CE) acc[A_CE] += double((lse2 - zy) * LN2);
+        if (f & L_Z) acc[A_Z] += double(lse) * double(lse);
+        if (f & L_DIST_CE) acc[A_DCE] += double(dce);
+        if (f & L_FKL) acc[A_FKL] += double(fkl);
+        if (f & L_RKL) acc[A_RKL] += double(rkl);
+        if (f & L_GRPO) acc[A_GRPO] += double(grpo);
+        if (f & L_GRPO_STATS) {
+            acc[A_LP] += double(lp);
+            acc[A_RATIO] += double(rho);
+            acc[A_KL3] += double(kl3);
+            acc[A_ADV] += double(adv);
+            acc[A_ADV2] += double(adv) * double(adv);
+            acc[A_NCLIP] += clipped ? 1.0 : 0.0;
+        }
+        if (f & L_ENTROPY) acc[A_ENT] += double(H);
+    }
+}
+
+template <typename DT, int FEAT>
+__global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constant__ Params p) {
+    using P16 = Pack16<DT>;
+    constexpr int EPW = 8;
+    constexpr int ES = 2;
+    constexpr bool TEACH = (FEAT & F_TEACH) != 0;
+    constexpr bool RKL = (FEAT & F_RKL) != 0;
+    constexpr bool ENT = (FEAT & F_ENT) != 0;
+    constexpr bool CAP = (FEAT & F_SOFTCAP) != 0;
+    constexpr int OPS = TEACH ? 2 : 1;
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int W = p.words;
+    const uint32_t opbytes = uint32_t(W) * 16u;
+    const uint32_t stage_bytes = opbytes * OPS;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(stage_bytes) * p.nbuf);
+    double* acc = reinterpret_cast<double*>(bars + MAX_STAGES);  // [NACC], rank 0 only
+    float* xch = reinterpret_cast<float*>(acc + NACC);         // [2][MAX_CLUSTER][NREC]
+    float* red = xch + 2 * MAX_CLUSTER * NREC;                   // [NWARPS][NREC]
+    float* coef = red + NWARPS * NREC;                           // [16]
+
+    const int C = p.C;
+    uint32_t rank, cid, ncl;
+    if (C > 1) {
+        rank = cluster_ctarank();
+        cid = cluster_id_x();
+        ncl = ncluster_x();
+    } else {
+        rank = 0;
+        cid = blockIdx.x;
+        ncl = gridDim.x;
+    }
+    const int64_t N = p.N, V = p.V;
+    const int64_t col0 = int64_t(rank) * p.L;
+    const int64_t col1 = col0 + p.L < V ? col0 + p.L : V;
+    const DT* __restrict__ xg = static_cast<const DT*>(p.x);
+    const DT* __restrict__ tg = static_cast<const DT*>(p.t);
+    DT* gg = static_cast<DT*>(p.g);
+
+    const float LOG2E = 1.4426950408889634f;
+    const float s = p.s;
+    const float K = s * LOG2E;                                // zs = x * K (no softcap)
+    const float A2 = CAP ? 2.f * LOG2E / p.softcap : 0.f;     // ex2 argument of tanh(x / c)
+    const float Kc = CAP ? s * p.softcap * LOG2E : 0.f;       // zs = tanh(x / c) * Kc
+    const float invT = 1.f / p.T;
+    const float KT = LOG2E * invT;                            // us = t * KT
+    const f2 K2 = pk1(K), A22 = pk1(A2), Kc2 = pk1(Kc), invT2 = pk1(invT), KT2 = pk1(KT);
+    const f2 z2 = pk1(0.f);
+
+    // zs of one value, and of a pair: the same operations in the same order.
+    auto zs1 = [&](float v) -> float {
+        return CAP ? __fmul_rn(Scal::tanh_a2x(__fmul_rn(v, A2)), Kc) : __fmul_rn(v, K);
+    };
+    auto zs2 = [&](f2 v) -> f2 {
+        return CAP ? mul2(tanh_from_ex2_arg(mul2(v, A22)), Kc2) : mul2(v, K2);
+    };
+
+    if (tid == 0) {
+        for (int b = 0; b < p.nbuf; ++b) mbar_init(smem_addr(&bars[b]), 1);
+        fence_mbar_init();
+        for (int i = 0; i < NACC; ++i) acc[i] = 0.0;
+    }
+    __syncthreads();
+    if (C > 1) cluster_barrier();  // every peer has started before any DSMEM store
+
+    auto issue = [&](int it) {
+        const int64_t r = int64_t(cid) + int64_t(it) * ncl;
+        if (r >= N) return;
+        const int st = it % p.nbuf;
+        const uint32_t bar = smem_addr(&bars[st]);
+        const int64_t e0 = r * V + col0, e1 = r * V + col1;
+        const int64_t f0 = (e0 + EPW - 1) / EPW * EPW, f1 = e1 / EPW * EPW;
+        const uint32_t bytes = (e1 > e0 && f1 > f0) ? uint32_t((f1 - f0) * ES) : 0u;
+        fence_proxy_async();
+        mbar_arrive_expect_tx(bar, bytes * OPS);
+        if (bytes) {
+            const uint32_t dst = smem_addr(smem + size_t(st) * stage_bytes) +
+                                 uint32_t((f0 / EPW - e0 / EPW) * 16);
+            bulk_g2s(dst, xg + f0, bytes, bar);
+            if (TEACH) bulk_g2s(dst + opbytes, tg + f0, bytes, bar);
+        }
+    };
+    if (tid == 0)
+        for (int it = 0; it < p.nbuf; ++it) issue(it);
+
+    const bool has_labels = p.labels != nullptr;
+    const bool need_side = (p.flags & (L_GRPO | L_GRPO_STATS)) != 0;
+    int xc = 0;
+    uint32_t lost = 0, lost_par = 0;
+    int64_t y_next = 0;
+    float o_next = 0.f, a_next = 0.f;
+    if (int64_t(cid) < N) {
+        if (has_labels) y_next = p.labels[cid];
+        if (need_side) {
+            o_next = p.old_lp[cid];
+            a_next = p.adv[cid];
+        }
+    }
+
+    for (int it = 0;; ++it) {
+        const int64_t r = int64_t(cid) + int64_t(it) * ncl;
+        if (r >= N) break;
+        const int64_t y = y_next;
+        const float old_lp = o_next, adv = a_next;
+        {
+            const int64_t rn = r + ncl;
+            if (rn < N) {
+                if (has_labels) y_next = p.labels[rn];
+                if (need_side) {
+                    o_next = p.old_lp[rn];
+                    a_next = p.adv[rn];
+                }
+            }
+        }
+        const bool valid = !has_labels || (y >= 0 && y < V);
+        if (has_labels && y >= V && rank == 0 && tid == 0) atomicOr(p.err, E_LABEL);
+
+        const int st = it % p.nbuf;
+        const uint32_t par = uint32_t(it / p.nbuf) & 1u;
+        if (!mbar_wait_bounded(smem_addr(&bars[st]), par)) {
+            lost |= 1u << st;
+            lost_par = (lost_par & ~(1u << st)) | (par << st);
+            if (tid == 0) atomicOr(p.err, E_TIMEOUT);
+        }
+        unsigned char* xs_b = smem + size_t(st) * stage_bytes;
+        uint16_t* xs = reinterpret_cast<uint16_t*>(xs_b);
+        uint16_t* ts = reinterpret_cast<uint16_t*>(xs_b + opbytes);
+
+        const int64_t e0 = r * V + col0, e1 = r * V + col1;
+        const bool nonempty = e1 > e0;
+        const int64_t wf = e0 / EPW;
+        const int nw = nonempty ? int((e1 + EPW - 1) / EPW - wf) : 0;
+        // words [wlo, whi) lie wholly inside the slice
+        const int wlo = (nonempty && (e0 % EPW) != 0) ? 1 : 0;
+        const int whi = (nonempty && (e1 % EPW) != 0) ? nw - 1 : nw;
+
+        if (valid && nonempty) {
+            const int64_t f0 = (e0 + EPW - 1) / EPW * EPW, f1 = e1 / EPW * EPW;
+            const int64_t head_end = e1 < f0 ? e1 : f0;
+            const int64_t tail_start = f1 > head_end ? f1 : head_end;
+            const int nh = int(head_end - e0), nt = int(e1 - tail_start);
+            if (nh + nt > 0) {
+                if (tid < nh + nt) {
+                    const int64_t e = tid < nh ? e0 + tid : tail_start + (tid - nh);
+                    xs[e - wf * EPW] = reinterpret_cast<const uint16_t*>(xg)[e];
+                    if (TEACH) ts[e - wf * EPW] = reinterpret_cast<const uint16_t*>(tg)[e];
+                }
+                __syncthreads();
+            }
+        }
+
+        if (valid) {
+            // ---- pass A: slice max on packed 16-bit pairs ----
+            float mx[2];
+            {
+                uint32_t mxx = P16::NEG_INF2, mxt = P16::NEG_INF2;
+                float sx = -CUDART_INF_F, stt = -CUDART_INF_F;
+                for (int w = tid; w < nw; w += THREADS) {
+                    if (w >= wlo && w < whi) {
+                        const uint4 a = *reinterpret_cast<const uint4*>(xs_b + size_t(w) * 16);
+                        mxx = P16::max2(P16::max2(mxx, a.x), P16::max2(a.y, a.z));
+                        mxx = P16::max2(mxx, a.w);
+                        if (TEACH) {
+                            const uint4 b = *reinterpret_cast<const uint4*>(xs_b + opbytes +
+                                                                            size_t(w) * 16);
+                            mxt = P16::max2(P16::max2(mxt, b.x), P16::max2(b.y, b.z));
+                            mxt = P16::max2(mxt, b.w);
+                        }
+                    } else {
+                        const int64_t eb = (wf + w) * EPW;
+                        for (int i = 0; i < EPW; ++i) {
+                            if (eb + i < e0 || eb + i >= e1) continue;
+                            sx = fmaxf(sx, P16::to_f(xs[w * EPW + i]));
+                            if (TEACH) stt = fmaxf(stt, P16::to_f(ts[w * EPW + i]));
+                        }
+                    }
+                }
+                float a, b;
+                upk(P16::unpack(mxx), a, b);
+                mx[0] = fmaxf(sx, fmaxf(a, b));
+                upk(P16::unpack(mxt), a, b);
+                mx[1] = fmaxf(stt, fmaxf(a, b));
+            }
+            block_max<float, 2>(mx, red, lane, warp);
+            if (tid == 0) {
+                coef[0] = nonempty ? zs1(mx[0]) : -CUDART_INF_F;
+                coef[1] = (TEACH && nonempty) ? __fmul_rn(mx[1], KT) : -CUDART_INF_F;
+            }
+            __syncthreads();
+            const float zm = coef[0], um = coef[1];
+            const f2 zm2 = pk1(zm), um2 = pk1(um);
+
+            // ---- pass B: exponent sums relative to the slice max ----
+            // S = sum 2^d, E = sum 2^d d (d = zs - zm); ST = sum 2^(d/T);
+            // Sq = sum 2^du, Eq = sum 2^du du (du = us - um);
+            // Xp = sum 2^du (du - d/T);  Y = -sum 2^(d/T) (du - d/T).
+            f2 S2 = z2, E2 = z2, ST2 = z2, Sq2 = z2, Eq2 = z2, Xp2 = z2, Y2 = z2;
+            float sS = 0.f, sE = 0.f, sST = 0.f, sSq = 0.f, sEq = 0.f, sXp = 0.f, sY = 0.f;
+            for (int w = tid; w < nw; w += THREADS) {
+                if (w >= wlo && w < whi) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(xs_b + size_t(w) * 16);
+                    uint4 b = make_uint4(0, 0, 0, 0);
+                    if (TEACH) b = *reinterpret_cast<const uint4*>(xs_b + opbytes + size_t(w) * 16);
+                    const uint32_t xa[4] = {a.x, a.y, a.z, a.w};
+                    const uint32_t tb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const f2 d = sub2(zs2(P16::unpack(xa[k])), zm2);
+                        const f2 e = ex2p(d);
+                        S2 = add2(S2, e);
+                        if (ENT) E2 = fma2(e, d, E2);
+                        if (TEACH) {
+                            const f2 dT = mul2(d, invT2);
+                            const f2 eT = ex2p(dT);
+                            ST2 = add2(ST2, eT);
+                            const f2 du = sub2(mul2(P16::unpack(tb[k]), KT2), um2);
+                            const f2 eq = ex2p(du);
+                            Sq2 = add2(Sq2, eq);
+                            Eq2 = fma2(eq, du, Eq2);
+                            const f2 wd = sub2(du, dT);
+                            Xp2 = fma2(eq, wd, Xp2);
+                            if (RKL) Y2 = fma2(eT, wd, Y2);
+                        }
+                    }
+                } else {
+                    const int64_t eb = (wf + w) * EPW;
+                    for (int i = 0; i < EPW; ++i) {
+                        if (eb + i < e0 || eb + i >= e1) continue;
+                        const float d = __fsub_rn(zs1(P16::to_f(xs[w * EPW + i])), zm);
+                        const float e = ex2f(d);
+                        sS += e;
+                        if (ENT) sE = fmaf(e, d, sE);
+                        if (TEACH) {
+                            const float dT = __fmul_rn(d, invT);
+                            const float eT = ex2f(dT);
+                            sST += eT;
+                            const float du =
+                                __fsub_rn(__fmul_rn(P16::to_f(ts[w * EPW + i]), KT), um);
+                            const float eq = ex2f(du);
+                            sSq += eq;
+                            sEq = fmaf(eq, du, sEq);
+                            const float wd = __fsub_rn(du, dT);
+                            sXp = fmaf(eq, wd, sXp);
+                            if (RKL) sY = fmaf(eT, wd, sY);
+                        }
+                    }
+                }
+            }
+            float sm[7] = {hsum(S2) + sS, hsum(E2) + sE, hsum(ST2) + sST, hsum(Sq2) + sSq,
+                           hsum(Eq2) + sEq, hsum(Xp2) + sXp, -(hsum(Y2) + sY)};
+            block_sum<float, 7>(sm, red, lane, warp);
+            // warp 0 now holds the CTA totals in every lane
+            float* myrec = xch + ((xc & 1) * MAX_CLUSTER + rank) * NREC;
+            if (warp == 0) {
+                float zyv = 0.f, hasy = 0.f;
+                if (has_labels && y >= col0 && y < col1) {
+                    zyv = zs1(P16::to_f(xs[r * V + y - wf * EPW]));
+                    hasy = 1.f;
+                }
+                const float rec[NREC] = {zm, um, sm[0], sm[1], sm[2], sm[3], sm[4], sm[5], sm[6],
+                                         zyv, hasy};
+                if (C > 1) {
+                    if (lane < C) {
+                        const uint32_t ra = map_peer(smem_addr(myrec), uint32_t(lane));
+#pragma unroll
+                        for (int i = 0; i < NREC; ++i) st_peer(ra + i * 4u, rec[i]);
+                    }
+                } else if (lane == 0) {
+#pragma unroll
+                    for (int i = 0; i < NREC; ++i) myrec[i] = rec[i];
+                }
+            }
+            if (C > 1) cluster_barrier();
+            else __syncwarp();
+            if (warp == 0)
+                row_epilogue16<TEACH, RKL, ENT, CAP>(p, xch + (xc & 1) * MAX_CLUSTER * NREC, C,
+                                                     rank == 0, old_lp, adv, acc, coef, lane);
+            ++xc;
+            __syncthreads();
+        }
+
+        // ---- pass C: the combined gradient, written once ----
+        if (gg != nullptr) {
+            float lse2 = 0.f, lseT2 = 0.f, lsq2 = 0.f, pc = 0.f, ps = 0.f, tc = 0.f, ts_ = 0.f,
+                  qc = 0.f, bc = 0.f;
+            if (valid) {
+                lse2 = coef[K_LSE2];
+                lseT2 = coef[K_LSET2];
+                lsq2 = coef[K_LSQ2];
+                pc = coef[K_PC];
+                ps = coef[K_PS];
+                tc = coef[K_TC];
+                ts_ = coef[K_TS];
+                qc = coef[K_QC];
+                bc = coef[K_BC];
+            }
+            const float dlse = lseT2 - lsq2;
+            const f2 nlse2 = pk1(-lse2), nlseT2 = pk1(-lseT2), nlsq2 = pk1(-lsq2);
+            const f2 pc2 = pk1(pc), ps2 = pk1(ps), tc2 = pk1(tc), ts2 = pk1(ts_), qc2 = pk1(qc);
+            const f2 s2 = pk1(s), ns2 = pk1(-s), ndlse2 = pk1(-dlse), L2E2 = pk1(LOG2E);
+            // word and element of the label column in this slice (or none)
+            const int64_t ey = (has_labels && valid && y >= col0 && y < col1) ? r * V + y : -1;
+            const int wy = ey >= 0 ? int(ey / EPW - wf) : -1;
+            const int iy = ey >= 0 ? int(ey % EPW) : 0;
+            for (int w = tid; w < nw; w += THREADS) {
+                const int64_t eb = (wf + w) * EPW;
+                if (!valid) {
+                    if (w >= wlo && w < whi) {
+                        *reinterpret_cast<uint4*>(gg + eb) = make_uint4(0, 0, 0, 0);
+                    } else {
+                        for (int i = 0; i < EPW; ++i)
+                            if (eb + i >= e0 && eb + i < e1)
+                                reinterpret_cast<uint16_t*>(gg)[eb + i] = 0;
+                    }
+                    continue;
+                }
+                if (w >= wlo && w < whi) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(xs_b + size_t(w) * 16);
+                    uint4 b = make_uint4(0, 0, 0, 0);
+                    if (TEACH) b = *reinterpret_cast<const uint4*>(xs_b + opbytes + size_t(w) * 16);
+                    const uint32_t xa[4] = {a.x, a.y, a.z, a.w};
+                    const uint32_t tb[4] = {b.x, b.y, b.z, b.w};
+                    uint32_t out[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const f2 xv = P16::unpack(xa[k]);
+                        f2 zs, dz = z2;
+                        if (CAP) {
+                            const f2 th = tanh_from_ex2_arg(mul2(xv, A22));
+                            zs = mul2(th, Kc2);
+                            dz = fma2(mul2(th, th), ns2, s2);
+                        } else {
+                            zs = mul2(xv, K2);
+                        }
+                        const f2 arg = add2(zs, nlse2);
+                        f2 g = mul2(ex2p(arg), ENT ? fma2(ps2, arg, pc2) : pc2);
+                        if (TEACH) {
+                            const f2 tv = P16::unpack(tb[k]);
+                            const f2 pT = ex2p(fma2(zs, invT2, nlseT2));
+                            const f2 q = ex2p(fma2(tv, KT2, nlsq2));
+                            f2 tco = tc2;
+                            if (RKL) {
+                                // log2 pT - log2 q from the logit difference
+                                const f2 dxu = CAP ? mul2(fma2(tv, pk1(-LOG2E), zs), invT2)
+                                                   : mul2(fma2(xv, s2, sub2(z2, tv)), KT2);
+                                tco = fma2(ts2, add2(dxu, ndlse2), tc2);
+                            }
+                            g = fma2(pT, tco, g);
+                            g = fma2(q, qc2, g);
+                        }
+                        if (w == wy && (iy >> 1) == k) {  // the label column
+                            float gl, gh;
+                            upk(g, gl, gh);
+                            if (iy & 1) gh -= bc;
+                            else gl -= bc;
+                            g = pk(gl, gh);
+                        }
+                        if (CAP) g = mul2(g, dz);
+                        out[k] = P16::pack(g);
+                    }
+                    *reinterpret_cast<uint4*>(gg + eb) = make_uint4(out[0], out[1], out[2], out[3]);
+                } else {
+                    for (int i = 0; i < EPW; ++i) {
+                        if (eb + i < e0 || eb + i >= e1) continue;
+                        const float xv = P16::to_f(xs[w * EPW + i]);
+                        float zs, dz = 1.f;
+                        if (CAP) {
+                            const float th = Scal::tanh_a2x(__fmul_rn(xv, A2));
+                            zs = __fmul_rn(th, Kc);
+                            dz = fmaf(th * th, -s, s);
+                        } else {
+                            zs = __fmul_rn(xv, K);
+                        }
+                        const float arg = zs - lse2;
+                        float g = ex2f(arg) * (ENT ? fmaf(ps, arg, pc) : pc);
+                        if (TEACH) {
+                            const float tv = P16::to_f(ts[w * EPW + i]);
+                            const float pT = ex2f(fmaf(zs, invT, -lseT2));
+                            const float q = ex2f(fmaf(tv, KT, -lsq2));
+                            float tco = tc;
+                            if (RKL) {
+                                const float dxu = CAP ? fmaf(tv, -LOG2E, zs) * invT
+                                                      : fmaf(xv, s, -tv) * KT;
+                                tco = fmaf(ts_, dxu - dlse, tc);
+                            }
+                            g = fmaf(pT, tco, g);
+                            g = fmaf(q, qc, g);
+                        }
+                        if (eb + i == ey) g -= bc;
+                        if (CAP) g *= dz;
+                        reinterpret_cast<uint16_t*>(gg)[eb + i] = P16::from_f(g);
+                    }
+                }
+            }
+        }
+        __syncthreads();  // every thread is done with this stage
+        if (tid == 0) issue(it + p.nbuf);
+    }
+
+    if (lost && tid == 0) {
+        for (int b = 0; b < p.nbuf; ++b)
+            if (lost & (1u << b)) (void)mbar_wait_bounded(smem_addr(&bars[b]), (lost_par >> b) & 1u);
+    }
+    if (rank == 0 && tid == 0) {
+        double* out = p.partials + size_t(cid) * NACC;
+#pragma unroll
+        for (int i = 0; i < NACC; ++i) out[i] = acc[i];
+    }
+    if (C > 1) cluster_barrier();
+}
+
+}  // namespace hl

@@ -1,10 +1,10 @@
-// hl_rows_bf16.cu -- row-kernel instantiations for bf16 logits (one per feature set).
-#include "hl_rows_kernel.cuh"
+// hl_rows_bf16.cu -- 16-bit row-kernel instantiations for bf16 logits (one per feature set).
+#include "hl_rows16.cuh"
 
 namespace hl {
 
 #define HL_CASE(F) \
-    case F: return reinterpret_cast<const void*>(&rows_kernel<__nv_bfloat16, F>);
+    case F: return reinterpret_cast<const void*>(&rows_kernel16<__nv_bfloat16, F>);
 
 const void* rows_kernel_bf16(int feat) {
     switch (feat) {

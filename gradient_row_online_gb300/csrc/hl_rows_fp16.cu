@@ -1,10 +1,10 @@
-// hl_rows_fp16.cu -- row-kernel instantiations for fp16 logits (one per feature set).
-#include "hl_rows_kernel.cuh"
+// hl_rows_fp16.cu -- 16-bit row-kernel instantiations for fp16 logits (one per feature set).
+#include "hl_rows16.cuh"
 
 namespace hl {
 
 #define HL_CASE(F) \
-    case F: return reinterpret_cast<const void*>(&rows_kernel<__half, F>);
+    case F: return reinterpret_cast<const void*>(&rows_kernel16<__half, F>);
 
 const void* rows_kernel_fp16(int feat) {
     switch (feat) {

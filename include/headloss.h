@@ -174,7 +174,7 @@ int headloss_plan(headloss_t h, int64_t V, int dtype, int* cluster, int* stages,
                   int* threads, int* smem_bytes);
 
 /*
- * headloss_force_plan -- pin the cluster size (1, 2, 4 or 8) and the stage
+ * headloss_force_plan -- pin the cluster size (1..8) and the stage
  * count (2..4) for later calls on this handle, or 0 / 0 for the automatic
  * plan.  For tests and tuning.  A later call whose rows do not fit the pinned
  * plan returns ERR_SIZE.
