@@ -111,7 +111,7 @@ constexpr int kLaunchesPerCall = 3;
 struct Plan {
     int64_t V = -1;
     int dtype = -1, feat = -1;
-    int C = 0, nbuf = 0, words = 0, smem = 0, ncl = 0;
+    int C = 0, nbuf = 0, words = 0, smem = 0, ncl = 0, threads = 0;
     int64_t L = 0;
     const void* kernel = nullptr;
 };
@@ -128,7 +128,7 @@ struct headloss {
     int partials_cap;  // clusters
     long long* n_valid;
     int* err;
-    int forced_C, forced_nbuf;
+    int forced_C, forced_nbuf, forced_threads;
     Plan plan;  // cache of the last plan
     std::mutex mu;
 };
@@ -156,10 +156,10 @@ const void* kernel_for(int dtype, int feat) {
 }
 
 // Max co-resident clusters of `C` CTAs of `kernel` with `smem` bytes each.
-int active_clusters(const void* kernel, int C, int smem, int num_sms, int* out) {
+int active_clusters(const void* kernel, int C, int threads, int smem, int num_sms, int* out) {
     if (C == 1) {
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, THREADS, smem) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) !=
             cudaSuccess)
             return HEADLOSS_ERR_CUDA;
         *out = per_sm * num_sms;
@@ -172,7 +172,7 @@ int active_clusters(const void* kernel, int C, int smem, int num_sms, int* out) 
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(C * num_sms, 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -181,16 +181,21 @@ int active_clusters(const void* kernel, int C, int smem, int num_sms, int* out) 
 }
 
 // Chooses the cluster size C (CTAs sharing one row), the column slice per
-// CTA, the number of row stages each CTA buffers, and the persistent grid.
-// Every C in 1..8 whose slice leaves room for at least two stages (one
-// computing, one or more in flight) is a candidate; the plan with the most
-// co-resident CTAs wins (the GPCs of a GB300 fit 15 clusters of 8 but 28 of
-// 5), ties going to the smaller cluster.
+// CTA, the threads per CTA, the row stages each CTA buffers, and the
+// persistent grid.  Candidates: every C in 1..8, 512 or 256 threads, 1..4
+// stages that fit in shared memory.  Measured on GB300 across the five loss
+// sets: what pays is many co-resident CTAs (two to four per SM, each holding
+// one row slice) -- one CTA's barriers, row merge and copy wait then hide
+// behind another's arithmetic -- more than deep per-CTA staging.  So: a
+// single-CTA cluster (no cluster exchange at all) if it fits at least two
+// CTAs per SM; otherwise the plans within 5% of the most co-resident CTAs,
+// and among them the smallest cluster, then one stage, then 256 threads.
 int make_plan(headloss* h, int64_t V, int dtype, Plan* out) {
     const int feat = feature_set(h);
     if (h->plan.V == V && h->plan.dtype == dtype && h->plan.feat == feat &&
         (h->forced_C == 0 || h->forced_C == h->plan.C) &&
-        (h->forced_nbuf == 0 || h->forced_nbuf == h->plan.nbuf)) {
+        (h->forced_nbuf == 0 || h->forced_nbuf == h->plan.nbuf) &&
+        (h->forced_threads == 0 || h->forced_threads == h->plan.threads)) {
         *out = h->plan;
         return HEADLOSS_OK;
     }
@@ -205,8 +210,9 @@ int make_plan(headloss* h, int64_t V, int dtype, Plan* out) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              h->smem_optin) != cudaSuccess)
         return HEADLOSS_ERR_CUDA;
-    Plan best;
-    int best_ctas = 0;
+    static const int kThreads[] = {512, 256};
+    Plan cand[MAX_CLUSTER * 2 * MAX_STAGES];
+    int ncand = 0;
     for (int C = 1; C <= MAX_CLUSTER; ++C) {
         if (h->forced_C && C != h->forced_C) continue;
         int64_t L = (V + C - 1) / C;
@@ -214,30 +220,47 @@ int make_plan(headloss* h, int64_t V, int dtype, Plan* out) {
         if (C > 1 && (C - 1) * L >= V && !h->forced_C) continue;  // an idle CTA
         const int64_t words = L / epw + 2;
         const int64_t stage = words * 16 * ops;
-        int64_t nbuf = budget / stage;
-        if (nbuf > MAX_STAGES) nbuf = MAX_STAGES;
-        if (h->forced_nbuf) {
-            if (nbuf < h->forced_nbuf) continue;
-            nbuf = h->forced_nbuf;
-        }
-        if (nbuf < 2) continue;
-        Plan pl;
-        pl.C = C;
-        pl.L = L;
-        pl.words = int(words);
-        pl.nbuf = int(nbuf);
-        pl.smem = int(stage * nbuf) + smem_fixed_bytes(acc_bytes);
-        int ncl = 0;
-        const int rc = active_clusters(kernel, C, pl.smem, h->num_sms, &ncl);
-        if (rc) return rc;
-        if (ncl > h->partials_cap) ncl = h->partials_cap;
-        if (ncl < 1) continue;
-        pl.ncl = ncl;
-        if (ncl * C > best_ctas) {
-            best = pl;
-            best_ctas = ncl * C;
+        const int64_t max_nbuf = budget / stage < MAX_STAGES ? budget / stage : MAX_STAGES;
+        for (int ti = 0; ti < 2; ++ti) {
+            const int T = kThreads[ti];
+            if (h->forced_threads && T != h->forced_threads) continue;
+            for (int64_t nbuf = 1; nbuf <= max_nbuf; ++nbuf) {
+                if (h->forced_nbuf && nbuf != h->forced_nbuf) continue;
+                Plan pl;
+                pl.C = C;
+                pl.L = L;
+                pl.words = int(words);
+                pl.nbuf = int(nbuf);
+                pl.threads = T;
+                pl.smem = int(stage * nbuf) + smem_fixed_bytes(acc_bytes);
+                int ncl = 0;
+                const int rc = active_clusters(kernel, C, T, pl.smem, h->num_sms, &ncl);
+                if (rc) return rc;
+                if (ncl > h->partials_cap) ncl = h->partials_cap;
+                if (ncl < 1) continue;
+                pl.ncl = ncl;
+                cand[ncand++] = pl;
+            }
         }
     }
+    Plan best;
+    int most = 0;
+    for (int i = 0; i < ncand; ++i)
+        if (cand[i].ncl * cand[i].C > most) most = cand[i].ncl * cand[i].C;
+    auto better = [](const Plan& a, const Plan& b) {  // a preferred over b?
+        if (a.C != b.C) return a.C < b.C;
+        if (a.nbuf != b.nbuf) return a.nbuf < b.nbuf;
+        return a.threads < b.threads;
+    };
+    for (int i = 0; i < ncand; ++i) {  // a one-CTA cluster with two or more CTAs per SM
+        const Plan& c = cand[i];
+        if (c.C == 1 && c.ncl >= 2 * h->num_sms && (best.C == 0 || better(c, best))) best = c;
+    }
+    if (best.C == 0)
+        for (int i = 0; i < ncand; ++i) {
+            const Plan& c = cand[i];
+            if (double(c.ncl) * c.C >= 0.95 * most && (best.C == 0 || better(c, best))) best = c;
+        }
     if (best.C == 0) return HEADLOSS_ERR_SIZE;
     best.V = V;
     best.dtype = dtype;
@@ -329,13 +352,15 @@ void headloss_destroy(headloss_t h) {
     delete h;
 }
 
-int headloss_force_plan(headloss_t h, int cluster, int stages) {
+int headloss_force_plan(headloss_t h, int cluster, int stages, int threads) {
     if (!h) return HEADLOSS_ERR_ARG;
     if (cluster < 0 || cluster > MAX_CLUSTER) return HEADLOSS_ERR_ARG;
-    if (!(stages == 0 || (stages >= 2 && stages <= MAX_STAGES))) return HEADLOSS_ERR_ARG;
+    if (stages < 0 || stages > MAX_STAGES) return HEADLOSS_ERR_ARG;
+    if (!(threads == 0 || threads == 256 || threads == 512)) return HEADLOSS_ERR_ARG;
     std::lock_guard<std::mutex> g(h->mu);
     h->forced_C = cluster;
     h->forced_nbuf = stages;
+    h->forced_threads = threads;
     h->plan = Plan();
     return HEADLOSS_OK;
 }
@@ -351,7 +376,7 @@ int headloss_plan(headloss_t h, int64_t V, int dtype, int* cluster, int* stages,
     if (cluster) *cluster = pl.C;
     if (stages) *stages = pl.nbuf;
     if (ctas) *ctas = pl.ncl * pl.C;
-    if (threads) *threads = THREADS;
+    if (threads) *threads = pl.threads;
     if (smem_bytes) *smem_bytes = pl.smem;
     return HEADLOSS_OK;
 }
@@ -432,7 +457,7 @@ int headloss_forward_backward(headloss_t h, const void* logits, int64_t N, int64
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3(ncl * pl.C, 1, 1);
-        cfg.blockDim = dim3(THREADS, 1, 1);
+        cfg.blockDim = dim3(pl.threads, 1, 1);
         cfg.dynamicSmemBytes = pl.smem;
         cfg.stream = s;
         cfg.attrs = attr;

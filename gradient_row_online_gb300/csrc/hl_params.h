@@ -21,7 +21,7 @@ enum : uint32_t {
 // Device error bits (read back by headloss_get_device_error).
 enum : int { E_LABEL = 1, E_TIMEOUT = 2 };
 
-constexpr int THREADS = 512;
+constexpr int THREADS = 512;  // maximum threads per CTA (a plan may launch 256)
 constexpr int NWARPS = THREADS / 32;
 constexpr int MAX_CLUSTER = 8;
 constexpr int MAX_STAGES = 4;

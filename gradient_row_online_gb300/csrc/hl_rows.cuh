@@ -227,13 +227,17 @@ struct DTraits<float> {
 // Shared-memory bytes beyond the stage buffers (mbarriers, exchange records,
 // reduction scratch, row coefficients), for an accumulator of `acc_bytes`.
 __host__ __device__ constexpr int smem_fixed_bytes(int acc_bytes) {
-    return 8 * MAX_STAGES + 8 * NACC + acc_bytes * (2 * MAX_CLUSTER * NREC + NWARPS * NREC + 16);
+    return 8 * MAX_STAGES + 8 * NACC +
+           acc_bytes * (2 * MAX_CLUSTER * NREC + NWARPS * NREC + 2 * NWARPS + 16);
 }
 
 // ---------------------------------------------------------- reductions ----
 
+// Block reductions over the CTA's nwarps = blockDim.x / 32 (<= NWARPS) warps;
+// the result is left in every lane of warp 0.
 template <typename A, int NV>
 __device__ __forceinline__ void block_sum(A (&v)[NV], A* red, int lane, int warp) {
+    const int nwarps = int(blockDim.x >> 5);
 #pragma unroll
     for (int o = 16; o; o >>= 1)
 #pragma unroll
@@ -244,7 +248,7 @@ __device__ __forceinline__ void block_sum(A (&v)[NV], A* red, int lane, int warp
     __syncthreads();
     if (warp == 0) {
 #pragma unroll
-        for (int i = 0; i < NV; ++i) v[i] = lane < NWARPS ? red[lane * NV + i] : A(0);
+        for (int i = 0; i < NV; ++i) v[i] = lane < nwarps ? red[lane * NV + i] : A(0);
 #pragma unroll
         for (int o = 16; o; o >>= 1)
 #pragma unroll
@@ -254,6 +258,7 @@ __device__ __forceinline__ void block_sum(A (&v)[NV], A* red, int lane, int warp
 
 template <typename A, int NV>
 __device__ __forceinline__ void block_max(A (&v)[NV], A* red, int lane, int warp) {
+    const int nwarps = int(blockDim.x >> 5);
 #pragma unroll
     for (int o = 16; o; o >>= 1)
 #pragma unroll
@@ -264,7 +269,7 @@ __device__ __forceinline__ void block_max(A (&v)[NV], A* red, int lane, int warp
     __syncthreads();
     if (warp == 0) {
 #pragma unroll
-        for (int i = 0; i < NV; ++i) v[i] = lane < NWARPS ? red[lane * NV + i] : A(-CUDART_INF);
+        for (int i = 0; i < NV; ++i) v[i] = lane < nwarps ? red[lane * NV + i] : A(-CUDART_INF);
 #pragma unroll
         for (int o = 16; o; o >>= 1)
 #pragma unroll

@@ -3,33 +3,61 @@
 // Same row pipeline as the generic kernel (hl_rows_kernel.cuh): a cluster
 // per row, each CTA a column slice resident in shared memory, the row read
 // from HBM once and the gradient written once.  This version is written for
-// issue throughput, which bounds the 16-bit path on GB300:
-//   - pass A takes the slice max on packed 16-bit pairs (one max per 2 elements);
+// issue throughput and MUFU throughput, which bound the 16-bit path on GB300:
+//   - pass A takes the slice max on packed 16-bit pairs (one max per 2
+//     elements); every warp reduces the per-warp maxima itself, so no
+//     broadcast barrier follows;
 //   - passes B and C run on fp32 pairs (add / mul / fma .f32x2: one issued
-//     instruction per 2 elements) with single-instruction ex2 / rcp;
-//   - softcap's tanh comes from tanh(y) = 1 - 2 / (exp(2y) + 1) (ex2 + rcp),
+//     instruction per 2 elements) with single-instruction ex2;
+//   - softcap: z = s*c*tanh(x/c) lies in [-s*c, s*c], so the student needs no
+//     max (the shift is s*c); tanh comes from an odd polynomial on the FMA
+//     pipe when the slice's |x| / c stays within its fitted range, else from
+//     tanh(y) = 1 - 2 / (exp(2y) + 1) (ex2 + rcp);
 //   - 16-byte words wholly inside the slice take the packed path; only the
 //     (at most two) partial words at a ragged slice edge take a scalar path;
-//   - the C partial records of a row are merged by C lanes of warp 0 at once.
+//   - after the cluster exchange warp 0 merges the C partial records (C lanes
+//     at once) and broadcasts the row coefficients through shared memory.
 #pragma once
 #include "hl_pack.cuh"
 #include "hl_rows.cuh"
+#include "hl_tanh_poly.h"
 
 namespace hl {
 
-// Scalar twin of the packed element math, for the partial words.
-struct Scal {
-    __device__ static float tanh_a2x(float a2x) {
-        const float w = ex2f(a2x) + 1.f;
-        return fmaf(rcpf(w), -2.f, 1.f);
-    }
+template <bool B>
+struct BoolC {
+    static constexpr bool value = B;
 };
 
-// Warp 0 merges the C records of a row (lane k holds record k), then lane 0
-// derives the row's losses and gradient coefficients.
+// Scalar twin of the packed element math, for the partial words.
+__device__ __forceinline__ float tanh_a2x_1(float a2x) {
+    const float w = ex2f(a2x) + 1.f;
+    return fmaf(rcpf(w), -2.f, 1.f);
+}
+
+// tanh(y) = y * P(y^2) on |y| <= HL_TANH_POLY_Y0 (FMA pipe only).
+__device__ __forceinline__ f2 tanh_poly2(f2 y) {
+    const f2 u = mul2(y, y);
+    f2 q = fma2(u, pk1(HL_TANH_POLY_C6), pk1(HL_TANH_POLY_C5));
+    q = fma2(q, u, pk1(HL_TANH_POLY_C4));
+    q = fma2(q, u, pk1(HL_TANH_POLY_C3));
+    q = fma2(q, u, pk1(HL_TANH_POLY_C2));
+    q = fma2(q, u, pk1(HL_TANH_POLY_C1));
+    q = fma2(q, u, pk1(1.f));
+    return mul2(y, q);
+}
+
+// Row coefficients, identical in every lane of the calling warp.
+struct RowCoef {
+    float lse2, lseT2, lsq2, pc, ps, tc, ts, qc, bc;
+};
+
+// A warp merges the C records of a row (lane k holds record k) and derives
+// the row's gradient coefficients (identical in every lane); with
+// `accumulate` its lane 0 also adds the row's losses to the CTA's partial sums.
 template <bool TEACH, bool RKL, bool ENT, bool CAP>
-__device__ void row_epilogue16(const Params& p, const float* recs, int C, bool accumulate,
-                               float old_lp, float adv, double* acc, float* coef, int lane) {
+__device__ RowCoef row_epilogue16(const Params& p, const float* recs, int C, bool accumulate,
+                                  float old_lp, float adv, double* acc, int lane) {
     const float LN2 = 0.6931471805599453f;
     const float invT = 1.f / p.T;
     float r[NREC];
@@ -40,7 +68,7 @@ __device__ void row_epilogue16(const Params& p, const float* recs, int C, bool a
     float M = live ? r[R_ZM] : -CUDART_INF_F;
     float Mu = (live && TEACH) ? r[R_UM] : -CUDART_INF_F;
 #pragma unroll
-    for (int o = 4; o; o >>= 1) {
+    for (int o = 16; o; o >>= 1) {  // every lane needs the row max: reduce over all 32
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         if (TEACH) Mu = fmaxf(Mu, __shfl_xor_sync(0xffffffffu, Mu, o));
     }
@@ -67,7 +95,9 @@ __device__ void row_epilogue16(const Params& p, const float* recs, int C, bool a
     for (int o = 4; o; o >>= 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) c[i] += __shfl_xor_sync(0xffffffffu, c[i], o);
-    if (lane != 0) return;
+    // lane 0's sums (a fixed order) define the row for the whole warp
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = __shfl_sync(0xffffffffu, c[i], 0);
 
     const float S = c[0], E = c[1], ST = c[2], Sq = c[3], Eq = c[4], Xp = c[5], Y = c[6];
     const float zy = c[7];
@@ -85,6 +115,7 @@ __device__ void row_epilogue16(const Params& p, const float* recs, int C, bool a
         dce = LN2 * (Xp / Sq + lST - Eq / Sq);
         if (RKL) rkl = LN2 * (Y / ST - lST + lSq);
     }
+    RowCoef k{};
     float pc = 0.f, ps = 0.f, tc = 0.f, ts = 0.f, qc = 0.f, bc = 0.f;
     if (f & L_CE) {
         pc += kk * p.w_ce;
@@ -138,16 +169,16 @@ __device__ void row_epilogue16(const Params& p, const float* recs, int C, bool a
         qc *= p.s;
         bc *= p.s;
     }
-    coef[K_LSE2] = lse2;
-    coef[K_LSET2] = TEACH ? M * invT + lST : 0.f;
-    coef[K_LSQ2] = TEACH ? Mu + lSq : 0.f;
-    coef[K_PC] = pc;
-    coef[K_PS] = ps;
-    coef[K_TC] = tc;
-    coef[K_TS] = ts;
-    coef[K_QC] = qc;
-    coef[K_BC] = bc;
-    if (accumulate) {
+    k.lse2 = lse2;
+    k.lseT2 = TEACH ? M * invT + lST : 0.f;
+    k.lsq2 = TEACH ? Mu + lSq : 0.f;
+    k.pc = pc;
+    k.ps = ps;
+    k.tc = tc;
+    k.ts = ts;
+    k.qc = qc;
+    k.bc = bc;
+    if (accumulate && lane == 0) {
         acc[A_NVALID] += 1.0;
         if (f & L_CE) acc[A_CE] += double((lse2 - zy) * LN2);
         if (f & L_Z) acc[A_Z] += double(lse) * double(lse);
@@ -165,6 +196,7 @@ __device__ void row_epilogue16(const Params& p, const float* recs, int C, bool a
         }
         if (f & L_ENTROPY) acc[A_ENT] += double(H);
     }
+    return k;
 }
 
 template <typename DT, int FEAT>
@@ -180,14 +212,16 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
 
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nthr = int(blockDim.x), nwarps = nthr >> 5;
     const int W = p.words;
     const uint32_t opbytes = uint32_t(W) * 16u;
     const uint32_t stage_bytes = opbytes * OPS;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(stage_bytes) * p.nbuf);
     double* acc = reinterpret_cast<double*>(bars + MAX_STAGES);  // [NACC], rank 0 only
     float* xch = reinterpret_cast<float*>(acc + NACC);         // [2][MAX_CLUSTER][NREC]
-    float* red = xch + 2 * MAX_CLUSTER * NREC;                   // [NWARPS][NREC]
-    float* coef = red + NWARPS * NREC;                           // [16]
+    float* red = xch + 2 * MAX_CLUSTER * NREC;                   // [NWARPS][NREC]: sums
+    float* redmax = red + NWARPS * NREC;                         // [NWARPS][2]: maxima
+    float* coefs = redmax + 2 * NWARPS;                          // RowCoef of the row
 
     const int C = p.C;
     uint32_t rank, cid, ncl;
@@ -209,20 +243,24 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
 
     const float LOG2E = 1.4426950408889634f;
     const float s = p.s;
-    const float K = s * LOG2E;                                // zs = x * K (no softcap)
-    const float A2 = CAP ? 2.f * LOG2E / p.softcap : 0.f;     // ex2 argument of tanh(x / c)
-    const float Kc = CAP ? s * p.softcap * LOG2E : 0.f;       // zs = tanh(x / c) * Kc
+    const float K = s * LOG2E;                              // zs = x * K (no softcap)
+    const float invc = CAP ? 1.f / p.softcap : 0.f;         // y = x / c
+    const float A2 = CAP ? 2.f * LOG2E * invc : 0.f;        // ex2 argument of tanh(x / c)
+    const float Kc = CAP ? s * p.softcap * LOG2E : 0.f;     // zs = tanh(x / c) * Kc, |zs| <= Kc
     const float invT = 1.f / p.T;
-    const float KT = LOG2E * invT;                            // us = t * KT
+    const float KT = LOG2E * invT;                          // us = t * KT
     const f2 K2 = pk1(K), A22 = pk1(A2), Kc2 = pk1(Kc), invT2 = pk1(invT), KT2 = pk1(KT);
+    const f2 invc2 = pk1(invc), KcT2 = pk1(Kc * invT);
     const f2 z2 = pk1(0.f);
 
-    // zs of one value, and of a pair: the same operations in the same order.
+    // zs of one value (no softcap): the same operation as the packed path.
     auto zs1 = [&](float v) -> float {
-        return CAP ? __fmul_rn(Scal::tanh_a2x(__fmul_rn(v, A2)), Kc) : __fmul_rn(v, K);
+        return CAP ? __fmul_rn(tanh_a2x_1(__fmul_rn(v, A2)), Kc) : __fmul_rn(v, K);
     };
-    auto zs2 = [&](f2 v) -> f2 {
-        return CAP ? mul2(tanh_from_ex2_arg(mul2(v, A22)), Kc2) : mul2(v, K2);
+    // tanh(x / c) of a pair, by the polynomial or by ex2 + rcp
+    auto th2 = [&](f2 xv, auto poly) -> f2 {
+        if constexpr (decltype(poly)::value) return tanh_poly2(mul2(xv, invc2));
+        else return tanh_from_ex2_arg(mul2(xv, A22));
     };
 
     if (tid == 0) {
@@ -320,14 +358,20 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
         }
 
         if (valid) {
-            // ---- pass A: slice max on packed 16-bit pairs ----
+            // ---- pass A: slice max (softcap: max |x|) on packed 16-bit pairs ----
             float mx[2];
             {
-                uint32_t mxx = P16::NEG_INF2, mxt = P16::NEG_INF2;
-                float sx = -CUDART_INF_F, stt = -CUDART_INF_F;
-                for (int w = tid; w < nw; w += THREADS) {
+                uint32_t mxx = CAP ? 0u : P16::NEG_INF2, mxt = P16::NEG_INF2;
+                float sx = CAP ? 0.f : -CUDART_INF_F, stt = -CUDART_INF_F;
+                for (int w = tid; w < nw; w += nthr) {
                     if (w >= wlo && w < whi) {
-                        const uint4 a = *reinterpret_cast<const uint4*>(xs_b + size_t(w) * 16);
+                        uint4 a = *reinterpret_cast<const uint4*>(xs_b + size_t(w) * 16);
+                        if (CAP) {
+                            a.x &= 0x7fff7fffu;
+                            a.y &= 0x7fff7fffu;
+                            a.z &= 0x7fff7fffu;
+                            a.w &= 0x7fff7fffu;
+                        }
                         mxx = P16::max2(P16::max2(mxx, a.x), P16::max2(a.y, a.z));
                         mxx = P16::max2(mxx, a.w);
                         if (TEACH) {
@@ -340,7 +384,8 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                         const int64_t eb = (wf + w) * EPW;
                         for (int i = 0; i < EPW; ++i) {
                             if (eb + i < e0 || eb + i >= e1) continue;
-                            sx = fmaxf(sx, P16::to_f(xs[w * EPW + i]));
+                            const float v = P16::to_f(xs[w * EPW + i]);
+                            sx = fmaxf(sx, CAP ? fabsf(v) : v);
                             if (TEACH) stt = fmaxf(stt, P16::to_f(ts[w * EPW + i]));
                         }
                     }
@@ -350,77 +395,101 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                 mx[0] = fmaxf(sx, fmaxf(a, b));
                 upk(P16::unpack(mxt), a, b);
                 mx[1] = fmaxf(stt, fmaxf(a, b));
+#pragma unroll
+                for (int o = 16; o; o >>= 1) {
+                    mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], o));
+                    mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], o));
+                }
+                if (lane == 0) {
+                    redmax[warp * 2] = mx[0];
+                    redmax[warp * 2 + 1] = mx[1];
+                }
+                __syncthreads();
+                // every warp reduces the per-warp maxima itself
+                mx[0] = lane < nwarps ? redmax[lane * 2] : (CAP ? 0.f : -CUDART_INF_F);
+                mx[1] = lane < nwarps ? redmax[lane * 2 + 1] : -CUDART_INF_F;
+#pragma unroll
+                for (int o = 16; o; o >>= 1) {
+                    mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], o));
+                    mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], o));
+                }
             }
-            block_max<float, 2>(mx, red, lane, warp);
-            if (tid == 0) {
-                coef[0] = nonempty ? zs1(mx[0]) : -CUDART_INF_F;
-                coef[1] = (TEACH && nonempty) ? __fmul_rn(mx[1], KT) : -CUDART_INF_F;
-            }
-            __syncthreads();
-            const float zm = coef[0], um = coef[1];
-            const f2 zm2 = pk1(zm), um2 = pk1(um);
+            // student shift: s*c*log2e under softcap (|zs| <= Kc), else the slice max
+            const float zm = CAP ? Kc : (nonempty ? zs1(mx[0]) : -CUDART_INF_F);
+            const float um = (TEACH && nonempty) ? __fmul_rn(mx[1], KT) : -CUDART_INF_F;
+            // the polynomial tanh covers the slice when max |x| / c is in range
+            const bool poly = CAP && __fmul_rn(mx[0], invc) <= HL_TANH_POLY_Y0;
+            const f2 zm2 = pk1(zm), um2 = pk1(um), nzm2 = pk1(-zm);
 
-            // ---- pass B: exponent sums relative to the slice max ----
+            // ---- pass B: exponent sums relative to the shifts ----
             // S = sum 2^d, E = sum 2^d d (d = zs - zm); ST = sum 2^(d/T);
             // Sq = sum 2^du, Eq = sum 2^du du (du = us - um);
             // Xp = sum 2^du (du - d/T);  Y = -sum 2^(d/T) (du - d/T).
             f2 S2 = z2, E2 = z2, ST2 = z2, Sq2 = z2, Eq2 = z2, Xp2 = z2, Y2 = z2;
             float sS = 0.f, sE = 0.f, sST = 0.f, sSq = 0.f, sEq = 0.f, sXp = 0.f, sY = 0.f;
-            for (int w = tid; w < nw; w += THREADS) {
-                if (w >= wlo && w < whi) {
-                    const uint4 a = *reinterpret_cast<const uint4*>(xs_b + size_t(w) * 16);
-                    uint4 b = make_uint4(0, 0, 0, 0);
-                    if (TEACH) b = *reinterpret_cast<const uint4*>(xs_b + opbytes + size_t(w) * 16);
-                    const uint32_t xa[4] = {a.x, a.y, a.z, a.w};
-                    const uint32_t tb[4] = {b.x, b.y, b.z, b.w};
+            auto passB = [&](auto polyc) {
+                for (int w = tid; w < nw; w += nthr) {
+                    if (w >= wlo && w < whi) {
+                        const uint4 a = *reinterpret_cast<const uint4*>(xs_b + size_t(w) * 16);
+                        uint4 b = make_uint4(0, 0, 0, 0);
+                        if (TEACH)
+                            b = *reinterpret_cast<const uint4*>(xs_b + opbytes + size_t(w) * 16);
+                        const uint32_t xa[4] = {a.x, a.y, a.z, a.w};
+                        const uint32_t tb[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const f2 d = sub2(zs2(P16::unpack(xa[k])), zm2);
-                        const f2 e = ex2p(d);
-                        S2 = add2(S2, e);
-                        if (ENT) E2 = fma2(e, d, E2);
-                        if (TEACH) {
-                            const f2 dT = mul2(d, invT2);
-                            const f2 eT = ex2p(dT);
-                            ST2 = add2(ST2, eT);
-                            const f2 du = sub2(mul2(P16::unpack(tb[k]), KT2), um2);
-                            const f2 eq = ex2p(du);
-                            Sq2 = add2(Sq2, eq);
-                            Eq2 = fma2(eq, du, Eq2);
-                            const f2 wd = sub2(du, dT);
-                            Xp2 = fma2(eq, wd, Xp2);
-                            if (RKL) Y2 = fma2(eT, wd, Y2);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const f2 xv = P16::unpack(xa[kk]);
+                            // d = zs - zm; under softcap one fma: Kc * th - Kc
+                            const f2 d = CAP ? fma2(th2(xv, polyc), Kc2, nzm2)
+                                             : sub2(mul2(xv, K2), zm2);
+                            const f2 e = ex2p(d);
+                            S2 = add2(S2, e);
+                            if (ENT) E2 = fma2(e, d, E2);
+                            if (TEACH) {
+                                const f2 dT = mul2(d, invT2);
+                                const f2 eT = ex2p(dT);
+                                ST2 = add2(ST2, eT);
+                                const f2 du = sub2(mul2(P16::unpack(tb[kk]), KT2), um2);
+                                const f2 eq = ex2p(du);
+                                Sq2 = add2(Sq2, eq);
+                                Eq2 = fma2(eq, du, Eq2);
+                                const f2 wd = sub2(du, dT);
+                                Xp2 = fma2(eq, wd, Xp2);
+                                if (RKL) Y2 = fma2(eT, wd, Y2);
+                            }
                         }
-                    }
-                } else {
-                    const int64_t eb = (wf + w) * EPW;
-                    for (int i = 0; i < EPW; ++i) {
-                        if (eb + i < e0 || eb + i >= e1) continue;
-                        const float d = __fsub_rn(zs1(P16::to_f(xs[w * EPW + i])), zm);
-                        const float e = ex2f(d);
-                        sS += e;
-                        if (ENT) sE = fmaf(e, d, sE);
-                        if (TEACH) {
-                            const float dT = __fmul_rn(d, invT);
-                            const float eT = ex2f(dT);
-                            sST += eT;
-                            const float du =
-                                __fsub_rn(__fmul_rn(P16::to_f(ts[w * EPW + i]), KT), um);
-                            const float eq = ex2f(du);
-                            sSq += eq;
-                            sEq = fmaf(eq, du, sEq);
-                            const float wd = __fsub_rn(du, dT);
-                            sXp = fmaf(eq, wd, sXp);
-                            if (RKL) sY = fmaf(eT, wd, sY);
+                    } else {
+                        const int64_t eb = (wf + w) * EPW;
+                        for (int i = 0; i < EPW; ++i) {
+                            if (eb + i < e0 || eb + i >= e1) continue;
+                            const float d = __fsub_rn(zs1(P16::to_f(xs[w * EPW + i])), zm);
+                            const float e = ex2f(d);
+                            sS += e;
+                            if (ENT) sE = fmaf(e, d, sE);
+                            if (TEACH) {
+                                const float dT = __fmul_rn(d, invT);
+                                const float eT = ex2f(dT);
+                                sST += eT;
+                                const float du =
+                                    __fsub_rn(__fmul_rn(P16::to_f(ts[w * EPW + i]), KT), um);
+                                const float eq = ex2f(du);
+                                sSq += eq;
+                                sEq = fmaf(eq, du, sEq);
+                                const float wd = __fsub_rn(du, dT);
+                                sXp = fmaf(eq, wd, sXp);
+                                if (RKL) sY = fmaf(eT, wd, sY);
+                            }
                         }
                     }
                 }
-            }
+            };
+            if (CAP && poly) passB(BoolC<true>{});
+            else passB(BoolC<false>{});
             float sm[7] = {hsum(S2) + sS, hsum(E2) + sE, hsum(ST2) + sST, hsum(Sq2) + sSq,
                            hsum(Eq2) + sEq, hsum(Xp2) + sXp, -(hsum(Y2) + sY)};
             block_sum<float, 7>(sm, red, lane, warp);
             // warp 0 now holds the CTA totals in every lane
-            float* myrec = xch + ((xc & 1) * MAX_CLUSTER + rank) * NREC;
+            float* xrec = xch + (xc & 1) * MAX_CLUSTER * NREC;
             if (warp == 0) {
                 float zyv = 0.f, hasy = 0.f;
                 if (has_labels && y >= col0 && y < col1) {
@@ -431,135 +500,135 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                                          zyv, hasy};
                 if (C > 1) {
                     if (lane < C) {
-                        const uint32_t ra = map_peer(smem_addr(myrec), uint32_t(lane));
+                        const uint32_t ra = map_peer(smem_addr(xrec + rank * NREC), uint32_t(lane));
 #pragma unroll
                         for (int i = 0; i < NREC; ++i) st_peer(ra + i * 4u, rec[i]);
                     }
                 } else if (lane == 0) {
 #pragma unroll
-                    for (int i = 0; i < NREC; ++i) myrec[i] = rec[i];
+                    for (int i = 0; i < NREC; ++i) xrec[i] = rec[i];
                 }
             }
             if (C > 1) cluster_barrier();
             else __syncwarp();
-            if (warp == 0)
-                row_epilogue16<TEACH, RKL, ENT, CAP>(p, xch + (xc & 1) * MAX_CLUSTER * NREC, C,
-                                                     rank == 0, old_lp, adv, acc, coef, lane);
+            if (warp == 0) {
+                const RowCoef kw = row_epilogue16<TEACH, RKL, ENT, CAP>(
+                    p, xrec, C, rank == 0, old_lp, adv, acc, lane);
+                if (lane == 0) *reinterpret_cast<RowCoef*>(coefs) = kw;
+            }
             ++xc;
             __syncthreads();
-        }
+            const RowCoef k = *reinterpret_cast<const RowCoef*>(coefs);
 
-        // ---- pass C: the combined gradient, written once ----
-        if (gg != nullptr) {
-            float lse2 = 0.f, lseT2 = 0.f, lsq2 = 0.f, pc = 0.f, ps = 0.f, tc = 0.f, ts_ = 0.f,
-                  qc = 0.f, bc = 0.f;
-            if (valid) {
-                lse2 = coef[K_LSE2];
-                lseT2 = coef[K_LSET2];
-                lsq2 = coef[K_LSQ2];
-                pc = coef[K_PC];
-                ps = coef[K_PS];
-                tc = coef[K_TC];
-                ts_ = coef[K_TS];
-                qc = coef[K_QC];
-                bc = coef[K_BC];
-            }
-            const float dlse = lseT2 - lsq2;
-            const f2 nlse2 = pk1(-lse2), nlseT2 = pk1(-lseT2), nlsq2 = pk1(-lsq2);
-            const f2 pc2 = pk1(pc), ps2 = pk1(ps), tc2 = pk1(tc), ts2 = pk1(ts_), qc2 = pk1(qc);
-            const f2 s2 = pk1(s), ns2 = pk1(-s), ndlse2 = pk1(-dlse), L2E2 = pk1(LOG2E);
-            // word and element of the label column in this slice (or none)
-            const int64_t ey = (has_labels && valid && y >= col0 && y < col1) ? r * V + y : -1;
-            const int wy = ey >= 0 ? int(ey / EPW - wf) : -1;
-            const int iy = ey >= 0 ? int(ey % EPW) : 0;
-            for (int w = tid; w < nw; w += THREADS) {
-                const int64_t eb = (wf + w) * EPW;
-                if (!valid) {
-                    if (w >= wlo && w < whi) {
-                        *reinterpret_cast<uint4*>(gg + eb) = make_uint4(0, 0, 0, 0);
-                    } else {
-                        for (int i = 0; i < EPW; ++i)
-                            if (eb + i >= e0 && eb + i < e1)
-                                reinterpret_cast<uint16_t*>(gg)[eb + i] = 0;
-                    }
-                    continue;
-                }
-                if (w >= wlo && w < whi) {
-                    const uint4 a = *reinterpret_cast<const uint4*>(xs_b + size_t(w) * 16);
-                    uint4 b = make_uint4(0, 0, 0, 0);
-                    if (TEACH) b = *reinterpret_cast<const uint4*>(xs_b + opbytes + size_t(w) * 16);
-                    const uint32_t xa[4] = {a.x, a.y, a.z, a.w};
-                    const uint32_t tb[4] = {b.x, b.y, b.z, b.w};
-                    uint32_t out[4];
+            // ---- pass C: the combined gradient, written once ----
+            if (gg != nullptr) {
+                const float dlse = k.lseT2 - k.lsq2;
+                const f2 nlse2 = pk1(-k.lse2), nlseT2 = pk1(-k.lseT2), nlsq2 = pk1(-k.lsq2);
+                const f2 pc2 = pk1(k.pc), ps2 = pk1(k.ps), tc2 = pk1(k.tc), ts2 = pk1(k.ts);
+                const f2 qc2 = pk1(k.qc), s2 = pk1(s), ns2 = pk1(-s), ndlse2 = pk1(-dlse);
+                const f2 nKT2 = pk1(-KT);
+                // word and element of the label column in this slice (or none)
+                const int64_t ey = (has_labels && y >= col0 && y < col1) ? r * V + y : -1;
+                const int wy = ey >= 0 ? int(ey / EPW - wf) : -1;
+                const int iy = ey >= 0 ? int(ey % EPW) : 0;
+                auto passC = [&](auto polyc) {
+                    for (int w = tid; w < nw; w += nthr) {
+                        const int64_t eb = (wf + w) * EPW;
+                        if (w >= wlo && w < whi) {
+                            const uint4 a = *reinterpret_cast<const uint4*>(xs_b + size_t(w) * 16);
+                            uint4 b = make_uint4(0, 0, 0, 0);
+                            if (TEACH)
+                                b = *reinterpret_cast<const uint4*>(xs_b + opbytes +
+                                                                    size_t(w) * 16);
+                            const uint32_t xa[4] = {a.x, a.y, a.z, a.w};
+                            const uint32_t tb[4] = {b.x, b.y, b.z, b.w};
+                            uint32_t out[4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const f2 xv = P16::unpack(xa[k]);
-                        f2 zs, dz = z2;
-                        if (CAP) {
-                            const f2 th = tanh_from_ex2_arg(mul2(xv, A22));
-                            zs = mul2(th, Kc2);
-                            dz = fma2(mul2(th, th), ns2, s2);
-                        } else {
-                            zs = mul2(xv, K2);
-                        }
-                        const f2 arg = add2(zs, nlse2);
-                        f2 g = mul2(ex2p(arg), ENT ? fma2(ps2, arg, pc2) : pc2);
-                        if (TEACH) {
-                            const f2 tv = P16::unpack(tb[k]);
-                            const f2 pT = ex2p(fma2(zs, invT2, nlseT2));
-                            const f2 q = ex2p(fma2(tv, KT2, nlsq2));
-                            f2 tco = tc2;
-                            if (RKL) {
-                                // log2 pT - log2 q from the logit difference
-                                const f2 dxu = CAP ? mul2(fma2(tv, pk1(-LOG2E), zs), invT2)
-                                                   : mul2(fma2(xv, s2, sub2(z2, tv)), KT2);
-                                tco = fma2(ts2, add2(dxu, ndlse2), tc2);
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const f2 xv = P16::unpack(xa[kk]);
+                                f2 th = z2, arg, argT = z2;
+                                if (CAP) {
+                                    th = th2(xv, polyc);
+                                    arg = fma2(th, Kc2, nlse2);  // zs - lse2
+                                    if (TEACH) argT = fma2(th, KcT2, nlseT2);
+                                } else {
+                                    const f2 zs = mul2(xv, K2);
+                                    arg = add2(zs, nlse2);
+                                    if (TEACH) argT = fma2(zs, invT2, nlseT2);
+                                }
+                                f2 g = mul2(ex2p(arg), ENT ? fma2(ps2, arg, pc2) : pc2);
+                                if (TEACH) {
+                                    const f2 tv = P16::unpack(tb[kk]);
+                                    const f2 pT = ex2p(argT);
+                                    const f2 q = ex2p(fma2(tv, KT2, nlsq2));
+                                    f2 tco = tc2;
+                                    if (RKL) {
+                                        // log2 pT - log2 q from the logit difference
+                                        const f2 dxu = CAP ? fma2(th, KcT2, mul2(tv, nKT2))
+                                                           : mul2(fma2(xv, s2, sub2(z2, tv)), KT2);
+                                        tco = fma2(ts2, add2(dxu, ndlse2), tc2);
+                                    }
+                                    g = fma2(pT, tco, g);
+                                    g = fma2(q, qc2, g);
+                                }
+                                if (w == wy && (iy >> 1) == kk) {  // the label column
+                                    float gl, gh;
+                                    upk(g, gl, gh);
+                                    if (iy & 1) gh -= k.bc;
+                                    else gl -= k.bc;
+                                    g = pk(gl, gh);
+                                }
+                                if (CAP) g = mul2(g, fma2(mul2(th, th), ns2, s2));  // dz/dx
+                                out[kk] = P16::pack(g);
                             }
-                            g = fma2(pT, tco, g);
-                            g = fma2(q, qc2, g);
+                            *reinterpret_cast<uint4*>(gg + eb) =
+                                make_uint4(out[0], out[1], out[2], out[3]);
+                        } else {
+                            for (int i = 0; i < EPW; ++i) {
+                                if (eb + i < e0 || eb + i >= e1) continue;
+                                const float xv = P16::to_f(xs[w * EPW + i]);
+                                float zs, dz = 1.f;
+                                if (CAP) {
+                                    const float th = tanh_a2x_1(__fmul_rn(xv, A2));
+                                    zs = __fmul_rn(th, Kc);
+                                    dz = fmaf(th * th, -s, s);
+                                } else {
+                                    zs = __fmul_rn(xv, K);
+                                }
+                                const float arg = zs - k.lse2;
+                                float g = ex2f(arg) * (ENT ? fmaf(k.ps, arg, k.pc) : k.pc);
+                                if (TEACH) {
+                                    const float tv = P16::to_f(ts[w * EPW + i]);
+                                    const float pT = ex2f(fmaf(zs, invT, -k.lseT2));
+                                    const float q = ex2f(fmaf(tv, KT, -k.lsq2));
+                                    float tco = k.tc;
+                                    if (RKL) {
+                                        const float dxu = CAP ? fmaf(tv, -LOG2E, zs) * invT
+                                                              : fmaf(xv, s, -tv) * KT;
+                                        tco = fmaf(k.ts, dxu - dlse, k.tc);
+                                    }
+                                    g = fmaf(pT, tco, g);
+                                    g = fmaf(q, k.qc, g);
+                                }
+                                if (eb + i == ey) g -= k.bc;
+                                if (CAP) g *= dz;
+                                reinterpret_cast<uint16_t*>(gg)[eb + i] = P16::from_f(g);
+                            }
                         }
-                        if (w == wy && (iy >> 1) == k) {  // the label column
-                            float gl, gh;
-                            upk(g, gl, gh);
-                            if (iy & 1) gh -= bc;
-                            else gl -= bc;
-                            g = pk(gl, gh);
-                        }
-                        if (CAP) g = mul2(g, dz);
-                        out[k] = P16::pack(g);
                     }
-                    *reinterpret_cast<uint4*>(gg + eb) = make_uint4(out[0], out[1], out[2], out[3]);
+                };
+                if (CAP && poly) passC(BoolC<true>{});
+                else passC(BoolC<false>{});
+            }
+        } else if (gg != nullptr) {
+            // a masked row: its gradient row is exact +0
+            for (int w = tid; w < nw; w += nthr) {
+                const int64_t eb = (wf + w) * EPW;
+                if (w >= wlo && w < whi) {
+                    *reinterpret_cast<uint4*>(gg + eb) = make_uint4(0, 0, 0, 0);
                 } else {
-                    for (int i = 0; i < EPW; ++i) {
-                        if (eb + i < e0 || eb + i >= e1) continue;
-                        const float xv = P16::to_f(xs[w * EPW + i]);
-                        float zs, dz = 1.f;
-                        if (CAP) {
-                            const float th = Scal::tanh_a2x(__fmul_rn(xv, A2));
-                            zs = __fmul_rn(th, Kc);
-                            dz = fmaf(th * th, -s, s);
-                        } else {
-                            zs = __fmul_rn(xv, K);
-                        }
-                        const float arg = zs - lse2;
-                        float g = ex2f(arg) * (ENT ? fmaf(ps, arg, pc) : pc);
-                        if (TEACH) {
-                            const float tv = P16::to_f(ts[w * EPW + i]);
-                            const float pT = ex2f(fmaf(zs, invT, -lseT2));
-                            const float q = ex2f(fmaf(tv, KT, -lsq2));
-                            float tco = tc;
-                            if (RKL) {
-                                const float dxu = CAP ? fmaf(tv, -LOG2E, zs) * invT
-                                                      : fmaf(xv, s, -tv) * KT;
-                                tco = fmaf(ts_, dxu - dlse, tc);
-                            }
-                            g = fmaf(pT, tco, g);
-                            g = fmaf(q, qc, g);
-                        }
-                        if (eb + i == ey) g -= bc;
-                        if (CAP) g *= dz;
-                        reinterpret_cast<uint16_t*>(gg)[eb + i] = P16::from_f(g);
-                    }
+                    for (int i = 0; i < EPW; ++i)
+                        if (eb + i >= e0 && eb + i < e1) reinterpret_cast<uint16_t*>(gg)[eb + i] = 0;
                 }
             }
         }

@@ -19,6 +19,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
 
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nthr = int(blockDim.x);
     const int W = p.words;
     const uint32_t opbytes = uint32_t(W) * 16u;
     const uint32_t stage_bytes = opbytes * OPS;
@@ -155,7 +156,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
         if (valid) {
             // ---- pass A: slice max of raw student / teacher logits ----
             A mx[2] = {A(-CUDART_INF), A(-CUDART_INF)};
-            for (int w = tid; w < nw; w += THREADS) {
+            for (int w = tid; w < nw; w += nthr) {
                 const int64_t eb = (wf + w) * EPW;
                 const bool full = eb >= e0 && eb + EPW <= e1;
                 A v[EPW];
@@ -183,7 +184,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
             // Sq = sum 2^du, Eq = sum 2^du du (du = us - um);
             // Xp = sum 2^du (du - d/T);  Y = -sum 2^(d/T) (du - d/T).
             A sm[7] = {A(0), A(0), A(0), A(0), A(0), A(0), A(0)};
-            for (int w = tid; w < nw; w += THREADS) {
+            for (int w = tid; w < nw; w += nthr) {
                 const int64_t eb = (wf + w) * EPW;
                 const bool full = eb >= e0 && eb + EPW <= e1;
                 A v[EPW], u[EPW];
@@ -268,7 +269,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
             }
             const A dlse = lseT2 - lsq2;
             const int64_t ey = (has_labels && valid && y >= col0 && y < col1) ? r * V + y : -1;
-            for (int w = tid; w < nw; w += THREADS) {
+            for (int w = tid; w < nw; w += nthr) {
                 const int64_t eb = (wf + w) * EPW;
                 const bool full = eb >= e0 && eb + EPW <= e1;
                 A gv[EPW];

@@ -85,7 +85,7 @@ def load_library(path: str = LIB_PATH):
     lib.headloss_get_device_error.restype = i32
     lib.headloss_plan.argtypes = [vp, i64, i32, ip, ip, ip, ip, ip]
     lib.headloss_plan.restype = i32
-    lib.headloss_force_plan.argtypes = [vp, i32, i32]
+    lib.headloss_force_plan.argtypes = [vp, i32, i32, i32]
     lib.headloss_force_plan.restype = i32
     lib.headloss_launches_per_call.argtypes = []
     lib.headloss_launches_per_call.restype = i32
@@ -181,8 +181,8 @@ def headloss_plan(h, V: int, dtype: int) -> dict:
                     (v.value for v in vals)))
 
 
-def headloss_force_plan(h, cluster: int, stages: int) -> None:
-    _check(load_library().headloss_force_plan(h, int(cluster), int(stages)),
+def headloss_force_plan(h, cluster: int, stages: int, threads: int = 0) -> None:
+    _check(load_library().headloss_force_plan(h, int(cluster), int(stages), int(threads)),
            "headloss_force_plan")
 
 
@@ -225,8 +225,8 @@ class HeadLoss:
     def plan(self, V: int, dtype: int) -> dict:
         return headloss_plan(self.h, V, dtype)
 
-    def force_plan(self, cluster: int, stages: int) -> None:
-        headloss_force_plan(self.h, cluster, stages)
+    def force_plan(self, cluster: int, stages: int, threads: int = 0) -> None:
+        headloss_force_plan(self.h, cluster, stages, threads)
 
     def device_error(self, stream=None) -> int:
         return headloss_get_device_error(self.h, stream)

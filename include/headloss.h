@@ -174,12 +174,12 @@ int headloss_plan(headloss_t h, int64_t V, int dtype, int* cluster, int* stages,
                   int* threads, int* smem_bytes);
 
 /*
- * headloss_force_plan -- pin the cluster size (1..8) and the stage
- * count (2..4) for later calls on this handle, or 0 / 0 for the automatic
- * plan.  For tests and tuning.  A later call whose rows do not fit the pinned
- * plan returns ERR_SIZE.
+ * headloss_force_plan -- pin the cluster size (1..8), the row stages per CTA
+ * (1..4) and the threads per CTA (256 or 512) for later calls on this
+ * handle; 0 leaves that choice to the planner.  For tests and tuning.  A
+ * later call whose rows do not fit the pinned plan returns ERR_SIZE.
  */
-int headloss_force_plan(headloss_t h, int cluster, int stages);
+int headloss_force_plan(headloss_t h, int cluster, int stages, int threads);
 
 /* Kernel launches one headloss_forward_backward call enqueues (constant). */
 int headloss_launches_per_call(void);

@@ -51,7 +51,9 @@ def test_tiny_ce_z_fp32_workload():
 SUBSETS = [c for r in range(1, 9) for c in itertools.combinations(ALL_LOSSES, r)]
 
 
-@pytest.mark.parametrize("softcap,scale", [(0.0, 1.0), (20.0, 0.6)])
+# softcap 20: |x| / c stays in the polynomial tanh range; softcap 3: most rows
+# fall back to the exp / reciprocal tanh
+@pytest.mark.parametrize("softcap,scale", [(0.0, 1.0), (20.0, 0.6), (3.0, 0.7)])
 def test_every_loss_subset_bf16(softcap, scale):
     for losses in SUBSETS:
         full_check(small(losses, softcap=softcap, logits_scale=scale, seed=len(losses)))
@@ -71,12 +73,14 @@ def test_ragged_and_tiny_vocab(V, dtype):
     full_check(small(ALL_LOSSES, N=19, V=V, dtype=dtype))
 
 
-@pytest.mark.parametrize("cluster,stages", [(1, 2), (2, 2), (2, 3), (4, 2), (8, 2), (8, 4)])
-def test_forced_cluster_plans(cluster, stages):
+@pytest.mark.parametrize("cluster,stages,threads", [
+    (1, 2, 512), (2, 2, 512), (2, 3, 256), (3, 1, 256), (4, 2, 512), (5, 1, 256), (6, 1, 512),
+    (7, 1, 256), (8, 2, 256), (8, 4, 512)])
+def test_forced_cluster_plans(cluster, stages, threads):
     wl = small(ALL_LOSSES, N=40, V=20011, softcap=30.0, logits_scale=0.5)
-    full_check(wl, plan=(cluster, stages))
+    full_check(wl, plan=(cluster, stages, threads))
     full_check(small(("ce", "z", "entropy"), N=40, V=8000, dtype=torch.float32),
-               plan=(cluster, stages))
+               plan=(cluster, stages, threads))
 
 
 def test_large_logits_fp32():
