@@ -92,11 +92,13 @@ static double transform(const oracle_cfg* cfg, double x) {
     return cfg->logits_scale * y;
 }
 
-/* dz/dx of the transform above. */
+/* dz/dx of the transform above: s * (1 - tanh^2(x / c)), evaluated as
+ * s / cosh^2(x / c) -- the same quantity without the cancellation of
+ * 1 - tanh^2 where tanh saturates (cosh overflow gives the exact limit 0). */
 static double transform_deriv(const oracle_cfg* cfg, double x) {
     if (cfg->softcap > 0.0) {
-        double th = tanh(x / cfg->softcap);
-        return cfg->logits_scale * (1.0 - th * th);
+        const double ch = cosh(x / cfg->softcap);
+        return cfg->logits_scale / (ch * ch);
     }
     return cfg->logits_scale;
 }

@@ -266,6 +266,22 @@ def test_logits_scale_is_the_chain_rule():
     assert np.allclose(a[2], s_ * b[2], rtol=1e-11, atol=1e-16)
 
 
+@pytest.mark.parametrize("y", [0.3, 4.0, 12.0, 25.0])
+def test_saturated_softcap_gradient_keeps_relative_accuracy(y):
+    """Two classes, label 0, softcap c, logits (c*y, 0): dCE/dx_0 = (p_0 - 1) * s * sech^2(y),
+    with sech^2(y) = 4 e^{-2y} / (1 + e^{-2y})^2 written out independently of cosh / tanh."""
+    c, s_ = 3.0, 0.7
+    x = np.array([[c * y, 0.0]])
+    cfg = orc.make_cfg(orc.CE, softcap=c, logits_scale=s_)
+    _, _, g, _ = orc.forward_backward(cfg, x, np.array([0], np.int64))
+    e = math.exp(-2.0 * y)
+    sech2 = 4.0 * e / (1.0 + e) ** 2
+    z0 = s_ * c * math.tanh(y)
+    p0 = 1.0 / (1.0 + math.exp(-z0))
+    expect = (p0 - 1.0) * s_ * sech2
+    assert abs(g[0, 0] - expect) <= 1e-12 * abs(expect)
+
+
 def test_softcap_limit_is_no_softcap():
     rng = np.random.default_rng(14)
     x, labels, t, adv = _rand_problem(rng, 6, 17)
