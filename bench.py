@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--workload", default="all_in_bf16")
     ap.add_argument("--rows", type=int, default=0,
                     help="use only the first ROWS tokens of the workload (profiling cases)")
+    ap.add_argument("--plan", default="",
+                    help="pin the launch plan, e.g. kernel=2,stages=2,threads=512,chunk_words=4 "
+                         "(profiling; default: the library's planner)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -181,6 +184,8 @@ def run_ours(args, rank, world, local):
         wl = wl.replace(N=min(args.rows, wl.N))
     hlb.load_library()
     h = pkg.headloss_for(wl)
+    if args.plan:
+        h.force_plan(**{k: int(v) for k, v in (kv.split("=") for kv in args.plan.split(","))})
     inp = W.make_inputs(wl, dev)
     grad = torch.empty_like(inp["logits"])
     out = torch.empty(16, dtype=torch.float32, device=dev)

@@ -16,6 +16,8 @@ namespace hl {
 const void* rows_kernel_bf16(int feat);
 const void* rows_kernel_fp16(int feat);
 const void* rows_kernel_fp32(int feat);
+const void* stream_kernel_bf16(int feat);
+const void* stream_kernel_fp16(int feat);
 
 // Valid rows of the call (0 <= label < V); a label >= V raises E_LABEL.
 // One block: the count is an exact integer whatever the order.
@@ -111,7 +113,8 @@ constexpr int kLaunchesPerCall = 3;
 struct Plan {
     int64_t V = -1;
     int dtype = -1, feat = -1;
-    int C = 0, nbuf = 0, words = 0, smem = 0, ncl = 0, threads = 0;
+    int kind = 0;  // HEADLOSS_KERNEL_RESIDENT or HEADLOSS_KERNEL_STREAM
+    int C = 0, nbuf = 0, words = 0, smem = 0, ncl = 0, threads = 0, chunk_words = 0;
     int64_t L = 0;
     const void* kernel = nullptr;
 };
@@ -125,11 +128,11 @@ struct headloss {
     int device, num_sms, smem_optin;
     void* ws;
     double* partials;
-    int partials_cap;  // clusters
+    int partials_cap;  // clusters (resident) or CTAs (streaming)
     long long* n_valid;
     int* err;
-    int forced_C, forced_nbuf, forced_threads;
-    Plan plan;  // cache of the last plan
+    headloss_plan_desc forced;  // zero fields: the planner decides
+    Plan plan;                  // cache of the last plan
     std::mutex mu;
 };
 
@@ -146,7 +149,14 @@ int feature_set(const headloss* h) {
     return f;
 }
 
-const void* kernel_for(int dtype, int feat) {
+const void* kernel_for(int kind, int dtype, int feat) {
+    if (kind == HEADLOSS_KERNEL_STREAM) {
+        switch (dtype) {
+            case HEADLOSS_BF16: return stream_kernel_bf16(feat);
+            case HEADLOSS_FP16: return stream_kernel_fp16(feat);
+            default: return nullptr;
+        }
+    }
     switch (dtype) {
         case HEADLOSS_BF16: return rows_kernel_bf16(feat);
         case HEADLOSS_FP16: return rows_kernel_fp16(feat);
@@ -180,26 +190,12 @@ int active_clusters(const void* kernel, int C, int threads, int smem, int num_sm
     return HEADLOSS_OK;
 }
 
-// Chooses the cluster size C (CTAs sharing one row), the column slice per
-// CTA, the threads per CTA, the row stages each CTA buffers, and the
-// persistent grid.  Candidates: every C in 1..8, 512 or 256 threads, 1..4
-// stages that fit in shared memory.  Measured on GB300 across the five loss
-// sets: what pays is many co-resident CTAs (two to four per SM, each holding
-// one row slice) -- one CTA's barriers, row merge and copy wait then hide
-// behind another's arithmetic -- more than deep per-CTA staging.  So: a
-// single-CTA cluster (no cluster exchange at all) if it fits at least two
-// CTAs per SM; otherwise the plans within 5% of the most co-resident CTAs,
-// and among them the smallest cluster, then one stage, then 256 threads.
-int make_plan(headloss* h, int64_t V, int dtype, Plan* out) {
-    const int feat = feature_set(h);
-    if (h->plan.V == V && h->plan.dtype == dtype && h->plan.feat == feat &&
-        (h->forced_C == 0 || h->forced_C == h->plan.C) &&
-        (h->forced_nbuf == 0 || h->forced_nbuf == h->plan.nbuf) &&
-        (h->forced_threads == 0 || h->forced_threads == h->plan.threads)) {
-        *out = h->plan;
-        return HEADLOSS_OK;
-    }
-    const void* kernel = kernel_for(dtype, feat);
+bool wants(int forced, int v) { return forced == 0 || forced == v; }
+
+// Resident candidates: every cluster size C in 1..8, 512 or 256 threads,
+// 1..4 row stages that fit in shared memory.
+int resident_candidates(headloss* h, int64_t V, int dtype, int feat, Plan* cand, int* ncand) {
+    const void* kernel = kernel_for(HEADLOSS_KERNEL_RESIDENT, dtype, feat);
     if (!kernel) return HEADLOSS_ERR_DTYPE;
     const int es = elem_size(dtype);
     const int epw = 16 / es;
@@ -211,22 +207,23 @@ int make_plan(headloss* h, int64_t V, int dtype, Plan* out) {
                              h->smem_optin) != cudaSuccess)
         return HEADLOSS_ERR_CUDA;
     static const int kThreads[] = {512, 256};
-    Plan cand[MAX_CLUSTER * 2 * MAX_STAGES];
-    int ncand = 0;
     for (int C = 1; C <= MAX_CLUSTER; ++C) {
-        if (h->forced_C && C != h->forced_C) continue;
+        if (!wants(h->forced.cluster, C)) continue;
         int64_t L = (V + C - 1) / C;
         L = (L + epw - 1) / epw * epw;
-        if (C > 1 && (C - 1) * L >= V && !h->forced_C) continue;  // an idle CTA
+        if (C > 1 && (C - 1) * L >= V && !h->forced.cluster) continue;  // an idle CTA
         const int64_t words = L / epw + 2;
         const int64_t stage = words * 16 * ops;
-        const int64_t max_nbuf = budget / stage < MAX_STAGES ? budget / stage : MAX_STAGES;
+        const int64_t max_nbuf =
+            budget / stage < MAX_RESIDENT_STAGES ? budget / stage : MAX_RESIDENT_STAGES;
         for (int ti = 0; ti < 2; ++ti) {
             const int T = kThreads[ti];
-            if (h->forced_threads && T != h->forced_threads) continue;
+            if (!wants(h->forced.threads, T)) continue;
             for (int64_t nbuf = 1; nbuf <= max_nbuf; ++nbuf) {
-                if (h->forced_nbuf && nbuf != h->forced_nbuf) continue;
+                if (!wants(h->forced.stages, int(nbuf))) continue;
                 Plan pl;
+                pl.kind = HEADLOSS_KERNEL_RESIDENT;
+                pl.kernel = kernel;
                 pl.C = C;
                 pl.L = L;
                 pl.words = int(words);
@@ -239,33 +236,156 @@ int make_plan(headloss* h, int64_t V, int dtype, Plan* out) {
                 if (ncl > h->partials_cap) ncl = h->partials_cap;
                 if (ncl < 1) continue;
                 pl.ncl = ncl;
-                cand[ncand++] = pl;
+                cand[(*ncand)++] = pl;
             }
         }
     }
-    Plan best;
+    return HEADLOSS_OK;
+}
+
+// Streaming candidates (16-bit logits with 16-byte aligned rows): 512 or 256
+// threads, 1, 2 or 4 words per thread per chunk, 2..8 chunk slots.
+int stream_candidates(headloss* h, int64_t V, int dtype, int feat, Plan* cand, int* ncand) {
+    if (dtype == HEADLOSS_FP32 || (V * elem_size(dtype)) % 16 != 0) return HEADLOSS_OK;
+    const void* kernel = kernel_for(HEADLOSS_KERNEL_STREAM, dtype, feat);
+    if (!kernel) return HEADLOSS_ERR_DTYPE;
+    const int ops = (feat & F_TEACH) ? 2 : 1;
+    const int budget = h->smem_optin - smem_fixed_bytes(4);
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             h->smem_optin) != cudaSuccess)
+        return HEADLOSS_ERR_CUDA;
+    static const int kThreads[] = {512, 256};
+    static const int kWords[] = {1, 2, 4};
+    for (int ti = 0; ti < 2; ++ti) {
+        const int T = kThreads[ti];
+        if (!wants(h->forced.threads, T)) continue;
+        for (int wi = 0; wi < 3; ++wi) {
+            const int wpt = kWords[wi];
+            if (!wants(h->forced.chunk_words, wpt)) continue;
+            const int64_t CH = int64_t(wpt) * 8 * T;  // elements per chunk
+            const int64_t slot = CH * 2 * ops;
+            for (int S = 2; S <= MAX_STAGES; ++S) {
+                if (!wants(h->forced.stages, S)) continue;
+                if (slot * S > budget) break;
+                Plan pl;
+                pl.kind = HEADLOSS_KERNEL_STREAM;
+                pl.kernel = kernel;
+                pl.C = 1;
+                pl.L = CH;
+                pl.words = int(CH / 8);
+                pl.nbuf = S;
+                pl.threads = T;
+                pl.chunk_words = wpt;
+                pl.smem = int(slot * S) + smem_fixed_bytes(4);
+                int n = 0;
+                const int rc = active_clusters(kernel, 1, T, pl.smem, h->num_sms, &n);
+                if (rc) return rc;
+                if (n > h->partials_cap) n = h->partials_cap;
+                if (n < 1) continue;
+                pl.ncl = n;
+                cand[(*ncand)++] = pl;
+            }
+        }
+    }
+    return HEADLOSS_OK;
+}
+
+// Resident rule (measured on GB300 across the five loss sets): many
+// co-resident CTAs (two to four per SM, each holding one row slice) pay more
+// than deep per-CTA staging -- one CTA's barriers, row merge and copy wait
+// hide behind another's arithmetic.  So: a single-CTA cluster (no cluster
+// exchange at all) if it fits at least two CTAs per SM; otherwise the plans
+// within 5% of the most co-resident CTAs, and among them the smallest
+// cluster, then one stage, then 256 threads.
+bool pick_resident(const headloss* h, const Plan* cand, int ncand, Plan* best) {
     int most = 0;
     for (int i = 0; i < ncand; ++i)
-        if (cand[i].ncl * cand[i].C > most) most = cand[i].ncl * cand[i].C;
-    auto better = [](const Plan& a, const Plan& b) {  // a preferred over b?
+        if (cand[i].kind == HEADLOSS_KERNEL_RESIDENT && cand[i].ncl * cand[i].C > most)
+            most = cand[i].ncl * cand[i].C;
+    auto better = [](const Plan& a, const Plan& b) {
         if (a.C != b.C) return a.C < b.C;
         if (a.nbuf != b.nbuf) return a.nbuf < b.nbuf;
         return a.threads < b.threads;
     };
-    for (int i = 0; i < ncand; ++i) {  // a one-CTA cluster with two or more CTAs per SM
+    Plan b;
+    for (int i = 0; i < ncand; ++i) {
         const Plan& c = cand[i];
-        if (c.C == 1 && c.ncl >= 2 * h->num_sms && (best.C == 0 || better(c, best))) best = c;
+        if (c.kind == HEADLOSS_KERNEL_RESIDENT && c.C == 1 && c.ncl >= 2 * h->num_sms &&
+            (b.C == 0 || better(c, b)))
+            b = c;
     }
-    if (best.C == 0)
+    if (b.C == 0)
         for (int i = 0; i < ncand; ++i) {
             const Plan& c = cand[i];
-            if (double(c.ncl) * c.C >= 0.95 * most && (best.C == 0 || better(c, best))) best = c;
+            if (c.kind == HEADLOSS_KERNEL_RESIDENT && double(c.ncl) * c.C >= 0.95 * most &&
+                (b.C == 0 || better(c, b)))
+                b = c;
         }
-    if (best.C == 0) return HEADLOSS_ERR_SIZE;
+    if (b.C == 0) return false;
+    *best = b;
+    return true;
+}
+
+// Streaming rule (measured on GB300): the per-chunk bookkeeping (slot wait,
+// running-shift update, release) is amortised over the chunk, so the largest
+// chunk per thread wins; then two or more CTAs per SM; then fewer slots (two
+// or three already hide the copy latency).
+bool pick_stream(const headloss* h, const Plan* cand, int ncand, Plan* best) {
+    Plan b;
+    double bscore = -1.0;
+    for (int i = 0; i < ncand; ++i) {
+        const Plan& c = cand[i];
+        if (c.kind != HEADLOSS_KERNEL_STREAM) continue;
+        const double per_sm = double(c.ncl) / h->num_sms;
+        const double score = c.chunk_words * 1e6 + (per_sm >= 2.0 ? 1e3 : 0.0) - c.nbuf;
+        if (score > bscore) {
+            b = c;
+            bscore = score;
+        }
+    }
+    if (bscore < 0) return false;
+    *best = b;
+    return true;
+}
+
+// Chooses the kernel and its launch plan for rows of V elements of `dtype`.
+// The streaming kernel takes 16-bit rows whose resident plan would need a
+// cluster of three or more CTAs (a row too large for one or two SMs); the
+// resident kernel takes everything else.
+int make_plan(headloss* h, int64_t V, int dtype, Plan* out) {
+    const int feat = feature_set(h);
+    if (h->plan.V == V && h->plan.dtype == dtype && h->plan.feat == feat) {
+        *out = h->plan;
+        return HEADLOSS_OK;
+    }
+    Plan cand[2 * MAX_CLUSTER * 2 * MAX_STAGES + 2 * 3 * MAX_STAGES];
+    int ncand = 0;
+    const int fk = h->forced.kernel;
+    int rc = HEADLOSS_OK;
+    if (fk == 0 || fk == HEADLOSS_KERNEL_RESIDENT)
+        rc = resident_candidates(h, V, dtype, feat, cand, &ncand);
+    if (rc) return rc;
+    if (fk == 0 || fk == HEADLOSS_KERNEL_STREAM) rc = stream_candidates(h, V, dtype, feat, cand, &ncand);
+    if (rc) return rc;
+    Plan res, str, best;
+    const bool have_res = pick_resident(h, cand, ncand, &res);
+    const bool have_str = pick_stream(h, cand, ncand, &str);
+    if (fk == HEADLOSS_KERNEL_STREAM) {
+        if (!have_str) return HEADLOSS_ERR_SIZE;
+        best = str;
+    } else if (fk == HEADLOSS_KERNEL_RESIDENT) {
+        if (!have_res) return HEADLOSS_ERR_SIZE;
+        best = res;
+    } else if (have_str && (!have_res || res.C >= 3)) {
+        best = str;
+    } else if (have_res) {
+        best = res;
+    } else {
+        return HEADLOSS_ERR_SIZE;
+    }
     best.V = V;
     best.dtype = dtype;
     best.feat = feat;
-    best.kernel = kernel;
     h->plan = best;
     *out = best;
     return HEADLOSS_OK;
@@ -352,31 +472,38 @@ void headloss_destroy(headloss_t h) {
     delete h;
 }
 
-int headloss_force_plan(headloss_t h, int cluster, int stages, int threads) {
+int headloss_force_plan(headloss_t h, const headloss_plan_desc* plan) {
     if (!h) return HEADLOSS_ERR_ARG;
-    if (cluster < 0 || cluster > MAX_CLUSTER) return HEADLOSS_ERR_ARG;
-    if (stages < 0 || stages > MAX_STAGES) return HEADLOSS_ERR_ARG;
-    if (!(threads == 0 || threads == 256 || threads == 512)) return HEADLOSS_ERR_ARG;
+    headloss_plan_desc d = {0, 0, 0, 0, 0};
+    if (plan) d = *plan;
+    if (d.kernel < 0 || d.kernel > HEADLOSS_KERNEL_STREAM) return HEADLOSS_ERR_ARG;
+    if (d.cluster < 0 || d.cluster > MAX_CLUSTER) return HEADLOSS_ERR_ARG;
+    if (d.stages < 0 || d.stages > MAX_STAGES) return HEADLOSS_ERR_ARG;
+    if (!(d.threads == 0 || d.threads == 256 || d.threads == 512)) return HEADLOSS_ERR_ARG;
+    if (!(d.chunk_words == 0 || d.chunk_words == 1 || d.chunk_words == 2 || d.chunk_words == 4))
+        return HEADLOSS_ERR_ARG;
     std::lock_guard<std::mutex> g(h->mu);
-    h->forced_C = cluster;
-    h->forced_nbuf = stages;
-    h->forced_threads = threads;
+    h->forced = d;
     h->plan = Plan();
     return HEADLOSS_OK;
 }
 
-int headloss_plan(headloss_t h, int64_t V, int dtype, int* cluster, int* stages, int* ctas,
-                  int* threads, int* smem_bytes) {
+int headloss_plan(headloss_t h, int64_t V, int dtype, headloss_plan_desc* plan, int* ctas,
+                  int* smem_bytes) {
     if (!h || V < 1 || V >= (int64_t(1) << 31)) return HEADLOSS_ERR_ARG;
     if (dtype < 0 || dtype > 2) return HEADLOSS_ERR_DTYPE;
     std::lock_guard<std::mutex> g(h->mu);
     Plan pl;
     const int rc = make_plan(h, V, dtype, &pl);
     if (rc) return rc;
-    if (cluster) *cluster = pl.C;
-    if (stages) *stages = pl.nbuf;
+    if (plan) {
+        plan->kernel = pl.kind;
+        plan->cluster = pl.C;
+        plan->stages = pl.nbuf;
+        plan->threads = pl.threads;
+        plan->chunk_words = pl.chunk_words;
+    }
     if (ctas) *ctas = pl.ncl * pl.C;
-    if (threads) *threads = pl.threads;
     if (smem_bytes) *smem_bytes = pl.smem;
     return HEADLOSS_OK;
 }

@@ -75,13 +75,25 @@ __device__ __forceinline__ float hsum(f2 v) {
     return a + b;
 }
 
-// tanh(y) from the identity tanh(y) = 1 - 2 / (exp(2y) + 1), with
-// a2x = 2 * log2(e) * y already formed: one ex2, one rcp.  Exact limits:
-// exp -> inf gives 1, exp -> 0 gives -1.  Absolute error ~3e-7.
-__device__ __forceinline__ f2 tanh_from_ex2_arg(f2 a2x) {
-    const f2 one = pk1(1.f), m2 = pk1(-2.f);
-    const f2 w = add2(ex2p(a2x), one);
-    return fma2(rcpp(w), m2, one);
+// tanh(y) and 1 - tanh(y)^2 from w = exp(2y), r = 1 / (1 + w):
+// tanh = 1 - 2r and 1 - tanh^2 = 4 w r^2, which keeps full relative accuracy
+// where tanh saturates (1 - tanh^2 formed directly would cancel).  The ex2
+// argument a2x = 2 * log2(e) * y is clamped at 64 so w stays finite; tanh is
+// then 1 to fp32 precision and 4 w r^2 ~ 2^-62 (the true value is smaller
+// still).  One ex2 and one rcp per element; absolute tanh error ~3e-7.
+struct TanhD2 {
+    f2 th, omt;  // tanh, 1 - tanh^2
+};
+__device__ __forceinline__ TanhD2 tanh_from_ex2_arg(f2 a2x) {
+    const f2 one = pk1(1.f), m2 = pk1(-2.f), four = pk1(4.f);
+    float a, b;
+    upk(a2x, a, b);
+    const f2 w = pk(ex2f(fminf(a, 64.f)), ex2f(fminf(b, 64.f)));
+    const f2 r = rcpp(add2(w, one));
+    TanhD2 o;
+    o.th = fma2(r, m2, one);
+    o.omt = mul2(mul2(w, r), mul2(r, four));
+    return o;
 }
 
 // ---- 16-bit storage formats: a 32-bit word holds elements (2i, 2i+1) ----

@@ -24,7 +24,8 @@ enum : int { E_LABEL = 1, E_TIMEOUT = 2 };
 constexpr int THREADS = 512;  // maximum threads per CTA (a plan may launch 256)
 constexpr int NWARPS = THREADS / 32;
 constexpr int MAX_CLUSTER = 8;
-constexpr int MAX_STAGES = 4;
+constexpr int MAX_STAGES = 8;          // mbarrier slots (streaming ring)
+constexpr int MAX_RESIDENT_STAGES = 4; // row stages of the resident kernel
 
 // Partial-statistics record one CTA contributes for one row (all base-2
 // units; see the row kernel for definitions).

@@ -133,6 +133,8 @@ __device__ __forceinline__ float ex(float x) { return expf(x); }
 __device__ __forceinline__ double ex(double x) { return exp(x); }
 __device__ __forceinline__ float tnh(float x) { return tanhf(x); }
 __device__ __forceinline__ double tnh(double x) { return tanh(x); }
+__device__ __forceinline__ float csh(float x) { return coshf(x); }
+__device__ __forceinline__ double csh(double x) { return cosh(x); }
 __device__ __forceinline__ float amax(float a, float b) { return fmaxf(a, b); }
 // Uncontracted multiply / subtract: the statistics pass must reproduce the
 // row maximum exactly (its shifted logit is exactly 0), which an FMA that
@@ -228,7 +230,8 @@ struct DTraits<float> {
 // reduction scratch, row coefficients), for an accumulator of `acc_bytes`.
 __host__ __device__ constexpr int smem_fixed_bytes(int acc_bytes) {
     return 8 * MAX_STAGES + 8 * NACC +
-           acc_bytes * (2 * MAX_CLUSTER * NREC + NWARPS * NREC + 2 * NWARPS + 16);
+           acc_bytes * (2 * MAX_CLUSTER * NREC + NWARPS * NREC + 2 * NWARPS + 16) +
+           4 * MAX_STAGES;
 }
 
 // ---------------------------------------------------------- reductions ----

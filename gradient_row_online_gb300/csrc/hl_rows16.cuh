@@ -29,14 +29,18 @@ struct BoolC {
     static constexpr bool value = B;
 };
 
-// Scalar twin of the packed element math, for the partial words.
-__device__ __forceinline__ float tanh_a2x_1(float a2x) {
-    const float w = ex2f(a2x) + 1.f;
-    return fmaf(rcpf(w), -2.f, 1.f);
+// Scalar twin of the packed element math, for the partial words: tanh and
+// 1 - tanh^2 from w = exp(2y), r = 1 / (1 + w) (see tanh_from_ex2_arg).
+__device__ __forceinline__ float tanh_a2x_1(float a2x, float* omt = nullptr) {
+    const float w = ex2f(fminf(a2x, 64.f));
+    const float r = rcpf(w + 1.f);
+    if (omt) *omt = (w * r) * (4.f * r);
+    return fmaf(r, -2.f, 1.f);
 }
 
-// tanh(y) = y * P(y^2) on |y| <= HL_TANH_POLY_Y0 (FMA pipe only).
-__device__ __forceinline__ f2 tanh_poly2(f2 y) {
+// tanh(y) = y * P(y^2) on |y| <= HL_TANH_POLY_Y0 (FMA pipe only); there
+// |tanh| <= 0.67, so 1 - tanh^2 has no cancellation to fear.
+__device__ __forceinline__ TanhD2 tanh_poly2(f2 y) {
     const f2 u = mul2(y, y);
     f2 q = fma2(u, pk1(HL_TANH_POLY_C6), pk1(HL_TANH_POLY_C5));
     q = fma2(q, u, pk1(HL_TANH_POLY_C4));
@@ -44,7 +48,10 @@ __device__ __forceinline__ f2 tanh_poly2(f2 y) {
     q = fma2(q, u, pk1(HL_TANH_POLY_C2));
     q = fma2(q, u, pk1(HL_TANH_POLY_C1));
     q = fma2(q, u, pk1(1.f));
-    return mul2(y, q);
+    TanhD2 o;
+    o.th = mul2(y, q);
+    o.omt = fma2(o.th, mul2(o.th, pk1(-1.f)), pk1(1.f));
+    return o;
 }
 
 // Row coefficients, identical in every lane of the calling warp.
@@ -92,7 +99,7 @@ __device__ RowCoef row_epilogue16(const Params& p, const float* recs, int C, boo
     }
     if (have && r[R_HASY] > 0.f) c[7] = r[R_ZY];
 #pragma unroll
-    for (int o = 4; o; o >>= 1)
+    for (int o = 16; o; o >>= 1)  // up to 32 records (one per warp of a streaming CTA)
 #pragma unroll
         for (int i = 0; i < 8; ++i) c[i] += __shfl_xor_sync(0xffffffffu, c[i], o);
     // lane 0's sums (a fixed order) define the row for the whole warp
@@ -258,7 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
         return CAP ? __fmul_rn(tanh_a2x_1(__fmul_rn(v, A2)), Kc) : __fmul_rn(v, K);
     };
     // tanh(x / c) of a pair, by the polynomial or by ex2 + rcp
-    auto th2 = [&](f2 xv, auto poly) -> f2 {
+    auto th2 = [&](f2 xv, auto poly) -> TanhD2 {
         if constexpr (decltype(poly)::value) return tanh_poly2(mul2(xv, invc2));
         else return tanh_from_ex2_arg(mul2(xv, A22));
     };
@@ -440,7 +447,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                         for (int kk = 0; kk < 4; ++kk) {
                             const f2 xv = P16::unpack(xa[kk]);
                             // d = zs - zm; under softcap one fma: Kc * th - Kc
-                            const f2 d = CAP ? fma2(th2(xv, polyc), Kc2, nzm2)
+                            const f2 d = CAP ? fma2(th2(xv, polyc).th, Kc2, nzm2)
                                              : sub2(mul2(xv, K2), zm2);
                             const f2 e = ex2p(d);
                             S2 = add2(S2, e);
@@ -546,9 +553,11 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk) {
                                 const f2 xv = P16::unpack(xa[kk]);
-                                f2 th = z2, arg, argT = z2;
+                                f2 th = z2, omt = z2, arg, argT = z2;
                                 if (CAP) {
-                                    th = th2(xv, polyc);
+                                    const TanhD2 td = th2(xv, polyc);
+                                    th = td.th;
+                                    omt = td.omt;
                                     arg = fma2(th, Kc2, nlse2);  // zs - lse2
                                     if (TEACH) argT = fma2(th, KcT2, nlseT2);
                                 } else {
@@ -578,7 +587,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                                     else gl -= k.bc;
                                     g = pk(gl, gh);
                                 }
-                                if (CAP) g = mul2(g, fma2(mul2(th, th), ns2, s2));  // dz/dx
+                                if (CAP) g = mul2(g, mul2(omt, s2));  // dz/dx = s (1 - tanh^2)
                                 out[kk] = P16::pack(g);
                             }
                             *reinterpret_cast<uint4*>(gg + eb) =
@@ -589,9 +598,10 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                                 const float xv = P16::to_f(xs[w * EPW + i]);
                                 float zs, dz = 1.f;
                                 if (CAP) {
-                                    const float th = tanh_a2x_1(__fmul_rn(xv, A2));
+                                    float omt;
+                                    const float th = tanh_a2x_1(__fmul_rn(xv, A2), &omt);
                                     zs = __fmul_rn(th, Kc);
-                                    dz = fmaf(th * th, -s, s);
+                                    dz = s * omt;
                                 } else {
                                     zs = __fmul_rn(xv, K);
                                 }

@@ -285,7 +285,8 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
                         if (CAP) {
                             const A th = tnh(v[i] * invc);
                             zs = th * Kc;
-                            dz = s - s * th * th;
+                            const A ch = csh(v[i] * invc);  // 1 - tanh^2 = 1 / cosh^2, no cancellation
+                            dz = s / (ch * ch);
                         } else {
                             zs = v[i] * K;
                         }

@@ -1,0 +1,485 @@
+// hl_stream16.cuh -- the streaming row kernel for bf16 / fp16 logits.
+//
+// One CTA owns whole rows; no cluster, so no CTA ever waits for another SM.
+// A row is streamed through a ring of shared-memory chunk slots twice:
+//
+//   pass 1  chunks 0 .. K-1: online row statistics.  Each thread keeps its
+//           own running shifts (student max -- or s*c*log2e under softcap --
+//           and teacher max) and rescales its sums when a shift moves;
+//   merge   the thread records merge across the warp (butterfly), then across
+//           the CTA's warps, and warp 0 derives the row's losses and gradient
+//           coefficients (the same epilogue as the resident kernel);
+//   pass 2  chunks K-1 .. 0 (reverse order, so the chunks read most recently
+//           -- the ones most likely still in L2 -- come back first): the
+//           combined gradient, written once from registers.
+//
+// The chunk stream (row, pass, chunk) is one sequence per CTA; a thread of
+// the last warp to finish a chunk issues the bulk copy of the entry that
+// reuses its slot, so copies for the next row start while this row finishes.
+// The second read of a row is served by L2 when the row's chunks are still
+// resident; the DRAM bytes it costs are measured, not assumed.
+//
+// Rows must be 16-byte aligned (V * 2 a multiple of 16); the planner sends
+// other shapes to the resident kernel, which handles ragged rows.
+#pragma once
+#include "hl_rows16.cuh"
+
+namespace hl {
+
+// Thread-local partial statistics of a row (the resident kernel's record in
+// registers): shifts zm (student, base 2) and um (teacher), and the sums.
+struct TRec {
+    float zm, um, S, E, ST, Sq, Eq, Xp, Y, zy, hasy;
+};
+
+// Merges b into a (commutative: a + b and b + a give identical results).
+template <bool TEACH, bool RKL, bool ENT>
+__device__ __forceinline__ void trec_merge(TRec& a, const TRec& b, float invT) {
+    const bool la = a.S > 0.f, lb = b.S > 0.f;
+    const float M = fmaxf(la ? a.zm : -CUDART_INF_F, lb ? b.zm : -CUDART_INF_F);
+    const float da = la ? a.zm - M : 0.f, db = lb ? b.zm - M : 0.f;
+    const float aa = la ? exp2f(da) : 0.f, ab = lb ? exp2f(db) : 0.f;
+    TRec o;
+    o.zm = (la || lb) ? M : a.zm;
+    o.S = aa * a.S + ab * b.S;
+    o.E = ENT ? aa * (a.E + da * a.S) + ab * (b.E + db * b.S) : 0.f;
+    o.zy = a.zy + b.zy;
+    o.hasy = a.hasy + b.hasy;
+    if (TEACH) {
+        const float Mu = fmaxf(la ? a.um : -CUDART_INF_F, lb ? b.um : -CUDART_INF_F);
+        const float dua = la ? a.um - Mu : 0.f, dub = lb ? b.um - Mu : 0.f;
+        const float ba = la ? exp2f(dua) : 0.f, bb = lb ? exp2f(dub) : 0.f;
+        const float dTa = da * invT, dTb = db * invT;
+        const float ta = la ? exp2f(dTa) : 0.f, tb = lb ? exp2f(dTb) : 0.f;
+        o.um = (la || lb) ? Mu : a.um;
+        o.ST = ta * a.ST + tb * b.ST;
+        o.Sq = ba * a.Sq + bb * b.Sq;
+        o.Eq = ba * (a.Eq + dua * a.Sq) + bb * (b.Eq + dub * b.Sq);
+        o.Xp = ba * (a.Xp + (dua - dTa) * a.Sq) + bb * (b.Xp + (dub - dTb) * b.Sq);
+        o.Y = RKL ? ta * (a.Y - (dua - dTa) * a.ST) + tb * (b.Y - (dub - dTb) * b.ST) : 0.f;
+    } else {
+        o.um = a.um;
+        o.ST = o.Sq = o.Eq = o.Xp = o.Y = 0.f;
+    }
+    a = o;
+}
+
+__device__ __forceinline__ TRec trec_shfl_xor(const TRec& a, int o) {
+    TRec b;
+    b.zm = __shfl_xor_sync(0xffffffffu, a.zm, o);
+    b.um = __shfl_xor_sync(0xffffffffu, a.um, o);
+    b.S = __shfl_xor_sync(0xffffffffu, a.S, o);
+    b.E = __shfl_xor_sync(0xffffffffu, a.E, o);
+    b.ST = __shfl_xor_sync(0xffffffffu, a.ST, o);
+    b.Sq = __shfl_xor_sync(0xffffffffu, a.Sq, o);
+    b.Eq = __shfl_xor_sync(0xffffffffu, a.Eq, o);
+    b.Xp = __shfl_xor_sync(0xffffffffu, a.Xp, o);
+    b.Y = __shfl_xor_sync(0xffffffffu, a.Y, o);
+    b.zy = __shfl_xor_sync(0xffffffffu, a.zy, o);
+    b.hasy = __shfl_xor_sync(0xffffffffu, a.hasy, o);
+    return b;
+}
+
+template <typename DT, int FEAT>
+__global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_constant__ Params p) {
+    using P16 = Pack16<DT>;
+    constexpr int EPW = 8;
+    constexpr int ES = 2;
+    constexpr bool TEACH = (FEAT & F_TEACH) != 0;
+    constexpr bool RKL = (FEAT & F_RKL) != 0;
+    constexpr bool ENT = (FEAT & F_ENT) != 0;
+    constexpr bool CAP = (FEAT & F_SOFTCAP) != 0;
+    constexpr int OPS = TEACH ? 2 : 1;
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nthr = int(blockDim.x), nwarps = nthr >> 5;
+    const int S = p.nbuf;                 // chunk slots in the ring
+    const int CH = int(p.L);              // elements per chunk (a multiple of 8 * nthr)
+    const uint32_t opbytes = uint32_t(CH) * ES;
+    const uint32_t slot_bytes = opbytes * OPS;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(slot_bytes) * S);
+    double* acc = reinterpret_cast<double*>(bars + MAX_STAGES);
+    float* xch = reinterpret_cast<float*>(acc + NACC);  // per-warp records of a row
+    float* red = xch + 2 * MAX_CLUSTER * NREC;
+    float* redmax = red + NWARPS * NREC;
+    float* coefs = redmax + 2 * NWARPS;
+    int* done = reinterpret_cast<int*>(coefs + 16);     // [MAX_STAGES] warps finished per slot
+    (void)red;
+
+    const int64_t N = p.N, V = p.V;
+    const int K = int((V + CH - 1) / CH);                // chunks per row
+    const int64_t G = gridDim.x;
+    const DT* __restrict__ xg = static_cast<const DT*>(p.x);
+    const DT* __restrict__ tg = static_cast<const DT*>(p.t);
+    DT* gg = static_cast<DT*>(p.g);
+
+    const float LOG2E = 1.4426950408889634f;
+    const float s = p.s;
+    const float K1 = s * LOG2E;
+    const float invc = CAP ? 1.f / p.softcap : 0.f;
+    const float A2 = CAP ? 2.f * LOG2E * invc : 0.f;
+    const float Kc = CAP ? s * p.softcap * LOG2E : 0.f;
+    const float invT = 1.f / p.T;
+    const float KT = LOG2E * invT;
+    // softcap: the student shift is the constant Kc unless exp(-2 Kc) could
+    // underflow, in which case it follows the running max like the teacher
+    const bool fixed_shift = CAP && Kc <= 60.f;
+    const f2 K2 = pk1(K1), A22 = pk1(A2), Kc2 = pk1(Kc), invT2 = pk1(invT), KT2 = pk1(KT);
+    const f2 invc2 = pk1(invc), KcT2 = pk1(Kc * invT);
+    const f2 z2 = pk1(0.f);
+
+    auto zs1 = [&](float v) -> float {
+        return CAP ? __fmul_rn(tanh_a2x_1(__fmul_rn(v, A2)), Kc) : __fmul_rn(v, K1);
+    };
+    auto th2 = [&](f2 xv, auto poly) -> TanhD2 {
+        if constexpr (decltype(poly)::value) return tanh_poly2(mul2(xv, invc2));
+        else return tanh_from_ex2_arg(mul2(xv, A22));
+    };
+
+    // stream entry J -> (row, chunk); pass 1 then pass 2 (reverse) per row
+    const int64_t per_row = 2 * int64_t(K);
+    auto entry = [&](int64_t J, int64_t& r, int& c) {
+        const int64_t it = J / per_row;
+        const int jl = int(J - it * per_row);
+        c = jl < K ? jl : 2 * K - 1 - jl;
+        r = int64_t(blockIdx.x) + it * G;
+    };
+    auto issue = [&](int64_t J) {
+        int64_t r;
+        int c;
+        entry(J, r, c);
+        if (r >= N) return;
+        const int sl = int(J % S);
+        const uint32_t bar = smem_addr(&bars[sl]);
+        const int64_t c0 = int64_t(c) * CH;
+        const int64_t len = (V - c0) < CH ? (V - c0) : CH;
+        const uint32_t bytes = uint32_t(len * ES);
+        fence_proxy_async();
+        mbar_arrive_expect_tx(bar, bytes * OPS);
+        const uint32_t dst = smem_addr(smem + size_t(sl) * slot_bytes);
+        bulk_g2s(dst, xg + r * V + c0, bytes, bar);
+        if (TEACH) bulk_g2s(dst + opbytes, tg + r * V + c0, bytes, bar);
+    };
+
+    if (tid == 0) {
+        for (int b = 0; b < S; ++b) {
+            mbar_init(smem_addr(&bars[b]), 1);
+            done[b] = 0;
+        }
+        fence_mbar_init();
+        for (int i = 0; i < NACC; ++i) acc[i] = 0.0;
+    }
+    __syncthreads();
+    if (tid == 0)
+        for (int j = 0; j < S; ++j) issue(j);
+
+    int64_t J = 0;  // stream entries consumed by this thread
+    uint32_t lost = 0, lost_par = 0;  // slots (and phase parities) whose wait gave up
+    // wait for entry J's slot; returns its shared-memory base
+    auto acquire = [&](int64_t jj) -> const unsigned char* {
+        const int sl = int(jj % S);
+        const uint32_t par = uint32_t((jj / S) & 1);
+        if (!mbar_wait_bounded(smem_addr(&bars[sl]), par)) {
+            lost |= 1u << sl;
+            lost_par = (lost_par & ~(1u << sl)) | (par << sl);
+            if (lane == 0) atomicOr(p.err, E_TIMEOUT);
+        }
+        return smem + size_t(sl) * slot_bytes;
+    };
+    // this warp is done with entry jj; the last warp refills the slot
+    auto release = [&](int64_t jj) {
+        __syncwarp();
+        if (lane == 0) {
+            const int sl = int(jj % S);
+            __threadfence_block();
+            const int old = atomicAdd(&done[sl], 1);
+            if (old + 1 == int((jj / S) + 1) * nwarps) {
+                __threadfence_block();
+                issue(jj + S);
+            }
+        }
+    };
+
+    const bool has_labels = p.labels != nullptr;
+    const bool need_side = (p.flags & (L_GRPO | L_GRPO_STATS)) != 0;
+    const int WPT = CH / (EPW * nthr);  // words per thread per chunk (full chunks)
+
+    for (int64_t r = blockIdx.x; r < N; r += G) {
+        const int64_t y = has_labels ? p.labels[r] : 0;
+        const float old_lp = need_side ? p.old_lp[r] : 0.f;
+        const float adv = need_side ? p.adv[r] : 0.f;
+        const bool valid = !has_labels || (y >= 0 && y < V);
+        if (has_labels && y >= V && tid == 0) atomicOr(p.err, E_LABEL);
+
+        if (!valid) {  // a masked row: consume its entries, write exact +0
+            for (int c = 0; c < 2 * K; ++c, ++J) {
+                acquire(J);
+                const int cc = c < K ? c : 2 * K - 1 - c;
+                if (c >= K && gg != nullptr) {
+                    const int64_t c0 = int64_t(cc) * CH;
+                    const int nwc = int(((V - c0) < CH ? (V - c0) : CH) / EPW);
+                    for (int w = tid; w < nwc; w += nthr)
+                        *reinterpret_cast<uint4*>(gg + r * V + c0 + int64_t(w) * EPW) =
+                            make_uint4(0, 0, 0, 0);
+                }
+                release(J);
+            }
+            continue;
+        }
+
+        // ---------------- pass 1: online statistics ----------------
+        float xm = -CUDART_INF_F, tm = -CUDART_INF_F;  // running raw maxima
+        float zm = fixed_shift ? Kc : -CUDART_INF_F, um = -CUDART_INF_F;
+        float amax = 0.f;  // softcap: running max |x|
+        f2 S2 = z2, E2 = z2, ST2 = z2, Sq2 = z2, Eq2 = z2, Xp2 = z2, Y2 = z2;
+        float zy = 0.f, hasy = 0.f;
+        int needexp = 0;  // softcap: some chunk of this thread's fell outside the polynomial range
+        for (int c = 0; c < K; ++c, ++J) {
+            const unsigned char* sb = acquire(J);
+            const int64_t c0 = int64_t(c) * CH;
+            const int nwc = int(((V - c0) < CH ? (V - c0) : CH) / EPW);
+            uint4 xw[4], tw[4];
+            int nmine = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int w = tid + i * nthr;
+                if (i < WPT && w < nwc) {
+                    xw[i] = *reinterpret_cast<const uint4*>(sb + size_t(w) * 16);
+                    if (TEACH) tw[i] = *reinterpret_cast<const uint4*>(sb + opbytes + size_t(w) * 16);
+                    nmine = i + 1;
+                }
+            }
+            // chunk maxima of this thread's words (packed), then the running shifts
+            uint32_t mx = CAP ? 0u : P16::NEG_INF2, mt = P16::NEG_INF2;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (i < nmine) {
+                    uint4 a = xw[i];
+                    if (CAP) {
+                        a.x &= 0x7fff7fffu;
+                        a.y &= 0x7fff7fffu;
+                        a.z &= 0x7fff7fffu;
+                        a.w &= 0x7fff7fffu;
+                    }
+                    mx = P16::max2(P16::max2(mx, a.x), P16::max2(a.y, a.z));
+                    mx = P16::max2(mx, a.w);
+                    if (TEACH) {
+                        mt = P16::max2(P16::max2(mt, tw[i].x), P16::max2(tw[i].y, tw[i].z));
+                        mt = P16::max2(mt, tw[i].w);
+                    }
+                }
+            }
+            float ca, cb;
+            upk(P16::unpack(mx), ca, cb);
+            const float cx = fmaxf(ca, cb);
+            float newz = zm, newu = um;
+            if (CAP) amax = fmaxf(amax, cx);
+            if (!fixed_shift) {
+                // without softcap the chunk max is the raw max; under a large
+                // softcap the bound of |x| bounds z as well
+                xm = fmaxf(xm, cx);
+                newz = nmine ? zs1(xm) : zm;
+            }
+            if (TEACH) {
+                upk(P16::unpack(mt), ca, cb);
+                tm = fmaxf(tm, fmaxf(ca, cb));
+                newu = nmine ? __fmul_rn(tm, KT) : um;
+            }
+            // rescale the sums when a shift moved (warp-uniform decision)
+            const bool moved = (newz != zm) || (TEACH && newu != um);
+            if (__any_sync(0xffffffffu, moved)) {
+                const float d = (zm == -CUDART_INF_F) ? 0.f : zm - newz;
+                const float du = (um == -CUDART_INF_F) ? 0.f : um - newu;
+                const float al = exp2f(d), dTv = d * invT;
+                const f2 al2 = pk1(al), d2 = pk1(d);
+                if (ENT) E2 = mul2(al2, fma2(d2, S2, E2));
+                S2 = mul2(al2, S2);
+                if (TEACH) {
+                    const float alT = exp2f(dTv), be = exp2f(du);
+                    const f2 alT2 = pk1(alT), be2 = pk1(be), du2 = pk1(du);
+                    const f2 w2 = pk1(du - dTv);
+                    Xp2 = mul2(be2, fma2(w2, Sq2, Xp2));
+                    Eq2 = mul2(be2, fma2(du2, Sq2, Eq2));
+                    if (RKL) Y2 = mul2(alT2, fma2(w2, ST2, Y2));
+                    ST2 = mul2(alT2, ST2);
+                    Sq2 = mul2(be2, Sq2);
+                }
+                zm = newz;
+                um = newu;
+            }
+            // the polynomial tanh covers these words when max |x| / c is in range
+            const bool poly_ok = !CAP || __fmul_rn(cx, invc) <= HL_TANH_POLY_Y0;
+            const bool use_poly = CAP && __all_sync(0xffffffffu, poly_ok);
+            if (CAP && !use_poly) needexp = 1;
+            const f2 zm2 = pk1(zm), um2 = pk1(um), nzm2 = pk1(-zm);
+            auto sums = [&](auto polyc) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (i >= nmine) continue;
+                    const uint32_t xa[4] = {xw[i].x, xw[i].y, xw[i].z, xw[i].w};
+                    const uint32_t tb[4] = {tw[i].x, tw[i].y, tw[i].z, tw[i].w};
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const f2 xv = P16::unpack(xa[kk]);
+                        const f2 d = CAP ? fma2(th2(xv, polyc).th, Kc2, nzm2) : sub2(mul2(xv, K2), zm2);
+                        const f2 e = ex2p(d);
+                        S2 = add2(S2, e);
+                        if (ENT) E2 = fma2(e, d, E2);
+                        if (TEACH) {
+                            const f2 dT = mul2(d, invT2);
+                            const f2 eT = ex2p(dT);
+                            ST2 = add2(ST2, eT);
+                            const f2 du = sub2(mul2(P16::unpack(tb[kk]), KT2), um2);
+                            const f2 eq = ex2p(du);
+                            Sq2 = add2(Sq2, eq);
+                            Eq2 = fma2(eq, du, Eq2);
+                            const f2 wd = sub2(du, dT);
+                            Xp2 = fma2(eq, wd, Xp2);
+                            if (RKL) Y2 = fma2(eT, wd, Y2);
+                        }
+                    }
+                }
+            };
+            if (use_poly) sums(BoolC<true>{});
+            else sums(BoolC<false>{});
+            // the label column's logit, from the thread that holds it
+            if (has_labels && y >= c0 && y < c0 + int64_t(nwc) * EPW) {
+                const int wl = int((y - c0) / EPW);
+                if ((wl - tid) % nthr == 0 && wl >= tid) {
+                    zy = zs1(P16::to_f(reinterpret_cast<const uint16_t*>(sb)[y - c0]));
+                    hasy = 1.f;
+                }
+            }
+            release(J);
+        }
+
+        // ---------------- merge: threads -> warps -> row ----------------
+        TRec tr;
+        tr.zm = zm;
+        tr.um = um;
+        tr.S = hsum(S2);
+        tr.E = hsum(E2);
+        tr.ST = hsum(ST2);
+        tr.Sq = hsum(Sq2);
+        tr.Eq = hsum(Eq2);
+        tr.Xp = hsum(Xp2);
+        tr.Y = -hsum(Y2);
+        tr.zy = zy;
+        tr.hasy = hasy;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) trec_merge<TEACH, RKL, ENT>(tr, trec_shfl_xor(tr, o), invT);
+        if (lane == 0) {
+            float* rec = xch + warp * NREC;
+            rec[R_ZM] = tr.zm;
+            rec[R_UM] = tr.um;
+            rec[R_S] = tr.S;
+            rec[R_E] = tr.E;
+            rec[R_ST] = tr.ST;
+            rec[R_SQ] = tr.Sq;
+            rec[R_EQ] = tr.Eq;
+            rec[R_XP] = tr.Xp;
+            rec[R_Y] = tr.Y;
+            rec[R_ZY] = tr.zy;
+            rec[R_HASY] = tr.hasy;
+        }
+        // the barrier also ORs "some chunk needed the exp tanh" over the CTA
+        const bool row_exp = __syncthreads_or(CAP && needexp) != 0;
+        if (warp == 0) {
+            const RowCoef kw =
+                row_epilogue16<TEACH, RKL, ENT, CAP>(p, xch, nwarps, true, old_lp, adv, acc, lane);
+            if (lane == 0) *reinterpret_cast<RowCoef*>(coefs) = kw;
+        }
+        __syncthreads();
+        const RowCoef k = *reinterpret_cast<const RowCoef*>(coefs);
+
+        // ---------------- pass 2: the gradient, reverse chunk order ----------------
+        const float dlse = k.lseT2 - k.lsq2;
+        const f2 nlse2 = pk1(-k.lse2), nlseT2 = pk1(-k.lseT2), nlsq2 = pk1(-k.lsq2);
+        const f2 pc2 = pk1(k.pc), ps2 = pk1(k.ps), tc2 = pk1(k.tc), ts2 = pk1(k.ts);
+        const f2 qc2 = pk1(k.qc), s2 = pk1(s), ns2 = pk1(-s), ndlse2 = pk1(-dlse);
+        const f2 nKT2 = pk1(-KT);
+        for (int cr = 0; cr < K; ++cr, ++J) {
+            const int c = K - 1 - cr;
+            const unsigned char* sb = acquire(J);
+            if (gg != nullptr) {
+                const int64_t c0 = int64_t(c) * CH;
+                const int nwc = int(((V - c0) < CH ? (V - c0) : CH) / EPW);
+                const int64_t wy = (has_labels && y >= c0 && y < c0 + int64_t(nwc) * EPW)
+                                       ? (y - c0) / EPW : -1;
+                const int iy = int((y - c0) % EPW);
+                auto grad = [&](auto polyc) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int w = tid + i * nthr;
+                        if (i >= WPT || w >= nwc) continue;
+                        const uint4 a = *reinterpret_cast<const uint4*>(sb + size_t(w) * 16);
+                        uint4 b = make_uint4(0, 0, 0, 0);
+                        if (TEACH) b = *reinterpret_cast<const uint4*>(sb + opbytes + size_t(w) * 16);
+                        const uint32_t xa[4] = {a.x, a.y, a.z, a.w};
+                        const uint32_t tb[4] = {b.x, b.y, b.z, b.w};
+                        uint32_t out[4];
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const f2 xv = P16::unpack(xa[kk]);
+                            f2 th = z2, omt = z2, arg, argT = z2;
+                            if (CAP) {
+                                const TanhD2 td = th2(xv, polyc);
+                                th = td.th;
+                                omt = td.omt;
+                                arg = fma2(th, Kc2, nlse2);
+                                if (TEACH) argT = fma2(th, KcT2, nlseT2);
+                            } else {
+                                const f2 zs = mul2(xv, K2);
+                                arg = add2(zs, nlse2);
+                                if (TEACH) argT = fma2(zs, invT2, nlseT2);
+                            }
+                            f2 g = mul2(ex2p(arg), ENT ? fma2(ps2, arg, pc2) : pc2);
+                            if (TEACH) {
+                                const f2 tv = P16::unpack(tb[kk]);
+                                const f2 pT = ex2p(argT);
+                                const f2 q = ex2p(fma2(tv, KT2, nlsq2));
+                                f2 tco = tc2;
+                                if (RKL) {
+                                    const f2 dxu = CAP ? fma2(th, KcT2, mul2(tv, nKT2))
+                                                       : mul2(fma2(xv, s2, sub2(z2, tv)), KT2);
+                                    tco = fma2(ts2, add2(dxu, ndlse2), tc2);
+                                }
+                                g = fma2(pT, tco, g);
+                                g = fma2(q, qc2, g);
+                            }
+                            if (w == wy && (iy >> 1) == kk) {
+                                float gl, gh;
+                                upk(g, gl, gh);
+                                if (iy & 1) gh -= k.bc;
+                                else gl -= k.bc;
+                                g = pk(gl, gh);
+                            }
+                            if (CAP) g = mul2(g, mul2(omt, s2));  // dz/dx = s (1 - tanh^2)
+                            out[kk] = P16::pack(g);
+                        }
+                        *reinterpret_cast<uint4*>(gg + r * V + c0 + int64_t(w) * EPW) =
+                            make_uint4(out[0], out[1], out[2], out[3]);
+                    }
+                };
+                if (CAP && !row_exp) grad(BoolC<true>{});
+                else grad(BoolC<false>{});
+            }
+            release(J);
+        }
+    }
+
+    // a slot whose wait gave up may still receive its copy: wait once more
+    // (bounded) before the CTA's shared memory goes away
+    if (lost && tid == 0) {
+        for (int b = 0; b < S; ++b)
+            if (lost & (1u << b)) (void)mbar_wait_bounded(smem_addr(&bars[b]), (lost_par >> b) & 1u);
+    }
+    if (tid == 0) {
+        double* out = p.partials + size_t(blockIdx.x) * NACC;
+#pragma unroll
+        for (int i = 0; i < NACC; ++i) out[i] = acc[i];
+    }
+}
+
+}  // namespace hl

@@ -51,6 +51,16 @@ EXPORTS = ("headloss_create", "headloss_forward_backward", "headloss_get_device_
            "headloss_destroy", "headloss_strerror", "headloss_version")
 
 
+# enum headloss_kernel
+HEADLOSS_KERNEL_AUTO, HEADLOSS_KERNEL_RESIDENT, HEADLOSS_KERNEL_STREAM = 0, 1, 2
+KERNELS = {0: "auto", 1: "resident", 2: "stream"}
+
+
+class headloss_plan_desc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("kernel", "cluster", "stages", "threads",
+                                             "chunk_words")]
+
+
 class headloss_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_float) for n in
                 ("ce", "z", "dist_ce", "fkl", "rkl", "grpo", "entropy", "grad_scale")]
@@ -83,9 +93,10 @@ def load_library(path: str = LIB_PATH):
     lib.headloss_forward_backward.restype = i32
     lib.headloss_get_device_error.argtypes = [vp, vp, ip]
     lib.headloss_get_device_error.restype = i32
-    lib.headloss_plan.argtypes = [vp, i64, i32, ip, ip, ip, ip, ip]
+    pp = ctypes.POINTER(headloss_plan_desc)
+    lib.headloss_plan.argtypes = [vp, i64, i32, pp, ip, ip]
     lib.headloss_plan.restype = i32
-    lib.headloss_force_plan.argtypes = [vp, i32, i32, i32]
+    lib.headloss_force_plan.argtypes = [vp, pp]
     lib.headloss_force_plan.restype = i32
     lib.headloss_launches_per_call.argtypes = []
     lib.headloss_launches_per_call.restype = i32
@@ -174,16 +185,20 @@ def headloss_get_device_error(h, stream=None) -> int:
 
 def headloss_plan(h, V: int, dtype: int) -> dict:
     lib = load_library()
-    vals = [ctypes.c_int() for _ in range(5)]
-    _check(lib.headloss_plan(h, int(V), int(dtype), *[ctypes.byref(v) for v in vals]),
-           "headloss_plan")
-    return dict(zip(("cluster", "stages", "ctas", "threads", "smem_bytes"),
-                    (v.value for v in vals)))
+    d = headloss_plan_desc()
+    ctas, smem = ctypes.c_int(), ctypes.c_int()
+    _check(lib.headloss_plan(h, int(V), int(dtype), ctypes.byref(d), ctypes.byref(ctas),
+                             ctypes.byref(smem)), "headloss_plan")
+    return dict(kernel=KERNELS[d.kernel], cluster=d.cluster, stages=d.stages,
+                threads=d.threads, chunk_words=d.chunk_words, ctas=ctas.value,
+                smem_bytes=smem.value)
 
 
-def headloss_force_plan(h, cluster: int, stages: int, threads: int = 0) -> None:
-    _check(load_library().headloss_force_plan(h, int(cluster), int(stages), int(threads)),
-           "headloss_force_plan")
+def headloss_force_plan(h, kernel: int = 0, cluster: int = 0, stages: int = 0, threads: int = 0,
+                        chunk_words: int = 0) -> None:
+    """Pin plan choices (0 = the planner decides); all zero restores the automatic plan."""
+    d = headloss_plan_desc(int(kernel), int(cluster), int(stages), int(threads), int(chunk_words))
+    _check(load_library().headloss_force_plan(h, ctypes.byref(d)), "headloss_force_plan")
 
 
 def headloss_launches_per_call() -> int:
@@ -225,8 +240,9 @@ class HeadLoss:
     def plan(self, V: int, dtype: int) -> dict:
         return headloss_plan(self.h, V, dtype)
 
-    def force_plan(self, cluster: int, stages: int, threads: int = 0) -> None:
-        headloss_force_plan(self.h, cluster, stages, threads)
+    def force_plan(self, kernel: int = 0, cluster: int = 0, stages: int = 0, threads: int = 0,
+                   chunk_words: int = 0) -> None:
+        headloss_force_plan(self.h, kernel, cluster, stages, threads, chunk_words)
 
     def device_error(self, stream=None) -> int:
         return headloss_get_device_error(self.h, stream)

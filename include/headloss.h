@@ -164,22 +164,43 @@ int headloss_forward_backward(headloss_t h, const void* logits, int64_t N, int64
  */
 int headloss_get_device_error(headloss_t h, headloss_stream_t stream, int* err);
 
-/*
- * headloss_plan -- the launch plan a call with (V, dtype) would use:
- * cluster size (CTAs sharing one row), row stages buffered per CTA, CTAs
- * launched, threads per CTA, dynamic shared memory per CTA.  Any pointer may
- * be NULL.  Errors: ERR_ARG, ERR_DTYPE, ERR_SIZE, ERR_CUDA.
- */
-int headloss_plan(headloss_t h, int64_t V, int dtype, int* cluster, int* stages, int* ctas,
-                  int* threads, int* smem_bytes);
+/* The two row kernels a plan may use. */
+enum headloss_kernel {
+    HEADLOSS_KERNEL_AUTO = 0,
+    /* A thread-block cluster holds each row in shared memory (each CTA a
+     * column slice, statistics merged over DSMEM): every byte of logits is
+     * read from HBM once.  Any dtype, any V up to its shared-memory limit. */
+    HEADLOSS_KERNEL_RESIDENT = 1,
+    /* One CTA streams each row through a ring of chunk slots twice
+     * (statistics, then gradient in reverse chunk order so the second read
+     * finds the row in L2).  bf16 / fp16 rows whose bytes are a multiple of 16. */
+    HEADLOSS_KERNEL_STREAM = 2
+};
+
+/* A launch plan.  In headloss_force_plan a zero field leaves that choice to
+ * the planner. */
+typedef struct {
+    int kernel;      /* enum headloss_kernel */
+    int cluster;     /* resident: CTAs per row, 1..8 (streaming: 1) */
+    int stages;      /* resident: row stages per CTA, 1..4; streaming: chunk slots, 2..8 */
+    int threads;     /* threads per CTA: 256 or 512 */
+    int chunk_words; /* streaming: 16-byte words per thread per chunk: 1, 2 or 4 */
+} headloss_plan_desc;
 
 /*
- * headloss_force_plan -- pin the cluster size (1..8), the row stages per CTA
- * (1..4) and the threads per CTA (256 or 512) for later calls on this
- * handle; 0 leaves that choice to the planner.  For tests and tuning.  A
- * later call whose rows do not fit the pinned plan returns ERR_SIZE.
+ * headloss_plan -- the plan a call with (V, dtype) would use, the CTAs it
+ * launches and its dynamic shared memory per CTA.  Any output may be NULL.
+ * Errors: ERR_ARG, ERR_DTYPE, ERR_SIZE, ERR_CUDA.
  */
-int headloss_force_plan(headloss_t h, int cluster, int stages, int threads);
+int headloss_plan(headloss_t h, int64_t V, int dtype, headloss_plan_desc* plan, int* ctas,
+                  int* smem_bytes);
+
+/*
+ * headloss_force_plan -- pin some or all plan choices for later calls on this
+ * handle (NULL: back to the automatic plan).  For tests and tuning.  A call
+ * whose rows cannot use the pinned choices returns ERR_SIZE.  Errors: ERR_ARG.
+ */
+int headloss_force_plan(headloss_t h, const headloss_plan_desc* plan);
 
 /* Kernel launches one headloss_forward_backward call enqueues (constant). */
 int headloss_launches_per_call(void);

@@ -62,10 +62,11 @@ def host_i64(t):
 
 
 def run_gpu(wl, inp, grad=True, inplace=False, plan=None, handle=None):
-    """One library call; returns (scalars f64 numpy[16], grad tensor or None, handle)."""
+    """One library call; returns (scalars f64 numpy[16], grad tensor or None, handle).
+    plan: keyword arguments of HeadLoss.force_plan, or None for the automatic plan."""
     h = handle or headloss_for(wl)
     if plan is not None:
-        h.force_plan(*plan)
+        h.force_plan(**plan)
     x = inp["logits"]
     g = None
     if grad:

@@ -42,7 +42,7 @@ def test_host_only_calls(lib):
     assert hlb.headloss_launches_per_call() == 3
     assert hlb.headloss_strerror(0) == "ok"
     assert "aligned" in hlb.headloss_strerror(hlb.HEADLOSS_ERR_ALIGN)
-    assert lib.headloss_force_plan(None, 0, 0, 0) == hlb.HEADLOSS_ERR_ARG
+    assert lib.headloss_force_plan(None, None) == hlb.HEADLOSS_ERR_ARG
     assert lib.headloss_forward_backward(None, None, 1, 1, 1, None, None, None, None, None,
                                          None, None) == hlb.HEADLOSS_ERR_ARG
     e = ctypes.c_int()

@@ -73,14 +73,37 @@ def test_ragged_and_tiny_vocab(V, dtype):
     full_check(small(ALL_LOSSES, N=19, V=V, dtype=dtype))
 
 
+RESIDENT, STREAM = hlb.HEADLOSS_KERNEL_RESIDENT, hlb.HEADLOSS_KERNEL_STREAM
+
+
 @pytest.mark.parametrize("cluster,stages,threads", [
     (1, 2, 512), (2, 2, 512), (2, 3, 256), (3, 1, 256), (4, 2, 512), (5, 1, 256), (6, 1, 512),
     (7, 1, 256), (8, 2, 256), (8, 4, 512)])
-def test_forced_cluster_plans(cluster, stages, threads):
+def test_forced_resident_plans(cluster, stages, threads):
+    plan = dict(kernel=RESIDENT, cluster=cluster, stages=stages, threads=threads)
     wl = small(ALL_LOSSES, N=40, V=20011, softcap=30.0, logits_scale=0.5)
-    full_check(wl, plan=(cluster, stages, threads))
-    full_check(small(("ce", "z", "entropy"), N=40, V=8000, dtype=torch.float32),
-               plan=(cluster, stages, threads))
+    full_check(wl, plan=plan)
+    full_check(small(("ce", "z", "entropy"), N=40, V=8000, dtype=torch.float32), plan=plan)
+
+
+# the streaming kernel: aligned rows only (V a multiple of 8), several chunks
+# per row plus a partial last chunk, every feature set, both tanh paths
+@pytest.mark.parametrize("stages,threads,words", [(2, 256, 1), (3, 512, 1), (4, 256, 2),
+                                                   (6, 256, 4), (6, 512, 2), (8, 256, 1)])
+@pytest.mark.parametrize("V", [8, 1000, 20008])
+def test_forced_stream_plans(stages, threads, words, V):
+    plan = dict(kernel=STREAM, stages=stages, threads=threads, chunk_words=words)
+    full_check(small(ALL_LOSSES, N=23, V=V, softcap=30.0, logits_scale=0.5), plan=plan)
+    full_check(small(ALL_LOSSES, N=23, V=V, softcap=2.0, seed=5), plan=plan)
+    full_check(small(("ce", "z", "grpo", "grpo_stats"), N=23, V=V, dtype=torch.float16),
+               plan=plan)
+    full_check(small(("dist_ce", "fkl", "rkl", "entropy"), N=23, V=V, sigma=6.0), plan=plan)
+
+
+def test_stream_every_loss_subset():
+    plan = dict(kernel=STREAM, stages=4, threads=256, chunk_words=1)
+    for losses in SUBSETS:
+        full_check(small(losses, N=17, V=4104, seed=len(losses)), plan=plan)
 
 
 def test_large_logits_fp32():
