@@ -620,3 +620,113 @@ int headloss_get_device_error(headloss_t h, headloss_stream_t stream, int* err) 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// headloss_forward_backward_noalloc: the same call for callers that must not
+// allocate device memory.
+//
+// Some callers cannot call cudaMalloc at the point where they compute the
+// loss: code running while a CUDA graph is being captured on its stream
+// (allocation is not allowed there), code behind a framework memory pool that
+// forbids raw device allocations, or a real-time loop that must not touch the
+// allocator.  The handle-based entry point needs a workspace allocated by
+// headloss_create; this one keeps that workspace in a fixed file-scope device
+// array instead, so it allocates nothing, ever.
+//
+// The array holds NOALLOC_MAX_SLOTS partial-sum slots (one per launched
+// cluster or CTA, 16 doubles each) plus the valid-row count and the error
+// word: 1024 * 128 + 256 bytes = 131,328 bytes, present on every device that
+// loads this library, for the life of the process.  A launch never uses more
+// slots than that (the planner caps its grid there); a launch that would
+// still need more is rejected with HEADLOSS_ERR_SIZE.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int NOALLOC_MAX_SLOTS = 1024;
+constexpr size_t NOALLOC_PARTIAL_BYTES = size_t(NOALLOC_MAX_SLOTS) * NACC * sizeof(double);
+constexpr size_t NOALLOC_BYTES = NOALLOC_PARTIAL_BYTES + 256;
+constexpr int NOALLOC_MAX_DEVICES = 64;
+
+// Host code must not use this name as an address: it only identifies the
+// symbol; the device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
+
+// Device address of the scratch array on device `dev` (the current device),
+// resolved once per device.
+int noalloc_scratch(int dev, void** out) {
+    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return HEADLOSS_ERR_ARG;
+    std::lock_guard<std::mutex> g(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
+            return HEADLOSS_ERR_CUDA;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return HEADLOSS_OK;
+}
+
+}  // namespace
+
+extern "C" int headloss_forward_backward_noalloc(
+    uint32_t flags, const headloss_weights* w, float temperature, float clip_eps, float softcap,
+    float logits_scale, const void* logits, int64_t N, int64_t V, int dtype,
+    const int64_t* labels, const void* teacher_logits, const float* old_logprobs,
+    const float* advantages, void* grad_out, float* scalars_out, headloss_stream_t stream) {
+    // the same configuration checks as headloss_create
+    if (flags == 0 || (flags & ~kAllFlags)) return HEADLOSS_ERR_ARG;
+    if (!(temperature > 0.f) || !isfinite(temperature)) return HEADLOSS_ERR_ARG;
+    if (!(clip_eps >= 0.f) || !isfinite(clip_eps)) return HEADLOSS_ERR_ARG;
+    if (!(softcap >= 0.f) || !isfinite(softcap)) return HEADLOSS_ERR_ARG;
+    if (!(logits_scale > 0.f) || !isfinite(logits_scale)) return HEADLOSS_ERR_ARG;
+    headloss_weights ww = {1.f, 0.f, 0.f, 0.f, 0.f, 1.f, 0.f, 1.f};
+    if (w) ww = *w;
+    const float wl[8] = {ww.ce, ww.z, ww.dist_ce, ww.fkl, ww.rkl, ww.grpo, ww.entropy, ww.grad_scale};
+    for (float v : wl)
+        if (!isfinite(v)) return HEADLOSS_ERR_ARG;
+    int dev = 0, sms = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return HEADLOSS_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+        return HEADLOSS_ERR_CUDA;
+    void* scratch = nullptr;
+    const int rc = noalloc_scratch(dev, &scratch);
+    if (rc) return rc;
+
+    // a handle on the host stack whose workspace is the scratch array
+    headloss h;
+    h.flags = flags;
+    h.w = ww;
+    h.T = temperature;
+    h.eps = clip_eps;
+    h.softcap = softcap;
+    h.s = logits_scale;
+    h.device = dev;
+    h.num_sms = sms;
+    h.smem_optin = optin;
+    h.ws = scratch;
+    h.partials = static_cast<double*>(scratch);
+    h.partials_cap = NOALLOC_MAX_SLOTS < 4 * sms ? NOALLOC_MAX_SLOTS : 4 * sms;
+    h.n_valid = reinterpret_cast<long long*>(static_cast<char*>(scratch) + NOALLOC_PARTIAL_BYTES);
+    h.err = reinterpret_cast<int*>(static_cast<char*>(scratch) + NOALLOC_PARTIAL_BYTES + 64);
+    h.forced = headloss_plan_desc{0, 0, 0, 0, 0};
+    if (N > 0) {
+        Plan pl;
+        {
+            std::lock_guard<std::mutex> g(h.mu);
+            const int prc = make_plan(&h, V >= 1 && V < (int64_t(1) << 31) ? V : 1,
+                                      dtype >= 0 && dtype <= 2 ? dtype : 1, &pl);
+            if (prc == HEADLOSS_OK && pl.ncl > NOALLOC_MAX_SLOTS) return HEADLOSS_ERR_SIZE;
+        }
+    }
+    // the previous call's error bits must not leak into this one
+    if (cudaMemsetAsync(h.err, 0, sizeof(int), reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return HEADLOSS_ERR_CUDA;
+    return headloss_forward_backward(&h, logits, N, V, dtype, labels, teacher_logits,
+                                     old_logprobs, advantages, grad_out, scalars_out, stream);
+}

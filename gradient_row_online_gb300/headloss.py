@@ -48,7 +48,8 @@ SLOTS = ("total", "ce", "z", "dist_ce", "fkl", "rkl", "grpo_loss", "new_logprob_
 # Every function declared in include/headloss.h.
 EXPORTS = ("headloss_create", "headloss_forward_backward", "headloss_get_device_error",
            "headloss_plan", "headloss_force_plan", "headloss_launches_per_call",
-           "headloss_destroy", "headloss_strerror", "headloss_version")
+           "headloss_destroy", "headloss_strerror", "headloss_version",
+           "headloss_forward_backward_noalloc")
 
 
 # enum headloss_kernel
@@ -106,6 +107,10 @@ def load_library(path: str = LIB_PATH):
     lib.headloss_strerror.restype = ctypes.c_char_p
     lib.headloss_version.argtypes = []
     lib.headloss_version.restype = i32
+    lib.headloss_forward_backward_noalloc.argtypes = [
+        ctypes.c_uint32, ctypes.POINTER(headloss_weights), ctypes.c_float, ctypes.c_float,
+        ctypes.c_float, ctypes.c_float, vp, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp]
+    lib.headloss_forward_backward_noalloc.restype = i32
     _lib = lib
     return lib
 
@@ -173,6 +178,22 @@ def headloss_forward_backward(h, logits, N, V, dtype, labels, teacher_logits, ol
                                          _ptr(labels), _ptr(teacher_logits), _ptr(old_logprobs),
                                          _ptr(advantages), _ptr(grad_out), _ptr(scalars_out),
                                          _stream(stream)), "headloss_forward_backward")
+
+
+def headloss_forward_backward_noalloc(flags, weights, temperature, clip_eps, softcap,
+                                      logits_scale, logits, N, V, dtype, labels, teacher_logits,
+                                      old_logprobs, advantages, grad_out, scalars_out,
+                                      stream=None) -> None:
+    """The allocation-free call (no handle): for callers that must not allocate
+    device memory while computing the loss, e.g. inside a CUDA-graph capture."""
+    lib = load_library()
+    if isinstance(weights, dict):
+        weights = make_weights(**weights)
+    w = ctypes.byref(weights) if weights is not None else None
+    _check(lib.headloss_forward_backward_noalloc(
+        flags, w, temperature, clip_eps, softcap, logits_scale, _ptr(logits), int(N), int(V),
+        int(dtype), _ptr(labels), _ptr(teacher_logits), _ptr(old_logprobs), _ptr(advantages),
+        _ptr(grad_out), _ptr(scalars_out), _stream(stream)), "headloss_forward_backward_noalloc")
 
 
 def headloss_get_device_error(h, stream=None) -> int:

@@ -202,6 +202,40 @@ int headloss_plan(headloss_t h, int64_t V, int dtype, headloss_plan_desc* plan, 
  */
 int headloss_force_plan(headloss_t h, const headloss_plan_desc* plan);
 
+/*
+ * headloss_forward_backward_noalloc -- headloss_forward_backward without a
+ * handle and without any device allocation, for callers that cannot allocate
+ * when they compute the loss: inside a CUDA-graph capture (allocation is not
+ * allowed there), under a memory pool that forbids raw cudaMalloc, or in a
+ * loop that must never touch the allocator.  (The pages describe no such
+ * entry point; it is an addition of this library.)
+ *
+ * Arguments: the configuration of headloss_create followed by the arguments
+ * of headloss_forward_backward, with the same meanings, layouts and checks.
+ *
+ * Scratch: instead of a handle's workspace it uses one fixed device array in
+ * the library (1024 partial-sum slots + a count and an error word, 131,328
+ * bytes), present on every device that loads the library until the process
+ * exits.  Launches are planned to use at most those 1024 slots; a launch that
+ * would need more returns HEADLOSS_ERR_SIZE.
+ *
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address once; make that first call before any stream
+ * capture.  Every call shares the array and overwrites what it uses (the
+ * count and partial sums are rewritten by each call, the error word is
+ * cleared on `stream` first), so calls on different streams that overlap on
+ * the GPU race with one another: order them on one stream.  Device-side
+ * conditions (a label >= V, a copy timeout) are not reported to the caller by
+ * this entry point; such rows are treated as masked.  Never calls cudaMalloc,
+ * cudaFree or any allocating routine.
+ */
+int headloss_forward_backward_noalloc(uint32_t flags, const headloss_weights* w, float temperature,
+                                      float clip_eps, float softcap, float logits_scale,
+                                      const void* logits, int64_t N, int64_t V, int dtype,
+                                      const int64_t* labels, const void* teacher_logits,
+                                      const float* old_logprobs, const float* advantages,
+                                      void* grad_out, float* scalars_out, headloss_stream_t stream);
+
 /* Kernel launches one headloss_forward_backward call enqueues (constant). */
 int headloss_launches_per_call(void);
 
