@@ -353,7 +353,7 @@ def e2e(wl, h, inp, args, dev, world):
             "ms_per_step": total / len(ms)}
 
 
-def cpu_rows_per_s(wl, x, lab, t, old, adv, n_valid, threads):
+def cpu_seconds(wl, x, lab, t, old, adv, n_valid, threads):
     import oracle as orc
     from tests import _harness as H
     cfg = H.oracle_cfg(wl)
@@ -378,12 +378,12 @@ def cpu_baseline(wl, inp, seconds, reps=1):
         return (H.host64(pick("logits")), H.host_i64(pick("labels")), H.host64(pick("teacher")),
                 H.host64(pick("old_logprobs")), H.host64(pick("advantages")))
 
-    probe = min(wl.N, max(cores, 16))
+    probe = min(wl.N, max(8 * cores, 64))
     s = sample(probe)
-    dt = cpu_rows_per_s(wl, *s, n_valid, cores)
+    dt = cpu_seconds(wl, *s, n_valid, cores)
     rows = int(min(wl.N, max(probe, probe * seconds / max(dt, 1e-6))))
     s = sample(rows)
-    dt = cpu_rows_per_s(wl, *s, n_valid, cores)
+    dt = cpu_seconds(wl, *s, n_valid, cores)
     return {"value": rows / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"first {rows} of {wl.N} rows of {wl.name} (gradient + all scalars, fp64, "
                       f"{cores} OpenMP threads), {dt:.1f} s"}

@@ -328,30 +328,34 @@ bool pick_resident(const headloss* h, const Plan* cand, int ncand, Plan* best) {
 
 // Streaming rule (measured on GB300): the per-chunk bookkeeping (slot wait,
 // running-shift update, release) is amortised over the chunk, so the largest
-// chunk per thread wins; then two or more CTAs per SM; then fewer slots (two
-// or three already hide the copy latency).
+// chunk per thread wins; then 512 threads; then fewer slots (two already hide
+// the copy latency).
 bool pick_stream(const headloss* h, const Plan* cand, int ncand, Plan* best) {
     Plan b;
     double bscore = -1.0;
     for (int i = 0; i < ncand; ++i) {
         const Plan& c = cand[i];
         if (c.kind != HEADLOSS_KERNEL_STREAM) continue;
-        const double per_sm = double(c.ncl) / h->num_sms;
-        const double score = c.chunk_words * 1e6 + (per_sm >= 2.0 ? 1e3 : 0.0) - c.nbuf;
+        const double score = c.chunk_words * 1e6 + c.threads * 1e2 - c.nbuf;
         if (score > bscore) {
             b = c;
             bscore = score;
         }
     }
     if (bscore < 0) return false;
+    (void)h;
     *best = b;
     return true;
 }
 
 // Chooses the kernel and its launch plan for rows of V elements of `dtype`.
-// The streaming kernel takes 16-bit rows whose resident plan would need a
-// cluster of three or more CTAs (a row too large for one or two SMs); the
-// resident kernel takes everything else.
+// Measured on GB300 over the five loss sets: the streaming kernel wins when a
+// row carries a teacher (twice the bytes and twice the exponentials per
+// column, so a resident row needs a cluster of three or more CTAs and its
+// per-row cluster barriers cost the most), and loses when the row is
+// student-only (its second read, partly from DRAM, costs more than the
+// resident kernel's barriers).  So: streaming for 16-bit rows with a teacher
+// whose resident plan needs three or more CTAs per row; resident otherwise.
 int make_plan(headloss* h, int64_t V, int dtype, Plan* out) {
     const int feat = feature_set(h);
     if (h->plan.V == V && h->plan.dtype == dtype && h->plan.feat == feat) {
@@ -376,7 +380,7 @@ int make_plan(headloss* h, int64_t V, int dtype, Plan* out) {
     } else if (fk == HEADLOSS_KERNEL_RESIDENT) {
         if (!have_res) return HEADLOSS_ERR_SIZE;
         best = res;
-    } else if (have_str && (!have_res || res.C >= 3)) {
+    } else if (have_str && (!have_res || (res.C >= 3 && (feat & F_TEACH)))) {
         best = str;
     } else if (have_res) {
         best = res;
