@@ -1,7 +1,7 @@
 """Shared helpers of the parity tests: run the library and the oracle on the
 same seeded inputs and compare them under the stated tolerances.
 
-Tolerances (fused head-loss north star; readings in the design notes):
+Tolerances (scalars and gradient as stated below; readings in the design notes):
   scalars   rel. error <= 1e-5 (fp32 logits) / 1e-3 (bf16, fp16), where the
             error is divided by max(|ref|, mean_i |row value_i|) so that means
             close to 0 (GRPO) stay well defined; counts exact (n_clipped up to
