@@ -168,7 +168,7 @@ __device__ RowCoef row_epilogue16(const Params& p, const float* recs, int C, boo
             ts = rc * LN2;
         }
     }
-    if (!CAP) {  // dz/dx = s: fold the chain rule into the coefficients
+    {  // the scale of dz/dx = s (softcap: s (1 - tanh^2)) folds into the coefficients
         pc *= p.s;
         ps *= p.s;
         tc *= p.s;
@@ -580,18 +580,37 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                                     g = fma2(pT, tco, g);
                                     g = fma2(q, qc2, g);
                                 }
-                                if (w == wy && (iy >> 1) == kk) {  // the label column
-                                    float gl, gh;
-                                    upk(g, gl, gh);
-                                    if (iy & 1) gh -= k.bc;
-                                    else gl -= k.bc;
-                                    g = pk(gl, gh);
-                                }
-                                if (CAP) g = mul2(g, mul2(omt, s2));  // dz/dx = s (1 - tanh^2)
-                                out[kk] = P16::pack(g);
+                                // dz/dx = s (1 - tanh^2); s is already in the coefficients
+                                out[kk] = P16::pack(CAP ? mul2(g, omt) : g);
                             }
                             *reinterpret_cast<uint4*>(gg + eb) =
                                 make_uint4(out[0], out[1], out[2], out[3]);
+                            if (w == wy) {
+                                // the label column: this thread recomputes that one element
+                                // with the label term and overwrites it
+                                const float xv1 = P16::to_f(xs[w * EPW + iy]);
+                                float zs, om1 = 1.f;
+                                if (CAP) zs = __fmul_rn(tanh_a2x_1(__fmul_rn(xv1, A2), &om1), Kc);
+                                else zs = __fmul_rn(xv1, K);
+                                const float arg = zs - k.lse2;
+                                float g1 = ex2f(arg) * (ENT ? fmaf(k.ps, arg, k.pc) : k.pc);
+                                if (TEACH) {
+                                    const float tv1 = P16::to_f(ts[w * EPW + iy]);
+                                    const float pT = ex2f(fmaf(zs, invT, -k.lseT2));
+                                    const float q = ex2f(fmaf(tv1, KT, -k.lsq2));
+                                    float tco = k.tc;
+                                    if (RKL) {
+                                        const float dxu = CAP ? fmaf(tv1, -LOG2E, zs) * invT
+                                                              : fmaf(xv1, s, -tv1) * KT;
+                                        tco = fmaf(k.ts, dxu - dlse, k.tc);
+                                    }
+                                    g1 = fmaf(pT, tco, g1);
+                                    g1 = fmaf(q, k.qc, g1);
+                                }
+                                g1 -= k.bc;
+                                if (CAP) g1 *= om1;
+                                reinterpret_cast<uint16_t*>(gg)[eb + iy] = P16::from_f(g1);
+                            }
                         } else {
                             for (int i = 0; i < EPW; ++i) {
                                 if (eb + i < e0 || eb + i >= e1) continue;
@@ -601,7 +620,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                                     float omt;
                                     const float th = tanh_a2x_1(__fmul_rn(xv, A2), &omt);
                                     zs = __fmul_rn(th, Kc);
-                                    dz = s * omt;
+                                    dz = omt;  // s is in the coefficients
                                 } else {
                                     zs = __fmul_rn(xv, K);
                                 }
@@ -627,8 +646,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                         }
                     }
                 };
-                if (CAP && poly) passC(BoolC<true>{});
-                else passC(BoolC<false>{});
+                passC(BoolC<false>{});  // exp / reciprocal tanh: pass B keeps the FMA pipe busy
             }
         } else if (gg != nullptr) {
             // a masked row: its gradient row is exact +0

@@ -11,7 +11,10 @@
 //           coefficients (the same epilogue as the resident kernel);
 //   pass 2  chunks K-1 .. 0 (reverse order, so the chunks read most recently
 //           -- the ones most likely still in L2 -- come back first): the
-//           combined gradient, written once from registers.
+//           combined gradient, written once from registers.  Under softcap,
+//           pass 1 takes tanh from the FMA-pipe polynomial (when in range)
+//           and pass 2 from ex2 + rcp, which splits the work between the FMA
+//           pipe and the MUFU.
 //
 // The chunk stream (row, pass, chunk) is one sequence per CTA; a thread of
 // the last warp to finish a chunk issues the bulk copy of the entry that
@@ -234,7 +237,6 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         float amax = 0.f;  // softcap: running max |x|
         f2 S2 = z2, E2 = z2, ST2 = z2, Sq2 = z2, Eq2 = z2, Xp2 = z2, Y2 = z2;
         float zy = 0.f, hasy = 0.f;
-        int needexp = 0;  // softcap: some chunk of this thread's fell outside the polynomial range
         for (int c = 0; c < K; ++c, ++J) {
             const unsigned char* sb = acquire(J);
             const int64_t c0 = int64_t(c) * CH;
@@ -311,7 +313,6 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             // the polynomial tanh covers these words when max |x| / c is in range
             const bool poly_ok = !CAP || __fmul_rn(cx, invc) <= HL_TANH_POLY_Y0;
             const bool use_poly = CAP && __all_sync(0xffffffffu, poly_ok);
-            if (CAP && !use_poly) needexp = 1;
             const f2 zm2 = pk1(zm), um2 = pk1(um), nzm2 = pk1(-zm);
             auto sums = [&](auto polyc) {
 #pragma unroll
@@ -383,8 +384,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             rec[R_ZY] = tr.zy;
             rec[R_HASY] = tr.hasy;
         }
-        // the barrier also ORs "some chunk needed the exp tanh" over the CTA
-        const bool row_exp = __syncthreads_or(CAP && needexp) != 0;
+        __syncthreads();
         if (warp == 0) {
             const RowCoef kw =
                 row_epilogue16<TEACH, RKL, ENT, CAP>(p, xch, nwarps, true, old_lp, adv, acc, lane);
@@ -448,22 +448,44 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                                 g = fma2(pT, tco, g);
                                 g = fma2(q, qc2, g);
                             }
-                            if (w == wy && (iy >> 1) == kk) {
-                                float gl, gh;
-                                upk(g, gl, gh);
-                                if (iy & 1) gh -= k.bc;
-                                else gl -= k.bc;
-                                g = pk(gl, gh);
-                            }
-                            if (CAP) g = mul2(g, mul2(omt, s2));  // dz/dx = s (1 - tanh^2)
-                            out[kk] = P16::pack(g);
+                            // dz/dx = s (1 - tanh^2); s is already in the coefficients
+                            out[kk] = P16::pack(CAP ? mul2(g, omt) : g);
                         }
                         *reinterpret_cast<uint4*>(gg + r * V + c0 + int64_t(w) * EPW) =
                             make_uint4(out[0], out[1], out[2], out[3]);
+                        if (w == wy) {
+                            // the label column: this thread recomputes that one element
+                            // with the label term and overwrites it (program order keeps
+                            // the later store)
+                            const uint16_t* xs16 = reinterpret_cast<const uint16_t*>(sb);
+                            const float xv1 = P16::to_f(xs16[w * EPW + iy]);
+                            float zs, om1 = 1.f;
+                            if (CAP) zs = __fmul_rn(tanh_a2x_1(__fmul_rn(xv1, A2), &om1), Kc);
+                            else zs = __fmul_rn(xv1, K1);
+                            const float arg = zs - k.lse2;
+                            float g1 = ex2f(arg) * (ENT ? fmaf(k.ps, arg, k.pc) : k.pc);
+                            if (TEACH) {
+                                const float tv1 = P16::to_f(
+                                    reinterpret_cast<const uint16_t*>(sb + opbytes)[w * EPW + iy]);
+                                const float pT = ex2f(fmaf(zs, invT, -k.lseT2));
+                                const float q = ex2f(fmaf(tv1, KT, -k.lsq2));
+                                float tco = k.tc;
+                                if (RKL) {
+                                    const float dxu = CAP ? fmaf(tv1, -LOG2E, zs) * invT
+                                                          : fmaf(xv1, s, -tv1) * KT;
+                                    tco = fmaf(k.ts, dxu - dlse, k.tc);
+                                }
+                                g1 = fmaf(pT, tco, g1);
+                                g1 = fmaf(q, k.qc, g1);
+                            }
+                            g1 -= k.bc;
+                            if (CAP) g1 *= om1;
+                            reinterpret_cast<uint16_t*>(gg)[r * V + c0 + int64_t(w) * EPW + iy] =
+                                P16::from_f(g1);
+                        }
                     }
                 };
-                if (CAP && !row_exp) grad(BoolC<true>{});
-                else grad(BoolC<false>{});
+                grad(BoolC<false>{});  // exp / reciprocal tanh: pass 1 keeps the FMA pipe busy
             }
             release(J);
         }
