@@ -646,7 +646,8 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                         }
                     }
                 };
-                passC(BoolC<false>{});  // exp / reciprocal tanh: pass B keeps the FMA pipe busy
+                if (CAP && poly) passC(BoolC<true>{});
+                else passC(BoolC<false>{});
             }
         } else if (gg != nullptr) {
             // a masked row: its gradient row is exact +0

@@ -11,10 +11,9 @@
 //           coefficients (the same epilogue as the resident kernel);
 //   pass 2  chunks K-1 .. 0 (reverse order, so the chunks read most recently
 //           -- the ones most likely still in L2 -- come back first): the
-//           combined gradient, written once from registers.  Under softcap,
-//           pass 1 takes tanh from the FMA-pipe polynomial (when in range)
-//           and pass 2 from ex2 + rcp, which splits the work between the FMA
-//           pipe and the MUFU.
+//           combined gradient, written once from registers.  Under softcap
+//           both passes take tanh from the FMA-pipe polynomial when every
+//           chunk of the row is in its range, else from ex2 + rcp.
 //
 // The chunk stream (row, pass, chunk) is one sequence per CTA; a thread of
 // the last warp to finish a chunk issues the bulk copy of the entry that
@@ -237,6 +236,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         float amax = 0.f;  // softcap: running max |x|
         f2 S2 = z2, E2 = z2, ST2 = z2, Sq2 = z2, Eq2 = z2, Xp2 = z2, Y2 = z2;
         float zy = 0.f, hasy = 0.f;
+        int needexp = 0;  // softcap: a chunk of this thread's fell outside the polynomial range
         for (int c = 0; c < K; ++c, ++J) {
             const unsigned char* sb = acquire(J);
             const int64_t c0 = int64_t(c) * CH;
@@ -313,6 +313,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             // the polynomial tanh covers these words when max |x| / c is in range
             const bool poly_ok = !CAP || __fmul_rn(cx, invc) <= HL_TANH_POLY_Y0;
             const bool use_poly = CAP && __all_sync(0xffffffffu, poly_ok);
+            if (CAP && !use_poly) needexp = 1;
             const f2 zm2 = pk1(zm), um2 = pk1(um), nzm2 = pk1(-zm);
             auto sums = [&](auto polyc) {
 #pragma unroll
@@ -384,7 +385,8 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             rec[R_ZY] = tr.zy;
             rec[R_HASY] = tr.hasy;
         }
-        __syncthreads();
+        // the barrier also ORs "some chunk needed the exp tanh" over the CTA
+        const bool row_exp = __syncthreads_or(CAP && needexp) != 0;
         if (warp == 0) {
             const RowCoef kw =
                 row_epilogue16<TEACH, RKL, ENT, CAP>(p, xch, nwarps, true, old_lp, adv, acc, lane);
@@ -485,7 +487,8 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                         }
                     }
                 };
-                grad(BoolC<false>{});  // exp / reciprocal tanh: pass 1 keeps the FMA pipe busy
+                if (CAP && !row_exp) grad(BoolC<true>{});
+                else grad(BoolC<false>{});
             }
             release(J);
         }
