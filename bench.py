@@ -45,10 +45,12 @@ def parse():
     ap.add_argument("--plan", default="",
                     help="pin the launch plan, e.g. kernel=2,stages=2,threads=512,chunk_words=4 "
                          "(profiling; default: the library's planner)")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=4)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-loss-sets", action="store_true")
+    ap.add_argument("--no-per-loss", action="store_true",
+                    help="skip the per-loss-loop comparison")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall time the CPU-baseline sample is sized for")
     return ap.parse_args()
@@ -274,6 +276,8 @@ def run_ours(args, rank, world, local):
     }
     if not args.no_loss_sets and world == 1:
         line["loss_sets"] = loss_sets(args, dev, exclude=wl.name, peak=peak)
+    if not args.no_per_loss and world == 1:
+        line["per_loss_loop"] = per_loss_loop(wl, inp, grad, dev)
     if not args.no_e2e:
         del grad
         line["e2e"] = e2e(wl, h, inp, args, dev, world)
@@ -315,9 +319,67 @@ def loss_sets(args, dev, exclude, peak):
     return res
 
 
+def per_loss_loop(wl, inp, grad, dev, steps=5):
+    """The status quo the pages replace: one call per loss (each re-reads the
+    row and recomputes its softmax), gradients accumulated into one buffer,
+    against the one fused call.  Same kernels; only the flag sets differ."""
+    import gradient_row_online_gb300 as pkg
+    from gradient_row_online_gb300 import headloss as hlb
+
+    s = torch.cuda.current_stream(dev)
+    fused = pkg.headloss_for(wl)
+    out = torch.empty(16, dtype=torch.float32, device=dev)
+    args = (inp["logits"], inp["labels"], inp["teacher"], inp["old_logprobs"], inp["advantages"])
+    wkey = {"ce": "ce", "z": "z", "dist_ce": "dist_ce", "fkl": "fkl", "rkl": "rkl",
+            "grpo": "grpo", "entropy": "entropy"}
+    calls = []  # (handle, writes a gradient)
+    for name in wl.losses:
+        w = {k: 0.0 for k in ("ce", "z", "dist_ce", "fkl", "rkl", "grpo", "entropy")}
+        w["grad_scale"] = wl.weights["grad_scale"]
+        bearing = name in wkey and wl.weights.get(wkey[name], 0.0) != 0.0
+        if name in wkey:
+            w[wkey[name]] = wl.weights.get(wkey[name], 0.0)
+        hd = pkg.HeadLoss(pkg.flags_of((name,)), hlb.make_weights(**w), wl.temperature,
+                          wl.clip_eps, wl.softcap, wl.logits_scale)
+        calls.append((hd, bearing))
+    n_bearing = sum(1 for _, b in calls if b)
+    extra = [torch.empty_like(grad) for _ in range(max(0, n_bearing - 1))]
+
+    def loop():
+        first = True
+        k = 0
+        for hd, bearing in calls:
+            if not bearing:
+                hd(*args, None, out, s)
+            elif first:
+                hd(*args, grad, out, s)
+                first = False
+            else:
+                hd(*args, extra[k], out, s)
+                grad.add_(extra[k])
+                k += 1
+
+    f = lambda: fused(*args, grad, out, s)
+    for fn in (f, loop):
+        fn()
+    ms_fused = statistics.mean(time_calls(f, s, steps))
+    ms_loop = statistics.mean(time_calls(loop, s, steps))
+    for hd, _ in calls:
+        hd.close()
+    fused.close()
+    del extra
+    torch.cuda.empty_cache()
+    return {"workload": wl.name, "losses": list(wl.losses), "fused_ms": ms_fused,
+            "per_loss_ms": ms_loop, "speedup": ms_loop / ms_fused, "calls_in_loop": len(calls),
+            "gradient_writes_in_loop": n_bearing}
+
+
 def e2e(wl, h, inp, args, dev, world):
     """The same metric through the public call with pinned HOST buffers: every
-    step copies its inputs host->device and reads the gradient and scalars back."""
+    step copies its inputs host->device and reads its gradient and scalars
+    back.  Steps are pipelined over two device buffer sets on three streams
+    (copy in, compute, copy out), so one step's copies overlap another's
+    compute; the timed region spans the first copy in to the last copy out."""
     from gradient_row_online_gb300 import headloss as hlb
 
     names = ["logits", "labels", "teacher", "old_logprobs", "advantages"]
@@ -326,31 +388,62 @@ def e2e(wl, h, inp, args, dev, world):
     for k in names:
         if host[k] is not None:
             host[k].copy_(inp[k])
-    h_grad = torch.empty(inp["logits"].shape, dtype=inp["logits"].dtype, pin_memory=True)
-    h_out = torch.empty(16, dtype=torch.float32, pin_memory=True)
-    d_grad = torch.empty_like(inp["logits"])
-    d_out = torch.empty(16, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    # two device sets: the bench's own input tensors and one more
+    dsets = [inp, {k: (None if inp[k] is None else torch.empty_like(inp[k])) for k in names}]
+    d_grad = [torch.empty_like(inp["logits"]) for _ in range(2)]
+    d_out = [torch.empty(16, dtype=torch.float32, device=dev) for _ in range(2)]
+    h_grad = [torch.empty(inp["logits"].shape, dtype=inp["logits"].dtype, pin_memory=True)
+              for _ in range(2)]
+    h_out = [torch.empty(16, dtype=torch.float32, pin_memory=True) for _ in range(2)]
+    s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = lambda: torch.cuda.Event()
+    in_done, cmp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     h2d = sum(host[k].numel() * host[k].element_size() for k in names if host[k] is not None)
-    d2h = h_grad.numel() * h_grad.element_size() + 64
+    d2h = h_grad[0].numel() * h_grad[0].element_size() + 64
+    dcode = hlb.dtype_code(wl.dtype)
+    used = [False, False]
 
-    def step():
-        for k in names:
-            if host[k] is not None:
-                inp[k].copy_(host[k], non_blocking=True)
-        hlb.headloss_forward_backward(h.h, inp["logits"], wl.N, wl.V, hlb.dtype_code(wl.dtype),
-                                      inp["labels"], inp["teacher"], inp["old_logprobs"],
-                                      inp["advantages"], d_grad, d_out, stream)
-        h_grad.copy_(d_grad, non_blocking=True)
-        h_out.copy_(d_out, non_blocking=True)
+    def step(k):
+        b = k % 2
+        d = dsets[b]
+        with torch.cuda.stream(s_in):
+            if used[b]:
+                s_in.wait_event(cmp_done[b])  # the inputs of buffer set b are free
+            for name in names:
+                if host[name] is not None:
+                    d[name].copy_(host[name], non_blocking=True)
+            in_done[b].record(s_in)
+        s_cmp.wait_event(in_done[b])
+        if used[b]:
+            s_cmp.wait_event(out_done[b])  # the gradient of set b has been read back
+        hlb.headloss_forward_backward(h.h, d["logits"], wl.N, wl.V, dcode, d["labels"],
+                                      d["teacher"], d["old_logprobs"], d["advantages"],
+                                      d_grad[b], d_out[b], s_cmp)
+        cmp_done[b].record(s_cmp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(cmp_done[b])
+            h_grad[b].copy_(d_grad[b], non_blocking=True)
+            h_out[b].copy_(d_out[b], non_blocking=True)
+            out_done[b].record(s_out)
+        used[b] = True
 
-    step()
+    step(0)
+    step(1)
     torch.cuda.synchronize()
-    ms = time_calls(step, stream, args.e2e_steps)
-    total = sum(ms)
-    return {"value": wl.N * world * len(ms) / (total / 1e3), "unit": "tokens/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": len(ms),
-            "ms_per_step": total / len(ms)}
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    n = max(2, args.e2e_steps)
+    t0.record(s_in)
+    for k in range(n):
+        step(k)
+    s_in.wait_stream(s_out)
+    t1.record(s_in)
+    torch.cuda.synchronize()
+    total = t0.elapsed_time(t1)
+    del dsets[1], d_grad, h_grad
+    return {"value": wl.N * world * n / (total / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "ms_per_step": total / n, "pipelined": "2 buffer sets, copy-in / compute / copy-out streams"}
 
 
 def cpu_seconds(wl, x, lab, t, old, adv, n_valid, threads):

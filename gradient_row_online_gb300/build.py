@@ -45,17 +45,27 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every .cu under csrc/ and link libheadloss.so; returns its path."""
-    if not force and up_to_date():
-        return LIB
+FAULT_LIB = os.path.join(BUILD, "libheadloss_faultinject.so")
+
+
+def build(force: bool = False, verbose: bool = False, fault_inject: bool = False) -> str:
+    """Compile every .cu under csrc/ and link libheadloss.so; returns its path.
+
+    fault_inject=True builds the test-only variant (-DHL_FAULT_INJECT, which
+    adds headloss_test_inject) into _build/libheadloss_faultinject.so instead."""
+    lib = FAULT_LIB if fault_inject else LIB
+    if not force and os.path.exists(lib) and all(
+            os.path.getmtime(d) <= os.path.getmtime(lib) for d in _deps()):
+        return lib
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
     srcs = _sources()
+    tag = "_fi" if fault_inject else ""
+    extra = ["-DHL_FAULT_INJECT"] if fault_inject else []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + tag + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr}")
@@ -65,13 +75,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -134,6 +134,8 @@ struct headloss {
     headloss_plan_desc forced;  // zero fields: the planner decides
     Plan plan;                  // cache of the last plan
     std::mutex mu;
+    unsigned long long wait_ns = 2000000000ull;  // limit of every in-kernel wait
+    int64_t drop_row = -1;                       // fault-injection builds only
 };
 
 namespace {
@@ -580,6 +582,8 @@ int headloss_forward_backward(headloss_t h, const void* logits, int64_t N, int64
         p.partials = h->partials;
         p.n_valid = h->n_valid;
         p.err = h->err;
+        p.wait_ns = h->wait_ns;
+        p.drop_row = h->drop_row;
 
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
@@ -609,6 +613,18 @@ int headloss_forward_backward(headloss_t h, const void* logits, int64_t N, int64
     if (cudaGetLastError() != cudaSuccess) return HEADLOSS_ERR_CUDA;
     return HEADLOSS_OK;
 }
+
+#ifdef HL_FAULT_INJECT
+// Test builds only (never in libheadloss.so): skip the bulk copies of one
+// row and shorten every in-kernel wait, so a test can watch a bounded wait
+// give up and report HEADLOSS_ERR_TIMEOUT without hanging anything.
+int headloss_test_inject(headloss_t h, int64_t drop_row, unsigned long long wait_ns) {
+    if (!h) return HEADLOSS_ERR_ARG;
+    h->drop_row = drop_row;
+    h->wait_ns = wait_ns ? wait_ns : 2000000000ull;
+    return HEADLOSS_OK;
+}
+#endif
 
 int headloss_get_device_error(headloss_t h, headloss_stream_t stream, int* err) {
     if (!h || !err) return HEADLOSS_ERR_ARG;

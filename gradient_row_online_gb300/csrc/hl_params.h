@@ -56,6 +56,8 @@ struct Params {
     double* partials;              // [clusters][NACC]
     const long long* n_valid;      // valid-row count of this call
     int* err;                      // device error word
+    unsigned long long wait_ns;    // limit of every mbarrier wait (~2 s)
+    int64_t drop_row;              // fault-injection builds only: row whose copy is skipped (-1: none)
 };
 
 }  // namespace hl

@@ -112,13 +112,14 @@ __device__ __forceinline__ void st_peer(uint32_t addr, double v) {
     asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(addr), "d"(v) : "memory");
 }
 
-// Bounded wait on an mbarrier phase: gives up after ~2 s of wall time and
-// reports it, so a lost copy can never hang the GPU.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Bounded wait on an mbarrier phase: gives up after `limit_ns` of wall time
+// (~2 s in normal builds) and reports it, so a lost copy can never hang the GPU.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > 2000000000ull) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
     return true;
 }

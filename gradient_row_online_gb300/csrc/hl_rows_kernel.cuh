@@ -76,6 +76,9 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
         const uint32_t bytes = (e1 > e0 && f1 > f0) ? uint32_t((f1 - f0) * ES) : 0u;
         fence_proxy_async();  // order earlier generic stores to this stage before the copy
         mbar_arrive_expect_tx(bar, bytes * OPS);
+#ifdef HL_FAULT_INJECT
+        if (r == p.drop_row) return;  // the copy never comes: the wait must give up
+#endif
         if (bytes) {
             const uint32_t dst = smem_addr(smem + size_t(st) * stage_bytes) +
                                  uint32_t((f0 / EPW - e0 / EPW) * 16);
@@ -122,7 +125,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
 
         const int st = it % p.nbuf;
         const uint32_t par = uint32_t(it / p.nbuf) & 1u;
-        if (!mbar_wait_bounded(smem_addr(&bars[st]), par)) {
+        if (!mbar_wait_bounded(smem_addr(&bars[st]), par, p.wait_ns)) {
             lost |= 1u << st;
             lost_par = (lost_par & ~(1u << st)) | (par << st);
             if (tid == 0) atomicOr(p.err, E_TIMEOUT);
@@ -329,7 +332,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
     // more (bounded) before the CTA's shared memory goes away.
     if (lost && tid == 0) {
         for (int b = 0; b < p.nbuf; ++b)
-            if (lost & (1u << b)) (void)mbar_wait_bounded(smem_addr(&bars[b]), (lost_par >> b) & 1u);
+            if (lost & (1u << b)) (void)mbar_wait_bounded(smem_addr(&bars[b]), (lost_par >> b) & 1u, p.wait_ns);
     }
     if (rank == 0 && tid == 0) {
         double* out = p.partials + size_t(cid) * NACC;

@@ -159,6 +159,9 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         const uint32_t bytes = uint32_t(len * ES);
         fence_proxy_async();
         mbar_arrive_expect_tx(bar, bytes * OPS);
+#ifdef HL_FAULT_INJECT
+        if (r == p.drop_row && J % per_row == 0) return;  // pass-1 chunk 0 never comes
+#endif
         const uint32_t dst = smem_addr(smem + size_t(sl) * slot_bytes);
         bulk_g2s(dst, xg + r * V + c0, bytes, bar);
         if (TEACH) bulk_g2s(dst + opbytes, tg + r * V + c0, bytes, bar);
@@ -182,7 +185,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
     auto acquire = [&](int64_t jj) -> const unsigned char* {
         const int sl = int(jj % S);
         const uint32_t par = uint32_t((jj / S) & 1);
-        if (!mbar_wait_bounded(smem_addr(&bars[sl]), par)) {
+        if (!mbar_wait_bounded(smem_addr(&bars[sl]), par, p.wait_ns)) {
             lost |= 1u << sl;
             lost_par = (lost_par & ~(1u << sl)) | (par << sl);
             if (lane == 0) atomicOr(p.err, E_TIMEOUT);
@@ -498,7 +501,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
     // (bounded) before the CTA's shared memory goes away
     if (lost && tid == 0) {
         for (int b = 0; b < S; ++b)
-            if (lost & (1u << b)) (void)mbar_wait_bounded(smem_addr(&bars[b]), (lost_par >> b) & 1u);
+            if (lost & (1u << b)) (void)mbar_wait_bounded(smem_addr(&bars[b]), (lost_par >> b) & 1u, p.wait_ns);
     }
     if (tid == 0) {
         double* out = p.partials + size_t(blockIdx.x) * NACC;
