@@ -148,6 +148,8 @@ int feature_set(const headloss* h) {
     if (h->flags & L_RKL) f |= F_RKL;
     if (h->flags & L_ENTROPY) f |= F_ENT;
     if (h->softcap > 0.f) f |= F_SOFTCAP;
+    if (h->flags & L_DIST_CE) f |= F_DCE;
+    if ((h->flags & L_ENTROPY) && h->w.entropy != 0.f) f |= F_ENTG;
     return f;
 }
 
@@ -160,9 +162,9 @@ const void* kernel_for(int kind, int dtype, int feat) {
         }
     }
     switch (dtype) {
-        case HEADLOSS_BF16: return rows_kernel_bf16(feat);
-        case HEADLOSS_FP16: return rows_kernel_fp16(feat);
-        case HEADLOSS_FP32: return rows_kernel_fp32(feat);
+        case HEADLOSS_BF16: return rows_kernel_bf16(feat & F_BASE);
+        case HEADLOSS_FP16: return rows_kernel_fp16(feat & F_BASE);
+        case HEADLOSS_FP32: return rows_kernel_fp32(feat & F_BASE);
         default: return nullptr;
     }
 }

@@ -75,12 +75,12 @@ __device__ __forceinline__ float hsum(f2 v) {
     return a + b;
 }
 
-// tanh(y) and 1 - tanh(y)^2 from w = exp(2y), r = 1 / (1 + w):
-// tanh = 1 - 2r and 1 - tanh^2 = 4 w r^2, which keeps full relative accuracy
-// where tanh saturates (1 - tanh^2 formed directly would cancel).  The ex2
-// argument a2x = 2 * log2(e) * y is clamped at 64 so w stays finite; tanh is
-// then 1 to fp32 precision and 4 w r^2 ~ 2^-62 (the true value is smaller
-// still).  One ex2 and one rcp per element; absolute tanh error ~3e-7.
+// tanh(y) and 1 - tanh^2 from w = exp(-2|y|) in (0, 1], r = 1 / (1 + w):
+// |tanh| = 1 - 2 w r and 1 - tanh^2 = 4 w r^2, with the sign of y put back.
+// w never overflows, and 1 - tanh^2 keeps its relative accuracy where tanh
+// saturates (formed as 1 - tanh^2 it would cancel) until w itself leaves
+// fp32's normal range (|y| > 43).  The argument is a2x = 2 * log2(e) * y.
+// One ex2 and one rcp per element; absolute tanh error ~3e-7.
 struct TanhD2 {
     f2 th, omt;  // tanh, 1 - tanh^2
 };
@@ -88,11 +88,14 @@ __device__ __forceinline__ TanhD2 tanh_from_ex2_arg(f2 a2x) {
     const f2 one = pk1(1.f), m2 = pk1(-2.f), four = pk1(4.f);
     float a, b;
     upk(a2x, a, b);
-    const f2 w = pk(ex2f(fminf(a, 64.f)), ex2f(fminf(b, 64.f)));
+    const f2 w = pk(ex2f(-fabsf(a)), ex2f(-fabsf(b)));
     const f2 r = rcpp(add2(w, one));
+    const f2 wr = mul2(w, r);
+    float ta, tb;
+    upk(fma2(wr, m2, one), ta, tb);
     TanhD2 o;
-    o.th = fma2(r, m2, one);
-    o.omt = mul2(mul2(w, r), mul2(r, four));
+    o.th = pk(copysignf(ta, a), copysignf(tb, b));
+    o.omt = mul2(wr, mul2(r, four));
     return o;
 }
 
@@ -119,6 +122,12 @@ struct Pack16<__nv_bfloat16> {
         asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
         return r;
     }
+    // magnitude max(|a|, |b|) per half (the sign bit is not meaningful)
+    __device__ static uint32_t absmax2(uint32_t a, uint32_t b) {
+        uint32_t r;
+        asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+        return r;
+    }
     __device__ static float to_f(uint16_t h) { return __uint_as_float(uint32_t(h) << 16); }
     __device__ static uint16_t from_f(float v) {
         __nv_bfloat16 b = __float2bfloat16_rn(v);
@@ -143,6 +152,12 @@ struct Pack16<__half> {
     __device__ static uint32_t max2(uint32_t a, uint32_t b) {
         uint32_t r;
         asm("max.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+        return r;
+    }
+    // magnitude max(|a|, |b|) per half (the sign bit is not meaningful)
+    __device__ static uint32_t absmax2(uint32_t a, uint32_t b) {
+        uint32_t r;
+        asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
         return r;
     }
     __device__ static float to_f(uint16_t h) {

@@ -10,6 +10,10 @@ enum : int {
     F_RKL = 2,      // reverse-KL sum and its log-ratio gradient term
     F_ENT = 4,      // entropy sum (metric and/or gradient)
     F_SOFTCAP = 8,  // z = s * c * tanh(x / c)
+    // streaming kernel only (the resident kernels take FEAT & F_BASE):
+    F_DCE = 16,     // teacher-entropy sum for the from-distribution CE
+    F_ENTG = 32,    // entropy gradient term (entropy weight nonzero)
+    F_BASE = 15,
 };
 
 // Loss / metric bits (values match enum headloss_flag).

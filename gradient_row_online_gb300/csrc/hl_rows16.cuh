@@ -30,12 +30,13 @@ struct BoolC {
 };
 
 // Scalar twin of the packed element math, for the partial words: tanh and
-// 1 - tanh^2 from w = exp(2y), r = 1 / (1 + w) (see tanh_from_ex2_arg).
+// 1 - tanh^2 from w = exp(-2|y|), r = 1 / (1 + w) (see tanh_from_ex2_arg).
 __device__ __forceinline__ float tanh_a2x_1(float a2x, float* omt = nullptr) {
-    const float w = ex2f(fminf(a2x, 64.f));
+    const float w = ex2f(-fabsf(a2x));
     const float r = rcpf(w + 1.f);
-    if (omt) *omt = (w * r) * (4.f * r);
-    return fmaf(r, -2.f, 1.f);
+    const float wr = w * r;
+    if (omt) *omt = wr * (4.f * r);
+    return copysignf(fmaf(wr, -2.f, 1.f), a2x);
 }
 
 // tanh(y) = y * P(y^2) on |y| <= HL_TANH_POLY_Y0 (FMA pipe only); there
@@ -58,6 +59,40 @@ __device__ __forceinline__ TanhD2 tanh_poly2(f2 y) {
 struct RowCoef {
     float lse2, lseT2, lsq2, pc, ps, tc, ts, qc, bc;
 };
+
+// The gradient pass takes each exponential as 2^(arg + sg) and scales its
+// coefficient by 2^-sg, so terms whose exponential lies below fp32's normal
+// range (ex2 flushes under 2^-126) still reach the 16-bit output, down to its
+// subnormals.  sg = 64 unless a coefficient is so small that its scaled value
+// would leave the normal range with less than 24 bits to spare.
+struct ShiftCoef {
+    float nlse, nlseT, nlsq, pc, ps, tc, ts, qc;  // -lse + sg (base 2), scaled coefficients
+};
+__device__ __forceinline__ ShiftCoef shift_coefs(const RowCoef& k, bool entg) {
+    float cmin = CUDART_INF_F;
+    const float cs[5] = {k.pc, k.ps, k.tc, k.ts, k.qc};
+#pragma unroll
+    for (int i = 0; i < 5; ++i)
+        if (cs[i] != 0.f) cmin = fminf(cmin, fabsf(cs[i]));
+    int sg = 64;
+    if (cmin < CUDART_INF_F) {
+        const int e = int((__float_as_uint(cmin) >> 23) & 0xffu) - 127;  // floor(log2), normal cmin
+        sg = e + 100 < 64 ? (e + 100 > 0 ? e + 100 : 0) : 64;
+    }
+    const float sgf = float(sg);
+    const float sc = __uint_as_float(uint32_t(127 - sg) << 23);  // 2^-sg exactly
+    ShiftCoef o;
+    o.nlse = sgf - k.lse2;
+    o.nlseT = sgf - k.lseT2;
+    o.nlsq = sgf - k.lsq2;
+    // entropy term p (ps * arg + pc) with arg = (arg + sg) - sg
+    o.pc = (entg ? fmaf(-sgf, k.ps, k.pc) : k.pc) * sc;
+    o.ps = k.ps * sc;
+    o.tc = k.tc * sc;
+    o.ts = k.ts * sc;
+    o.qc = k.qc * sc;
+    return o;
+}
 
 // A warp merges the C records of a row (lane k holds record k) and derives
 // the row's gradient coefficients (identical in every lane); with
@@ -532,10 +567,12 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
 
             // ---- pass C: the combined gradient, written once ----
             if (gg != nullptr) {
+                // exponentials offset by 2^sg, coefficients scaled by 2^-sg
+                const ShiftCoef h = shift_coefs(k, ENT);
                 const float dlse = k.lseT2 - k.lsq2;
-                const f2 nlse2 = pk1(-k.lse2), nlseT2 = pk1(-k.lseT2), nlsq2 = pk1(-k.lsq2);
-                const f2 pc2 = pk1(k.pc), ps2 = pk1(k.ps), tc2 = pk1(k.tc), ts2 = pk1(k.ts);
-                const f2 qc2 = pk1(k.qc), s2 = pk1(s), ns2 = pk1(-s), ndlse2 = pk1(-dlse);
+                const f2 nlse2 = pk1(h.nlse), nlseT2 = pk1(h.nlseT), nlsq2 = pk1(h.nlsq);
+                const f2 pc2 = pk1(h.pc), ps2 = pk1(h.ps), tc2 = pk1(h.tc), ts2 = pk1(h.ts);
+                const f2 qc2 = pk1(h.qc), s2 = pk1(s), ns2 = pk1(-s), ndlse2 = pk1(-dlse);
                 const f2 nKT2 = pk1(-KT);
                 // word and element of the label column in this slice (or none)
                 const int64_t ey = (has_labels && y >= col0 && y < col1) ? r * V + y : -1;
@@ -595,20 +632,20 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                                 float zs, om1 = 1.f;
                                 if (CAP) zs = __fmul_rn(tanh_a2x_1(__fmul_rn(xv1, A2), &om1), Kc);
                                 else zs = __fmul_rn(xv1, K);
-                                const float arg = zs - k.lse2;
-                                float g1 = ex2f(arg) * (ENT ? fmaf(k.ps, arg, k.pc) : k.pc);
+                                const float arg = zs + h.nlse;
+                                float g1 = ex2f(arg) * (ENT ? fmaf(h.ps, arg, h.pc) : h.pc);
                                 if (TEACH) {
                                     const float tv1 = P16::to_f(ts[w * EPW + iy]);
-                                    const float pT = ex2f(fmaf(zs, invT, -k.lseT2));
-                                    const float q = ex2f(fmaf(tv1, KT, -k.lsq2));
-                                    float tco = k.tc;
+                                    const float pT = ex2f(fmaf(zs, invT, h.nlseT));
+                                    const float q = ex2f(fmaf(tv1, KT, h.nlsq));
+                                    float tco = h.tc;
                                     if (RKL) {
                                         const float dxu = CAP ? fmaf(tv1, -LOG2E, zs) * invT
                                                               : fmaf(xv1, s, -tv1) * KT;
-                                        tco = fmaf(k.ts, dxu - dlse, k.tc);
+                                        tco = fmaf(h.ts, dxu - dlse, h.tc);
                                     }
                                     g1 = fmaf(pT, tco, g1);
-                                    g1 = fmaf(q, k.qc, g1);
+                                    g1 = fmaf(q, h.qc, g1);
                                 }
                                 g1 -= k.bc;
                                 if (CAP) g1 *= om1;
@@ -627,20 +664,20 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                                 } else {
                                     zs = __fmul_rn(xv, K);
                                 }
-                                const float arg = zs - k.lse2;
-                                float g = ex2f(arg) * (ENT ? fmaf(k.ps, arg, k.pc) : k.pc);
+                                const float arg = zs + h.nlse;
+                                float g = ex2f(arg) * (ENT ? fmaf(h.ps, arg, h.pc) : h.pc);
                                 if (TEACH) {
                                     const float tv = P16::to_f(ts[w * EPW + i]);
-                                    const float pT = ex2f(fmaf(zs, invT, -k.lseT2));
-                                    const float q = ex2f(fmaf(tv, KT, -k.lsq2));
-                                    float tco = k.tc;
+                                    const float pT = ex2f(fmaf(zs, invT, h.nlseT));
+                                    const float q = ex2f(fmaf(tv, KT, h.nlsq));
+                                    float tco = h.tc;
                                     if (RKL) {
                                         const float dxu = CAP ? fmaf(tv, -LOG2E, zs) * invT
                                                               : fmaf(xv, s, -tv) * KT;
-                                        tco = fmaf(k.ts, dxu - dlse, k.tc);
+                                        tco = fmaf(h.ts, dxu - dlse, h.tc);
                                     }
                                     g = fmaf(pT, tco, g);
-                                    g = fmaf(q, k.qc, g);
+                                    g = fmaf(q, h.qc, g);
                                 }
                                 if (eb + i == ey) g -= k.bc;
                                 if (CAP) g *= dz;

@@ -1,5 +1,5 @@
-// hl_rows_bf16.cu -- 16-bit row-kernel instantiations (resident and streaming) for bf16 logits (one per feature set).
-#include "hl_stream16.cuh"
+// hl_rows_bf16.cu -- resident 16-bit row-kernel instantiations for bf16 logits (one per feature set).
+#include "hl_rows16.cuh"
 
 namespace hl {
 
@@ -7,29 +7,6 @@ namespace hl {
     case F: return reinterpret_cast<const void*>(&rows_kernel16<__nv_bfloat16, F>);
 
 const void* rows_kernel_bf16(int feat) {
-    switch (feat) {
-        HL_CASE(0)
-        HL_CASE(F_ENT)
-        HL_CASE(F_TEACH)
-        HL_CASE(F_TEACH | F_ENT)
-        HL_CASE(F_TEACH | F_RKL)
-        HL_CASE(F_TEACH | F_RKL | F_ENT)
-        HL_CASE(F_SOFTCAP)
-        HL_CASE(F_SOFTCAP | F_ENT)
-        HL_CASE(F_SOFTCAP | F_TEACH)
-        HL_CASE(F_SOFTCAP | F_TEACH | F_ENT)
-        HL_CASE(F_SOFTCAP | F_TEACH | F_RKL)
-        HL_CASE(F_SOFTCAP | F_TEACH | F_RKL | F_ENT)
-        default: return nullptr;
-    }
-}
-
-#undef HL_CASE
-
-#define HL_CASE(F) \
-    case F: return reinterpret_cast<const void*>(&stream_kernel16<__nv_bfloat16, F>);
-
-const void* stream_kernel_bf16(int feat) {
     switch (feat) {
         HL_CASE(0)
         HL_CASE(F_ENT)

@@ -4,22 +4,31 @@
 // A row is streamed through a ring of shared-memory chunk slots twice:
 //
 //   pass 1  chunks 0 .. K-1: online row statistics.  Each thread keeps its
-//           own running shifts (student max -- or s*c*log2e under softcap --
-//           and teacher max) and rescales its sums when a shift moves;
+//           own shifts (student: s*c*log2e under softcap, else a lazily
+//           raised running maximum; teacher: a lazily raised running
+//           maximum) and rescales its sums only when a chunk's maximum
+//           rises more than TAU above the shift, which after the first
+//           chunk almost never happens;
 //   merge   the thread records merge across the warp (butterfly), then across
 //           the CTA's warps, and warp 0 derives the row's losses and gradient
 //           coefficients (the same epilogue as the resident kernel);
 //   pass 2  chunks K-1 .. 0 (reverse order, so the chunks read most recently
 //           -- the ones most likely still in L2 -- come back first): the
-//           combined gradient, written once from registers.  Under softcap
-//           both passes take tanh from the FMA-pipe polynomial when every
-//           chunk of the row is in its range, else from ex2 + rcp.
+//           combined gradient, written once from registers.
 //
-// The chunk stream (row, pass, chunk) is one sequence per CTA; a thread of
-// the last warp to finish a chunk issues the bulk copy of the entry that
-// reuses its slot, so copies for the next row start while this row finishes.
-// The second read of a row is served by L2 when the row's chunks are still
-// resident; the DRAM bytes it costs are measured, not assumed.
+// Softcap transform, per (warp, chunk): zs = s*c*log2e*tanh(x/c) is x * Q(x^2)
+// with the scale folded into the polynomial Q when the chunk's max |x| / c is
+// within a fitted range (tier A: degree 3 on |y| <= 0.45; tier B: degree 5
+// on |y| <= 0.8), else tanh comes from ex2 + rcp (tier X).  Pass 1 records
+// each warp's tier per chunk; pass 2, which visits the same elements with the
+// same threads, reuses it.
+//
+// The chunk stream (row, pass, chunk) is one sequence per CTA; the ring slot
+// and phase of each entry advance incrementally, and a thread of the last
+// warp to finish an entry issues the bulk copy of the entry S places later
+// into the same slot, so copies for the next row start while this row
+// finishes.  The second read of a row is served by L2 when the row's chunks
+// are still resident; the DRAM bytes it costs are measured, not assumed.
 //
 // Rows must be 16-byte aligned (V * 2 a multiple of 16); the planner sends
 // other shapes to the resident kernel, which handles ragged rows.
@@ -35,7 +44,7 @@ struct TRec {
 };
 
 // Merges b into a (commutative: a + b and b + a give identical results).
-template <bool TEACH, bool RKL, bool ENT>
+template <bool TEACH, bool RKL, bool ENT, bool DCE>
 __device__ __forceinline__ void trec_merge(TRec& a, const TRec& b, float invT) {
     const bool la = a.S > 0.f, lb = b.S > 0.f;
     const float M = fmaxf(la ? a.zm : -CUDART_INF_F, lb ? b.zm : -CUDART_INF_F);
@@ -56,7 +65,7 @@ __device__ __forceinline__ void trec_merge(TRec& a, const TRec& b, float invT) {
         o.um = (la || lb) ? Mu : a.um;
         o.ST = ta * a.ST + tb * b.ST;
         o.Sq = ba * a.Sq + bb * b.Sq;
-        o.Eq = ba * (a.Eq + dua * a.Sq) + bb * (b.Eq + dub * b.Sq);
+        o.Eq = DCE ? ba * (a.Eq + dua * a.Sq) + bb * (b.Eq + dub * b.Sq) : 0.f;
         o.Xp = ba * (a.Xp + (dua - dTa) * a.Sq) + bb * (b.Xp + (dub - dTb) * b.Sq);
         o.Y = RKL ? ta * (a.Y - (dua - dTa) * a.ST) + tb * (b.Y - (dub - dTb) * b.ST) : 0.f;
     } else {
@@ -82,6 +91,15 @@ __device__ __forceinline__ TRec trec_shfl_xor(const TRec& a, int o) {
     return b;
 }
 
+template <int I>
+struct IntC {
+    static constexpr int value = I;
+};
+
+// Largest rise (base-2 units) of a value above its running shift before the
+// sums are rescaled: terms stay below 2^TAU, far from fp32 overflow.
+constexpr float STREAM_TAU = 16.f;
+
 template <typename DT, int FEAT>
 __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_constant__ Params p) {
     using P16 = Pack16<DT>;
@@ -91,6 +109,8 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
     constexpr bool RKL = (FEAT & F_RKL) != 0;
     constexpr bool ENT = (FEAT & F_ENT) != 0;
     constexpr bool CAP = (FEAT & F_SOFTCAP) != 0;
+    constexpr bool DCE = TEACH && (FEAT & F_DCE) != 0;
+    constexpr bool ENTG = ENT && (FEAT & F_ENTG) != 0;
     constexpr int OPS = TEACH ? 2 : 1;
 
     extern __shared__ __align__(128) unsigned char smem[];
@@ -111,6 +131,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
 
     const int64_t N = p.N, V = p.V;
     const int K = int((V + CH - 1) / CH);                // chunks per row
+    const int K2x = 2 * K;                               // stream entries per row
     const int64_t G = gridDim.x;
     const DT* __restrict__ xg = static_cast<const DT*>(p.x);
     const DT* __restrict__ tg = static_cast<const DT*>(p.t);
@@ -124,35 +145,92 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
     const float Kc = CAP ? s * p.softcap * LOG2E : 0.f;
     const float invT = 1.f / p.T;
     const float KT = LOG2E * invT;
-    // softcap: the student shift is the constant Kc unless exp(-2 Kc) could
-    // underflow, in which case it follows the running max like the teacher
-    const bool fixed_shift = CAP && Kc <= 60.f;
+    // softcap: the student shift is the constant Kc when every shifted term,
+    // at temperature 1 and T, stays above 2^-120 (|zs| <= Kc); otherwise it
+    // follows the running maximum like the teacher's
+    const bool fixed_shift = CAP && Kc * fmaxf(1.f, invT) <= 60.f;
+    // tier bounds on max |x| (tanh argument x / c); the narrow tier's fit
+    // error (2.4e-7 relative) stays below fp32 rounding of exp(zs) only while
+    // |zs| is moderate, so it is used for Kc <= 48 alone
+    const float XA = (CAP && Kc <= 48.f) ? HL_TANH_A_Y0 * p.softcap : 0.f;
+    const float XB = CAP ? HL_TANH_B_Y0 * p.softcap : 0.f;
+    // zs = x * Q(x^2): Q_k = s * log2e * C_k / c^(2k), formed in double
+    f2 QA[4], QB[6];
+    {
+        const double ic2 = CAP ? 1.0 / (double(p.softcap) * double(p.softcap)) : 0.0;
+        const double ca[4] = {HL_TANH_A_C0, HL_TANH_A_C1, HL_TANH_A_C2, HL_TANH_A_C3};
+        const double cb[6] = {HL_TANH_B_C0, HL_TANH_B_C1, HL_TANH_B_C2,
+                              HL_TANH_B_C3, HL_TANH_B_C4, HL_TANH_B_C5};
+        double f = double(s) * 1.4426950408889634;
+#pragma unroll
+        for (int k = 0; k < 6; ++k) {
+            if (k < 4) QA[k] = pk1(float(ca[k] * f));
+            QB[k] = pk1(float(cb[k] * f));
+            f *= ic2;
+        }
+    }
     const f2 K2 = pk1(K1), A22 = pk1(A2), Kc2 = pk1(Kc), invT2 = pk1(invT), KT2 = pk1(KT);
-    const f2 invc2 = pk1(invc), KcT2 = pk1(Kc * invT);
+    const f2 KinvT2 = pk1(K1 * invT);
+    const f2 m2 = pk1(CAP ? -1.f / (Kc * Kc) : 0.f), one2 = pk1(1.f);
     const f2 z2 = pk1(0.f);
 
     auto zs1 = [&](float v) -> float {
         return CAP ? __fmul_rn(tanh_a2x_1(__fmul_rn(v, A2)), Kc) : __fmul_rn(v, K1);
     };
-    auto th2 = [&](f2 xv, auto poly) -> TanhD2 {
-        if constexpr (decltype(poly)::value) return tanh_poly2(mul2(xv, invc2));
-        else return tanh_from_ex2_arg(mul2(xv, A22));
+    // zs + nshift of a pair (pass 1), by tier
+    auto shifted = [&](f2 xv, f2 nshift, auto tierc) -> f2 {
+        constexpr int TI = CAP ? decltype(tierc)::value : -1;
+        if constexpr (TI < 0) {
+            return fma2(xv, K2, nshift);
+        } else if constexpr (TI == 0) {
+            const f2 u = mul2(xv, xv);
+            f2 q = fma2(u, QA[3], QA[2]);
+            q = fma2(q, u, QA[1]);
+            q = fma2(q, u, QA[0]);
+            return fma2(xv, q, nshift);
+        } else if constexpr (TI == 1) {
+            const f2 u = mul2(xv, xv);
+            f2 q = fma2(u, QB[5], QB[4]);
+            q = fma2(q, u, QB[3]);
+            q = fma2(q, u, QB[2]);
+            q = fma2(q, u, QB[1]);
+            q = fma2(q, u, QB[0]);
+            return fma2(xv, q, nshift);
+        } else {
+            return fma2(tanh_from_ex2_arg(mul2(xv, A22)).th, Kc2, nshift);
+        }
+    };
+    // zs and 1 - tanh^2 of a pair (pass 2, softcap), by tier
+    auto zs_omt = [&](f2 xv, f2& zs, f2& omt, auto tierc) {
+        constexpr int TI = decltype(tierc)::value;
+        if constexpr (TI == 0 || TI == 1) {
+            const f2 u = mul2(xv, xv);
+            f2 q;
+            if constexpr (TI == 0) {
+                q = fma2(u, QA[3], QA[2]);
+                q = fma2(q, u, QA[1]);
+                q = fma2(q, u, QA[0]);
+            } else {
+                q = fma2(u, QB[5], QB[4]);
+                q = fma2(q, u, QB[3]);
+                q = fma2(q, u, QB[2]);
+                q = fma2(q, u, QB[1]);
+                q = fma2(q, u, QB[0]);
+            }
+            zs = mul2(xv, q);
+            omt = fma2(zs, mul2(zs, m2), one2);  // 1 - (zs / Kc)^2; |tanh| <= 0.67 here
+        } else {
+            const TanhD2 td = tanh_from_ex2_arg(mul2(xv, A22));
+            zs = mul2(td.th, Kc2);
+            omt = td.omt;
+        }
     };
 
-    // stream entry J -> (row, chunk); pass 1 then pass 2 (reverse) per row
-    const int64_t per_row = 2 * int64_t(K);
-    auto entry = [&](int64_t J, int64_t& r, int& c) {
-        const int64_t it = J / per_row;
-        const int jl = int(J - it * per_row);
-        c = jl < K ? jl : 2 * K - 1 - jl;
-        r = int64_t(blockIdx.x) + it * G;
-    };
-    auto issue = [&](int64_t J) {
-        int64_t r;
-        int c;
-        entry(J, r, c);
+    // stream position -> copy: entry jl of row r (jl < K: pass-1 chunk jl;
+    // else pass-2 chunk 2K-1-jl) into ring slot sl
+    auto issue = [&](int sl, int64_t r, int jl) {
         if (r >= N) return;
-        const int sl = int(J % S);
+        const int c = jl < K ? jl : K2x - 1 - jl;
         const uint32_t bar = smem_addr(&bars[sl]);
         const int64_t c0 = int64_t(c) * CH;
         const int64_t len = (V - c0) < CH ? (V - c0) : CH;
@@ -160,11 +238,19 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         fence_proxy_async();
         mbar_arrive_expect_tx(bar, bytes * OPS);
 #ifdef HL_FAULT_INJECT
-        if (r == p.drop_row && J % per_row == 0) return;  // pass-1 chunk 0 never comes
+        if (r == p.drop_row && jl == 0) return;  // pass-1 chunk 0 never comes
 #endif
         const uint32_t dst = smem_addr(smem + size_t(sl) * slot_bytes);
         bulk_g2s(dst, xg + r * V + c0, bytes, bar);
         if (TEACH) bulk_g2s(dst + opbytes, tg + r * V + c0, bytes, bar);
+    };
+    // the entry `ahead` places after (r, jl)
+    auto advance = [&](int64_t& r, int& jl, int ahead) {
+        jl += ahead;
+        while (jl >= K2x) {
+            jl -= K2x;
+            r += G;
+        }
     };
 
     if (tid == 0) {
@@ -176,33 +262,46 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         for (int i = 0; i < NACC; ++i) acc[i] = 0.0;
     }
     __syncthreads();
-    if (tid == 0)
-        for (int j = 0; j < S; ++j) issue(j);
+    if (tid == 0) {
+        for (int j = 0; j < S; ++j) {
+            int64_t r = blockIdx.x;
+            int jl = 0;
+            advance(r, jl, j);
+            issue(j, r, jl);
+        }
+    }
 
-    int64_t J = 0;  // stream entries consumed by this thread
+    int slot = 0;
+    uint32_t phase = 0;               // ring slot and phase parity of the next entry
     uint32_t lost = 0, lost_par = 0;  // slots (and phase parities) whose wait gave up
-    // wait for entry J's slot; returns its shared-memory base
-    auto acquire = [&](int64_t jj) -> const unsigned char* {
-        const int sl = int(jj % S);
-        const uint32_t par = uint32_t((jj / S) & 1);
-        if (!mbar_wait_bounded(smem_addr(&bars[sl]), par, p.wait_ns)) {
-            lost |= 1u << sl;
-            lost_par = (lost_par & ~(1u << sl)) | (par << sl);
+    // wait for the current entry's slot; returns its shared-memory base
+    auto acquire = [&]() -> const unsigned char* {
+        if (!mbar_wait_bounded(smem_addr(&bars[slot]), phase, p.wait_ns)) {
+            lost |= 1u << slot;
+            lost_par = (lost_par & ~(1u << slot)) | (phase << slot);
             if (lane == 0) atomicOr(p.err, E_TIMEOUT);
         }
-        return smem + size_t(sl) * slot_bytes;
+        return smem + size_t(slot) * slot_bytes;
     };
-    // this warp is done with entry jj; the last warp refills the slot
-    auto release = [&](int64_t jj) {
+    // this warp is done with the current entry (row r, position jl); the last
+    // warp refills the slot with the entry S places later; then step the ring
+    auto release = [&](int64_t r, int jl) {
         __syncwarp();
         if (lane == 0) {
-            const int sl = int(jj % S);
             __threadfence_block();
-            const int old = atomicAdd(&done[sl], 1);
-            if (old + 1 == int((jj / S) + 1) * nwarps) {
+            const int old = atomicAdd(&done[slot], 1);
+            if (old + 1 == nwarps) {
+                // every warp has left this slot; the next use can count again
+                // (the copy below completes before any warp touches the slot)
+                done[slot] = 0;
                 __threadfence_block();
-                issue(jj + S);
+                advance(r, jl, S);
+                issue(slot, r, jl);
             }
+        }
+        if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
         }
     };
 
@@ -218,30 +317,29 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         if (has_labels && y >= V && tid == 0) atomicOr(p.err, E_LABEL);
 
         if (!valid) {  // a masked row: consume its entries, write exact +0
-            for (int c = 0; c < 2 * K; ++c, ++J) {
-                acquire(J);
-                const int cc = c < K ? c : 2 * K - 1 - c;
-                if (c >= K && gg != nullptr) {
+            for (int jl = 0; jl < K2x; ++jl) {
+                acquire();
+                const int cc = jl < K ? jl : K2x - 1 - jl;
+                if (jl >= K && gg != nullptr) {
                     const int64_t c0 = int64_t(cc) * CH;
                     const int nwc = int(((V - c0) < CH ? (V - c0) : CH) / EPW);
                     for (int w = tid; w < nwc; w += nthr)
                         *reinterpret_cast<uint4*>(gg + r * V + c0 + int64_t(w) * EPW) =
                             make_uint4(0, 0, 0, 0);
                 }
-                release(J);
+                release(r, jl);
             }
             continue;
         }
 
         // ---------------- pass 1: online statistics ----------------
-        float xm = -CUDART_INF_F, tm = -CUDART_INF_F;  // running raw maxima
         float zm = fixed_shift ? Kc : -CUDART_INF_F, um = -CUDART_INF_F;
-        float amax = 0.f;  // softcap: running max |x|
         f2 S2 = z2, E2 = z2, ST2 = z2, Sq2 = z2, Eq2 = z2, Xp2 = z2, Y2 = z2;
         float zy = 0.f, hasy = 0.f;
-        int needexp = 0;  // softcap: a chunk of this thread's fell outside the polynomial range
-        for (int c = 0; c < K; ++c, ++J) {
-            const unsigned char* sb = acquire(J);
+        uint64_t tiers = 0;  // softcap: 2 bits per chunk (chunks 0..31) of this warp
+        int tier_hi = 0;     // softcap: highest tier of chunks 32.. of this warp
+        for (int c = 0; c < K; ++c) {
+            const unsigned char* sb = acquire();
             const int64_t c0 = int64_t(c) * CH;
             const int nwc = int(((V - c0) < CH ? (V - c0) : CH) / EPW);
             uint4 xw[4], tw[4];
@@ -255,47 +353,57 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                     nmine = i + 1;
                 }
             }
-            // chunk maxima of this thread's words (packed), then the running shifts
-            uint32_t mx = CAP ? 0u : P16::NEG_INF2, mt = P16::NEG_INF2;
+            // chunk maxima of this thread's words on packed pairs: max |x|
+            // (softcap tier), signed max x (shift, unless fixed), max t
+            uint32_t ma = 0u, ms = P16::NEG_INF2, mt = P16::NEG_INF2;
+            auto maxima = [&](auto sxc) {
+                constexpr bool SX = decltype(sxc)::value;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (i < nmine) {
-                    uint4 a = xw[i];
-                    if (CAP) {
-                        a.x &= 0x7fff7fffu;
-                        a.y &= 0x7fff7fffu;
-                        a.z &= 0x7fff7fffu;
-                        a.w &= 0x7fff7fffu;
-                    }
-                    mx = P16::max2(P16::max2(mx, a.x), P16::max2(a.y, a.z));
-                    mx = P16::max2(mx, a.w);
-                    if (TEACH) {
-                        mt = P16::max2(P16::max2(mt, tw[i].x), P16::max2(tw[i].y, tw[i].z));
-                        mt = P16::max2(mt, tw[i].w);
+                for (int i = 0; i < 4; ++i) {
+                    if (i < nmine) {
+                        const uint4 a = xw[i];
+                        if (CAP) {
+                            ma = P16::absmax2(ma, P16::absmax2(P16::absmax2(a.x, a.y),
+                                                               P16::absmax2(a.z, a.w)));
+                        }
+                        if (SX) {
+                            ms = P16::max2(ms, P16::max2(P16::max2(a.x, a.y),
+                                                         P16::max2(a.z, a.w)));
+                        }
+                        if (TEACH) {
+                            const uint4 b = tw[i];
+                            mt = P16::max2(mt, P16::max2(P16::max2(b.x, b.y),
+                                                         P16::max2(b.z, b.w)));
+                        }
                     }
                 }
-            }
+            };
+            const bool need_sx = !CAP || !fixed_shift;
+            if (need_sx) maxima(BoolC<true>{});
+            else maxima(BoolC<false>{});
             float ca, cb;
-            upk(P16::unpack(mx), ca, cb);
-            const float cx = fmaxf(ca, cb);
-            float newz = zm, newu = um;
-            if (CAP) amax = fmaxf(amax, cx);
-            if (!fixed_shift) {
-                // without softcap the chunk max is the raw max; under a large
-                // softcap the bound of |x| bounds z as well
-                xm = fmaxf(xm, cx);
-                newz = nmine ? zs1(xm) : zm;
+            // lazy shifts: raise a shift only when the chunk's max exceeds it by TAU
+            float nz = zm, nu = um;
+            bool mv = false;
+            if (need_sx && nmine) {
+                upk(P16::unpack(ms), ca, cb);
+                const float bz = zs1(fmaxf(ca, cb));
+                if (bz > zm + STREAM_TAU) {
+                    nz = bz;
+                    mv = true;
+                }
             }
-            if (TEACH) {
+            if (TEACH && nmine) {
                 upk(P16::unpack(mt), ca, cb);
-                tm = fmaxf(tm, fmaxf(ca, cb));
-                newu = nmine ? __fmul_rn(tm, KT) : um;
+                const float bu = __fmul_rn(fmaxf(ca, cb), KT);
+                if (bu > um + STREAM_TAU) {
+                    nu = bu;
+                    mv = true;
+                }
             }
-            // rescale the sums when a shift moved (warp-uniform decision)
-            const bool moved = (newz != zm) || (TEACH && newu != um);
-            if (__any_sync(0xffffffffu, moved)) {
-                const float d = (zm == -CUDART_INF_F) ? 0.f : zm - newz;
-                const float du = (um == -CUDART_INF_F) ? 0.f : um - newu;
+            if (__any_sync(0xffffffffu, mv)) {
+                const float d = (zm == -CUDART_INF_F) ? 0.f : zm - nz;
+                const float du = (um == -CUDART_INF_F) ? 0.f : um - nu;
                 const float al = exp2f(d), dTv = d * invT;
                 const f2 al2 = pk1(al), d2 = pk1(d);
                 if (ENT) E2 = mul2(al2, fma2(d2, S2, E2));
@@ -305,20 +413,26 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                     const f2 alT2 = pk1(alT), be2 = pk1(be), du2 = pk1(du);
                     const f2 w2 = pk1(du - dTv);
                     Xp2 = mul2(be2, fma2(w2, Sq2, Xp2));
-                    Eq2 = mul2(be2, fma2(du2, Sq2, Eq2));
+                    if (DCE) Eq2 = mul2(be2, fma2(du2, Sq2, Eq2));
                     if (RKL) Y2 = mul2(alT2, fma2(w2, ST2, Y2));
                     ST2 = mul2(alT2, ST2);
                     Sq2 = mul2(be2, Sq2);
                 }
-                zm = newz;
-                um = newu;
+                zm = nz;
+                um = nu;
             }
-            // the polynomial tanh covers these words when max |x| / c is in range
-            const bool poly_ok = !CAP || __fmul_rn(cx, invc) <= HL_TANH_POLY_Y0;
-            const bool use_poly = CAP && __all_sync(0xffffffffu, poly_ok);
-            if (CAP && !use_poly) needexp = 1;
-            const f2 zm2 = pk1(zm), um2 = pk1(um), nzm2 = pk1(-zm);
-            auto sums = [&](auto polyc) {
+            // softcap tier of this warp's words in the chunk
+            int tier = 0;
+            if (CAP) {
+                upk(P16::unpack(ma), ca, cb);
+                const float cx = fmaxf(fabsf(ca), fabsf(cb));
+                tier = __all_sync(0xffffffffu, cx <= XA) ? 0
+                       : __all_sync(0xffffffffu, cx <= XB) ? 1 : 2;
+                if (c < 32) tiers |= uint64_t(tier) << (2 * c);
+                else tier_hi = tier > tier_hi ? tier : tier_hi;
+            }
+            const f2 nzm2 = pk1(-zm), num2 = pk1(-um);
+            auto sums = [&](auto tierc) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     if (i >= nmine) continue;
@@ -326,8 +440,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                     const uint32_t tb[4] = {tw[i].x, tw[i].y, tw[i].z, tw[i].w};
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const f2 xv = P16::unpack(xa[kk]);
-                        const f2 d = CAP ? fma2(th2(xv, polyc).th, Kc2, nzm2) : sub2(mul2(xv, K2), zm2);
+                        const f2 d = shifted(P16::unpack(xa[kk]), nzm2, tierc);
                         const f2 e = ex2p(d);
                         S2 = add2(S2, e);
                         if (ENT) E2 = fma2(e, d, E2);
@@ -335,10 +448,10 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                             const f2 dT = mul2(d, invT2);
                             const f2 eT = ex2p(dT);
                             ST2 = add2(ST2, eT);
-                            const f2 du = sub2(mul2(P16::unpack(tb[kk]), KT2), um2);
+                            const f2 du = fma2(P16::unpack(tb[kk]), KT2, num2);
                             const f2 eq = ex2p(du);
                             Sq2 = add2(Sq2, eq);
-                            Eq2 = fma2(eq, du, Eq2);
+                            if (DCE) Eq2 = fma2(eq, du, Eq2);
                             const f2 wd = sub2(du, dT);
                             Xp2 = fma2(eq, wd, Xp2);
                             if (RKL) Y2 = fma2(eT, wd, Y2);
@@ -346,8 +459,9 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                     }
                 }
             };
-            if (use_poly) sums(BoolC<true>{});
-            else sums(BoolC<false>{});
+            if (tier == 0) sums(IntC<0>{});
+            else if (tier == 1) sums(IntC<1>{});
+            else sums(IntC<2>{});
             // the label column's logit, from the thread that holds it
             if (has_labels && y >= c0 && y < c0 + int64_t(nwc) * EPW) {
                 const int wl = int((y - c0) / EPW);
@@ -356,7 +470,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                     hasy = 1.f;
                 }
             }
-            release(J);
+            release(r, c);
         }
 
         // ---------------- merge: threads -> warps -> row ----------------
@@ -373,7 +487,8 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         tr.zy = zy;
         tr.hasy = hasy;
 #pragma unroll
-        for (int o = 16; o; o >>= 1) trec_merge<TEACH, RKL, ENT>(tr, trec_shfl_xor(tr, o), invT);
+        for (int o = 16; o; o >>= 1)
+            trec_merge<TEACH, RKL, ENT, DCE>(tr, trec_shfl_xor(tr, o), invT);
         if (lane == 0) {
             float* rec = xch + warp * NREC;
             rec[R_ZM] = tr.zm;
@@ -388,8 +503,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             rec[R_ZY] = tr.zy;
             rec[R_HASY] = tr.hasy;
         }
-        // the barrier also ORs "some chunk needed the exp tanh" over the CTA
-        const bool row_exp = __syncthreads_or(CAP && needexp) != 0;
+        __syncthreads();
         if (warp == 0) {
             const RowCoef kw =
                 row_epilogue16<TEACH, RKL, ENT, CAP>(p, xch, nwarps, true, old_lp, adv, acc, lane);
@@ -399,21 +513,24 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         const RowCoef k = *reinterpret_cast<const RowCoef*>(coefs);
 
         // ---------------- pass 2: the gradient, reverse chunk order ----------------
+        // exponentials offset by 2^sg, coefficients scaled by 2^-sg
+        const ShiftCoef h = shift_coefs(k, ENTG);
         const float dlse = k.lseT2 - k.lsq2;
-        const f2 nlse2 = pk1(-k.lse2), nlseT2 = pk1(-k.lseT2), nlsq2 = pk1(-k.lsq2);
-        const f2 pc2 = pk1(k.pc), ps2 = pk1(k.ps), tc2 = pk1(k.tc), ts2 = pk1(k.ts);
-        const f2 qc2 = pk1(k.qc), s2 = pk1(s), ns2 = pk1(-s), ndlse2 = pk1(-dlse);
+        const f2 nlse2 = pk1(h.nlse), nlseT2 = pk1(h.nlseT), nlsq2 = pk1(h.nlsq);
+        const f2 pc2 = pk1(h.pc), ps2 = pk1(h.ps), tc2 = pk1(h.tc), ts2 = pk1(h.ts);
+        const f2 qc2 = pk1(h.qc), s2 = pk1(s), ndlse2 = pk1(-dlse);
         const f2 nKT2 = pk1(-KT);
-        for (int cr = 0; cr < K; ++cr, ++J) {
+        for (int cr = 0; cr < K; ++cr) {
             const int c = K - 1 - cr;
-            const unsigned char* sb = acquire(J);
+            const unsigned char* sb = acquire();
             if (gg != nullptr) {
                 const int64_t c0 = int64_t(c) * CH;
                 const int nwc = int(((V - c0) < CH ? (V - c0) : CH) / EPW);
                 const int64_t wy = (has_labels && y >= c0 && y < c0 + int64_t(nwc) * EPW)
                                        ? (y - c0) / EPW : -1;
                 const int iy = int((y - c0) % EPW);
-                auto grad = [&](auto polyc) {
+                DT* grow = gg + r * V + c0;
+                auto grad = [&](auto tierc) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int w = tid + i * nthr;
@@ -427,26 +544,24 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             const f2 xv = P16::unpack(xa[kk]);
-                            f2 th = z2, omt = z2, arg, argT = z2;
-                            if (CAP) {
-                                const TanhD2 td = th2(xv, polyc);
-                                th = td.th;
-                                omt = td.omt;
-                                arg = fma2(th, Kc2, nlse2);
-                                if (TEACH) argT = fma2(th, KcT2, nlseT2);
-                            } else {
-                                const f2 zs = mul2(xv, K2);
+                            f2 zs = z2, omt = z2, arg, argT = z2;
+                            if constexpr (CAP) {
+                                zs_omt(xv, zs, omt, tierc);
                                 arg = add2(zs, nlse2);
                                 if (TEACH) argT = fma2(zs, invT2, nlseT2);
+                            } else {
+                                arg = fma2(xv, K2, nlse2);
+                                if (TEACH) argT = fma2(xv, KinvT2, nlseT2);
                             }
-                            f2 g = mul2(ex2p(arg), ENT ? fma2(ps2, arg, pc2) : pc2);
+                            f2 g = mul2(ex2p(arg), ENTG ? fma2(ps2, arg, pc2) : pc2);
                             if (TEACH) {
                                 const f2 tv = P16::unpack(tb[kk]);
                                 const f2 pT = ex2p(argT);
                                 const f2 q = ex2p(fma2(tv, KT2, nlsq2));
                                 f2 tco = tc2;
                                 if (RKL) {
-                                    const f2 dxu = CAP ? fma2(th, KcT2, mul2(tv, nKT2))
+                                    // log pT - log q from the logit difference
+                                    const f2 dxu = CAP ? fma2(zs, invT2, mul2(tv, nKT2))
                                                        : mul2(fma2(xv, s2, sub2(z2, tv)), KT2);
                                     tco = fma2(ts2, add2(dxu, ndlse2), tc2);
                                 }
@@ -456,7 +571,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                             // dz/dx = s (1 - tanh^2); s is already in the coefficients
                             out[kk] = P16::pack(CAP ? mul2(g, omt) : g);
                         }
-                        *reinterpret_cast<uint4*>(gg + r * V + c0 + int64_t(w) * EPW) =
+                        *reinterpret_cast<uint4*>(grow + int64_t(w) * EPW) =
                             make_uint4(out[0], out[1], out[2], out[3]);
                         if (w == wy) {
                             // the label column: this thread recomputes that one element
@@ -467,33 +582,35 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                             float zs, om1 = 1.f;
                             if (CAP) zs = __fmul_rn(tanh_a2x_1(__fmul_rn(xv1, A2), &om1), Kc);
                             else zs = __fmul_rn(xv1, K1);
-                            const float arg = zs - k.lse2;
-                            float g1 = ex2f(arg) * (ENT ? fmaf(k.ps, arg, k.pc) : k.pc);
+                            const float arg = zs + h.nlse;
+                            float g1 = ex2f(arg) * (ENTG ? fmaf(h.ps, arg, h.pc) : h.pc);
                             if (TEACH) {
                                 const float tv1 = P16::to_f(
                                     reinterpret_cast<const uint16_t*>(sb + opbytes)[w * EPW + iy]);
-                                const float pT = ex2f(fmaf(zs, invT, -k.lseT2));
-                                const float q = ex2f(fmaf(tv1, KT, -k.lsq2));
-                                float tco = k.tc;
+                                const float pT = ex2f(fmaf(zs, invT, h.nlseT));
+                                const float q = ex2f(fmaf(tv1, KT, h.nlsq));
+                                float tco = h.tc;
                                 if (RKL) {
                                     const float dxu = CAP ? fmaf(tv1, -LOG2E, zs) * invT
                                                           : fmaf(xv1, s, -tv1) * KT;
-                                    tco = fmaf(k.ts, dxu - dlse, k.tc);
+                                    tco = fmaf(h.ts, dxu - dlse, h.tc);
                                 }
                                 g1 = fmaf(pT, tco, g1);
-                                g1 = fmaf(q, k.qc, g1);
+                                g1 = fmaf(q, h.qc, g1);
                             }
                             g1 -= k.bc;
                             if (CAP) g1 *= om1;
-                            reinterpret_cast<uint16_t*>(gg)[r * V + c0 + int64_t(w) * EPW + iy] =
+                            reinterpret_cast<uint16_t*>(grow)[int64_t(w) * EPW + iy] =
                                 P16::from_f(g1);
                         }
                     }
                 };
-                if (CAP && !row_exp) grad(BoolC<true>{});
-                else grad(BoolC<false>{});
+                const int tier = !CAP ? 0 : c < 32 ? int((tiers >> (2 * c)) & 3u) : tier_hi;
+                if (tier == 0) grad(IntC<0>{});
+                else if (tier == 1) grad(IntC<1>{});
+                else grad(IntC<2>{});
             }
-            release(J);
+            release(r, K2x - 1 - c);
         }
     }
 

@@ -133,21 +133,73 @@ def make_inputs(wl: Workload, device="cuda", rows: Optional[int] = None,
 
     old = adv = None
     if wl.has_grpo:
-        nblk = (N + wl.adv_block - 1) // wl.adv_block
-        adv = torch.randn((nblk,), generator=g_adv, device=device, dtype=torch.float32)
-        adv = adv.repeat_interleave(wl.adv_block)[:N].contiguous()
-        old = torch.empty((N,), dtype=torch.float32, device=device)
-        noise = torch.randn((N,), generator=g_old, device=device, dtype=torch.float32)
-        for r0 in range(0, N, chunk_rows):
-            r1 = min(N, r0 + chunk_rows)
-            z = logits[r0:r1].float()
-            if wl.softcap > 0:
-                z = torch.tanh(z / wl.softcap) * wl.softcap
-            z = z * wl.logits_scale
-            lp = torch.log_softmax(z, dim=-1)
-            lab = labels[r0:r1]
-            picked = lp.gather(1, lab.clamp(min=0)[:, None])[:, 0]
-            old[r0:r1] = torch.where(lab >= 0, picked + wl.old_noise * noise[r0:r1],
-                                     torch.zeros_like(picked))
-            del z, lp
+        old, adv = _grpo_side(wl, logits, labels, g_old, g_adv, chunk_rows)
+    return dict(logits=logits, labels=labels, teacher=teacher, old_logprobs=old, advantages=adv)
+
+
+def _grpo_side(wl, logits, labels, g_old, g_adv, chunk_rows=2048):
+    """Per-sequence advantages and old log-probs near the current label
+    log-probs (torch's log_softmax of the transformed logits, plus noise)."""
+    N = logits.shape[0]
+    device = logits.device
+    nblk = (N + wl.adv_block - 1) // wl.adv_block
+    adv = torch.randn((nblk,), generator=g_adv, device=device, dtype=torch.float32)
+    adv = adv.repeat_interleave(wl.adv_block)[:N].contiguous()
+    old = torch.empty((N,), dtype=torch.float32, device=device)
+    noise = torch.randn((N,), generator=g_old, device=device, dtype=torch.float32)
+    for r0 in range(0, N, chunk_rows):
+        r1 = min(N, r0 + chunk_rows)
+        z = logits[r0:r1].float()
+        if wl.softcap > 0:
+            z = torch.tanh(z / wl.softcap) * wl.softcap
+        z = z * wl.logits_scale
+        lp = torch.log_softmax(z, dim=-1)
+        lab = labels[r0:r1]
+        picked = lp.gather(1, lab.clamp(min=0)[:, None])[:, 0]
+        old[r0:r1] = torch.where(lab >= 0, picked + wl.old_noise * noise[r0:r1],
+                                 torch.zeros_like(picked))
+        del z, lp
+    return old, adv
+
+
+def make_structured_inputs(wl: Workload, device="cuda") -> dict:
+    """Rows whose shape stresses the online statistics (small cases only).
+
+    Row r takes pattern r % 6 on top of N(0, sigma^2) noise, for the student
+    and (with its own pattern) the teacher: 0 an ascending ramp -20 -> +40
+    along the row (the maximum comes last), 1 the descending ramp, 2 a +300
+    offset, 3 one spike of +60 at a random column, 4 the noise alone, 5 the
+    noise scaled by 8.  Labels, mask and GRPO side inputs as in make_inputs."""
+    device = torch.device(device)
+    N, V = wl.N, wl.V
+    g_x, g_lab, g_mask = _gen(device, wl.seed, 0), _gen(device, wl.seed, 1), _gen(device, wl.seed, 2)
+    g_t, g_old, g_adv = _gen(device, wl.seed, 3), _gen(device, wl.seed, 4), _gen(device, wl.seed, 5)
+    g_pos = _gen(device, wl.seed, 6)
+    j = torch.arange(V, device=device, dtype=torch.float32) / max(V - 1, 1)
+    kind = torch.arange(N, device=device) % 6
+    spike = torch.randint(0, V, (N,), generator=g_pos, device=device)
+
+    def shaped(base, flip):
+        out = base.clone()
+        ramp = -20.0 + 60.0 * (1.0 - j if flip else j)
+        out[kind == 0] += ramp
+        out[kind == 1] += -20.0 + 60.0 * (j if flip else 1.0 - j)
+        out[kind == 2] += 300.0
+        rows = torch.nonzero(kind == 3)[:, 0]
+        out[rows, spike[rows]] += 60.0
+        out[kind == 5] *= 8.0
+        return out
+
+    xf = torch.randn((N, V), generator=g_x, device=device, dtype=torch.float32) * wl.sigma
+    logits = shaped(xf, False).to(wl.dtype)
+    teacher = None
+    if wl.has_teacher:
+        tf = torch.randn((N, V), generator=g_t, device=device, dtype=torch.float32)
+        teacher = shaped(tf * wl.teacher_noise + xf, True).to(wl.dtype)
+    labels = torch.randint(0, V, (N,), generator=g_lab, device=device, dtype=torch.int64)
+    mask = torch.rand((N,), generator=g_mask, device=device) < wl.mask_frac
+    labels[mask] = -100
+    old = adv = None
+    if wl.has_grpo:
+        old, adv = _grpo_side(wl, logits, labels, g_old, g_adv)
     return dict(logits=logits, labels=labels, teacher=teacher, old_logprobs=old, advantages=adv)

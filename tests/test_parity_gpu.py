@@ -100,6 +100,45 @@ def test_forced_stream_plans(stages, threads, words, V):
     full_check(small(("dist_ce", "fkl", "rkl", "entropy"), N=23, V=V, sigma=6.0), plan=plan)
 
 
+def structured_check(wl, plan=None):
+    inp = W.make_structured_inputs(wl, "cuda")
+    got, g, _ = H.run_gpu(wl, inp, plan=plan)
+    cfg, rec, ref, gmag = H.oracle_rows(wl, inp)
+    H.check_scalars(wl, got, cfg, rec)
+    H.check_grad(wl, g, ref, gmag, rec)
+
+
+# rows whose maximum comes last, first or as one spike, large offsets and
+# wide ranges: the streaming kernel's lazily raised shifts and its per-chunk
+# softcap tiers (35 chunks per row at V = 70000, beyond the 32 it records one
+# by one), with and without the entropy gradient and the teacher-entropy sum
+@pytest.mark.parametrize("softcap,scale", [(0.0, 0.7), (30.0, 0.5), (10.0, 1.0), (60.0, 1.0)])
+@pytest.mark.parametrize("V", [4104, 70000])
+def test_stream_structured_rows(softcap, scale, V):
+    plan = dict(kernel=STREAM, stages=3, threads=256, chunk_words=1)
+    for losses, ent in ((ALL_LOSSES, 0.5), (("ce", "z", "fkl", "grpo", "grpo_stats", "entropy"), 0.0),
+                        (("dist_ce", "rkl", "entropy"), 0.0)):
+        wl = small(losses, N=24, V=V, softcap=softcap, logits_scale=scale,
+                   weights=dict(FULL_W, entropy=ent))
+        structured_check(wl, plan=plan)
+
+
+@pytest.mark.parametrize("softcap,scale", [(0.0, 1.0), (30.0, 0.5), (15.0, 1.3)])
+def test_stream_structured_rows_default_plan(softcap, scale):
+    wl = small(ALL_LOSSES, N=40, V=128256, softcap=softcap, logits_scale=scale,
+               weights=dict(FULL_W, entropy=0.0))
+    structured_check(wl)
+
+
+@pytest.mark.parametrize("softcap,scale", [(0.0, 0.7), (10.0, 1.0), (30.0, 0.5)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+def test_resident_structured_rows(softcap, scale, dtype):
+    for plan in (dict(kernel=RESIDENT, cluster=2, stages=2, threads=256),
+                 dict(kernel=RESIDENT, cluster=1, stages=1, threads=512)):
+        wl = small(ALL_LOSSES, N=24, V=4100, dtype=dtype, softcap=softcap, logits_scale=scale)
+        structured_check(wl, plan=plan)
+
+
 def test_stream_every_loss_subset():
     plan = dict(kernel=STREAM, stages=4, threads=256, chunk_words=1)
     for losses in SUBSETS:
