@@ -331,16 +331,18 @@ bool pick_resident(const headloss* h, const Plan* cand, int ncand, Plan* best) {
 }
 
 // Streaming rule (measured on GB300): the per-chunk bookkeeping (slot wait,
-// running-shift update, release) is amortised over the chunk, so the largest
-// chunk per thread wins; then 512 threads; then fewer slots (two already hide
-// the copy latency).
+// shift check, release) is amortised over the chunk, so the largest chunk per
+// thread wins; then the most co-resident CTAs (two CTAs of 256 threads beat
+// one of 512: one CTA's row merge and barriers hide behind the other's
+// arithmetic); then the most slots that still keep them co-resident (a
+// deeper ring rides out DRAM latency: three slots beat two by ~1%).
 bool pick_stream(const headloss* h, const Plan* cand, int ncand, Plan* best) {
     Plan b;
     double bscore = -1.0;
     for (int i = 0; i < ncand; ++i) {
         const Plan& c = cand[i];
         if (c.kind != HEADLOSS_KERNEL_STREAM) continue;
-        const double score = c.chunk_words * 1e6 + c.threads * 1e2 - c.nbuf;
+        const double score = c.chunk_words * 1e6 + double(c.ncl) * 1e2 + c.nbuf;
         if (score > bscore) {
             b = c;
             bscore = score;

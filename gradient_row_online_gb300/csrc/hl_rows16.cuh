@@ -94,12 +94,37 @@ __device__ __forceinline__ ShiftCoef shift_coefs(const RowCoef& k, bool entg) {
     return o;
 }
 
+// One row's loss values (natural-log units), added to the CTA's fp64 sums by
+// row_accumulate.
+struct RowLoss {
+    float ce, lse, dce, fkl, rkl, grpo, lp, rho, kl3, adv, clipped, H;
+};
+__device__ __forceinline__ void row_accumulate(uint32_t f, const RowLoss& rl, double* acc) {
+    acc[A_NVALID] += 1.0;
+    if (f & L_CE) acc[A_CE] += double(rl.ce);
+    if (f & L_Z) acc[A_Z] += double(rl.lse) * double(rl.lse);
+    if (f & L_DIST_CE) acc[A_DCE] += double(rl.dce);
+    if (f & L_FKL) acc[A_FKL] += double(rl.fkl);
+    if (f & L_RKL) acc[A_RKL] += double(rl.rkl);
+    if (f & L_GRPO) acc[A_GRPO] += double(rl.grpo);
+    if (f & L_GRPO_STATS) {
+        acc[A_LP] += double(rl.lp);
+        acc[A_RATIO] += double(rl.rho);
+        acc[A_KL3] += double(rl.kl3);
+        acc[A_ADV] += double(rl.adv);
+        acc[A_ADV2] += double(rl.adv) * double(rl.adv);
+        acc[A_NCLIP] += double(rl.clipped);
+    }
+    if (f & L_ENTROPY) acc[A_ENT] += double(rl.H);
+}
+
 // A warp merges the C records of a row (lane k holds record k) and derives
 // the row's gradient coefficients (identical in every lane); with
 // `accumulate` its lane 0 also adds the row's losses to the CTA's partial sums.
 template <bool TEACH, bool RKL, bool ENT, bool CAP>
 __device__ RowCoef row_epilogue16(const Params& p, const float* recs, int C, bool accumulate,
-                                  float old_lp, float adv, double* acc, int lane) {
+                                  float old_lp, float adv, double* acc, int lane,
+                                  RowLoss* defer = nullptr) {
     const float LN2 = 0.6931471805599453f;
     const float invT = 1.f / p.T;
     float r[NREC];
@@ -220,23 +245,22 @@ __device__ RowCoef row_epilogue16(const Params& p, const float* recs, int C, boo
     k.ts = ts;
     k.qc = qc;
     k.bc = bc;
-    if (accumulate && lane == 0) {
-        acc[A_NVALID] += 1.0;
-        if (f & L_CE) acc[A_CE] += double((lse2 - zy) * LN2);
-        if (f & L_Z) acc[A_Z] += double(lse) * double(lse);
-        if (f & L_DIST_CE) acc[A_DCE] += double(dce);
-        if (f & L_FKL) acc[A_FKL] += double(fkl);
-        if (f & L_RKL) acc[A_RKL] += double(rkl);
-        if (f & L_GRPO) acc[A_GRPO] += double(grpo);
-        if (f & L_GRPO_STATS) {
-            acc[A_LP] += double(lp);
-            acc[A_RATIO] += double(rho);
-            acc[A_KL3] += double(kl3);
-            acc[A_ADV] += double(adv);
-            acc[A_ADV2] += double(adv) * double(adv);
-            acc[A_NCLIP] += clipped ? 1.0 : 0.0;
-        }
-        if (f & L_ENTROPY) acc[A_ENT] += double(H);
+    if (lane == 0 && (accumulate || defer != nullptr)) {
+        RowLoss rl;
+        rl.ce = (lse2 - zy) * LN2;
+        rl.lse = lse;
+        rl.dce = dce;
+        rl.fkl = fkl;
+        rl.rkl = rkl;
+        rl.grpo = grpo;
+        rl.lp = lp;
+        rl.rho = rho;
+        rl.kl3 = kl3;
+        rl.adv = adv;
+        rl.clipped = clipped ? 1.f : 0.f;
+        rl.H = H;
+        if (defer != nullptr) *defer = rl;
+        else row_accumulate(f, rl, acc);
     }
     return k;
 }

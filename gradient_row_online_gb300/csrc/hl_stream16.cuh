@@ -37,64 +37,18 @@
 
 namespace hl {
 
-// Thread-local partial statistics of a row (the resident kernel's record in
-// registers): shifts zm (student, base 2) and um (teacher), and the sums.
-struct TRec {
-    float zm, um, S, E, ST, Sq, Eq, Xp, Y, zy, hasy;
-};
-
-// Merges b into a (commutative: a + b and b + a give identical results).
-template <bool TEACH, bool RKL, bool ENT, bool DCE>
-__device__ __forceinline__ void trec_merge(TRec& a, const TRec& b, float invT) {
-    const bool la = a.S > 0.f, lb = b.S > 0.f;
-    const float M = fmaxf(la ? a.zm : -CUDART_INF_F, lb ? b.zm : -CUDART_INF_F);
-    const float da = la ? a.zm - M : 0.f, db = lb ? b.zm - M : 0.f;
-    const float aa = la ? exp2f(da) : 0.f, ab = lb ? exp2f(db) : 0.f;
-    TRec o;
-    o.zm = (la || lb) ? M : a.zm;
-    o.S = aa * a.S + ab * b.S;
-    o.E = ENT ? aa * (a.E + da * a.S) + ab * (b.E + db * b.S) : 0.f;
-    o.zy = a.zy + b.zy;
-    o.hasy = a.hasy + b.hasy;
-    if (TEACH) {
-        const float Mu = fmaxf(la ? a.um : -CUDART_INF_F, lb ? b.um : -CUDART_INF_F);
-        const float dua = la ? a.um - Mu : 0.f, dub = lb ? b.um - Mu : 0.f;
-        const float ba = la ? exp2f(dua) : 0.f, bb = lb ? exp2f(dub) : 0.f;
-        const float dTa = da * invT, dTb = db * invT;
-        const float ta = la ? exp2f(dTa) : 0.f, tb = lb ? exp2f(dTb) : 0.f;
-        o.um = (la || lb) ? Mu : a.um;
-        o.ST = ta * a.ST + tb * b.ST;
-        o.Sq = ba * a.Sq + bb * b.Sq;
-        o.Eq = DCE ? ba * (a.Eq + dua * a.Sq) + bb * (b.Eq + dub * b.Sq) : 0.f;
-        o.Xp = ba * (a.Xp + (dua - dTa) * a.Sq) + bb * (b.Xp + (dub - dTb) * b.Sq);
-        o.Y = RKL ? ta * (a.Y - (dua - dTa) * a.ST) + tb * (b.Y - (dub - dTb) * b.ST) : 0.f;
-    } else {
-        o.um = a.um;
-        o.ST = o.Sq = o.Eq = o.Xp = o.Y = 0.f;
-    }
-    a = o;
-}
-
-__device__ __forceinline__ TRec trec_shfl_xor(const TRec& a, int o) {
-    TRec b;
-    b.zm = __shfl_xor_sync(0xffffffffu, a.zm, o);
-    b.um = __shfl_xor_sync(0xffffffffu, a.um, o);
-    b.S = __shfl_xor_sync(0xffffffffu, a.S, o);
-    b.E = __shfl_xor_sync(0xffffffffu, a.E, o);
-    b.ST = __shfl_xor_sync(0xffffffffu, a.ST, o);
-    b.Sq = __shfl_xor_sync(0xffffffffu, a.Sq, o);
-    b.Eq = __shfl_xor_sync(0xffffffffu, a.Eq, o);
-    b.Xp = __shfl_xor_sync(0xffffffffu, a.Xp, o);
-    b.Y = __shfl_xor_sync(0xffffffffu, a.Y, o);
-    b.zy = __shfl_xor_sync(0xffffffffu, a.zy, o);
-    b.hasy = __shfl_xor_sync(0xffffffffu, a.hasy, o);
-    return b;
-}
-
 template <int I>
 struct IntC {
     static constexpr int value = I;
 };
+
+// Maximum of v over the warp, in every lane (order-preserving integer key).
+__device__ __forceinline__ float warp_max_f(float v) {
+    int k = __float_as_int(v);
+    k = k >= 0 ? k : k ^ 0x7fffffff;
+    k = __reduce_max_sync(0xffffffffu, k);
+    return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff);
+}
 
 // Largest rise (base-2 units) of a value above its running shift before the
 // sums are rescaled: terms stay below 2^TAU, far from fp32 overflow.
@@ -127,7 +81,6 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
     float* redmax = red + NWARPS * NREC;
     float* coefs = redmax + 2 * NWARPS;
     int* done = reinterpret_cast<int*>(coefs + 16);     // [MAX_STAGES] warps finished per slot
-    (void)red;
 
     const int64_t N = p.N, V = p.V;
     const int K = int((V + CH - 1) / CH);                // chunks per row
@@ -155,7 +108,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
     const float XA = (CAP && Kc <= 48.f) ? HL_TANH_A_Y0 * p.softcap : 0.f;
     const float XB = CAP ? HL_TANH_B_Y0 * p.softcap : 0.f;
     // zs = x * Q(x^2): Q_k = s * log2e * C_k / c^(2k), formed in double
-    f2 QA[4], QB[6];
+    f2 QA[4], QB[6];  // QB: staged in shared memory below (rarely needed)
     {
         const double ic2 = CAP ? 1.0 / (double(p.softcap) * double(p.softcap)) : 0.0;
         const double ca[4] = {HL_TANH_A_C0, HL_TANH_A_C1, HL_TANH_A_C2, HL_TANH_A_C3};
@@ -178,7 +131,15 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         return CAP ? __fmul_rn(tanh_a2x_1(__fmul_rn(v, A2)), Kc) : __fmul_rn(v, K1);
     };
     // zs + nshift of a pair (pass 1), by tier
-    auto shifted = [&](f2 xv, f2 nshift, auto tierc) -> f2 {
+    // the wide-tier and exp-tier constants live in shared memory (the `red`
+    // area, unused here) and are read where those tiers run, so the common
+    // tier keeps their registers free
+    f2* rare = reinterpret_cast<f2*>(red);  // QB[0..5], A22, Kc2
+    auto load_rare = [&](f2* cst) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cst[i] = rare[i];
+    };
+    auto shifted = [&](f2 xv, f2 nshift, auto tierc, const f2* cst) -> f2 {
         constexpr int TI = CAP ? decltype(tierc)::value : -1;
         if constexpr (TI < 0) {
             return fma2(xv, K2, nshift);
@@ -190,18 +151,18 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             return fma2(xv, q, nshift);
         } else if constexpr (TI == 1) {
             const f2 u = mul2(xv, xv);
-            f2 q = fma2(u, QB[5], QB[4]);
-            q = fma2(q, u, QB[3]);
-            q = fma2(q, u, QB[2]);
-            q = fma2(q, u, QB[1]);
-            q = fma2(q, u, QB[0]);
+            f2 q = fma2(u, cst[5], cst[4]);
+            q = fma2(q, u, cst[3]);
+            q = fma2(q, u, cst[2]);
+            q = fma2(q, u, cst[1]);
+            q = fma2(q, u, cst[0]);
             return fma2(xv, q, nshift);
         } else {
-            return fma2(tanh_from_ex2_arg(mul2(xv, A22)).th, Kc2, nshift);
+            return fma2(tanh_from_ex2_arg(mul2(xv, cst[6])).th, cst[7], nshift);
         }
     };
     // zs and 1 - tanh^2 of a pair (pass 2, softcap), by tier
-    auto zs_omt = [&](f2 xv, f2& zs, f2& omt, auto tierc) {
+    auto zs_omt = [&](f2 xv, f2& zs, f2& omt, auto tierc, const f2* cst) {
         constexpr int TI = decltype(tierc)::value;
         if constexpr (TI == 0 || TI == 1) {
             const f2 u = mul2(xv, xv);
@@ -211,17 +172,17 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                 q = fma2(q, u, QA[1]);
                 q = fma2(q, u, QA[0]);
             } else {
-                q = fma2(u, QB[5], QB[4]);
-                q = fma2(q, u, QB[3]);
-                q = fma2(q, u, QB[2]);
-                q = fma2(q, u, QB[1]);
-                q = fma2(q, u, QB[0]);
+                q = fma2(u, cst[5], cst[4]);
+                q = fma2(q, u, cst[3]);
+                q = fma2(q, u, cst[2]);
+                q = fma2(q, u, cst[1]);
+                q = fma2(q, u, cst[0]);
             }
             zs = mul2(xv, q);
             omt = fma2(zs, mul2(zs, m2), one2);  // 1 - (zs / Kc)^2; |tanh| <= 0.67 here
         } else {
-            const TanhD2 td = tanh_from_ex2_arg(mul2(xv, A22));
-            zs = mul2(td.th, Kc2);
+            const TanhD2 td = tanh_from_ex2_arg(mul2(xv, cst[6]));
+            zs = mul2(td.th, cst[7]);
             omt = td.omt;
         }
     };
@@ -260,6 +221,10 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         }
         fence_mbar_init();
         for (int i = 0; i < NACC; ++i) acc[i] = 0.0;
+#pragma unroll
+        for (int i = 0; i < 6; ++i) rare[i] = QB[i];
+        rare[6] = A22;
+        rare[7] = Kc2;
     }
     __syncthreads();
     if (tid == 0) {
@@ -332,6 +297,14 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             continue;
         }
 
+        // the label column: its chunk, its offset there, and whether this
+        // thread's words of that chunk hold it
+        const int yc = has_labels ? int(y / CH) : -1;
+        const int yin = has_labels ? int(y - int64_t(yc) * CH) : 0;
+        const int ywd = yin / EPW;
+        const bool yown = has_labels && ywd >= tid && (ywd - tid) % nthr == 0 &&
+                          (ywd - tid) / nthr < WPT;
+
         // ---------------- pass 1: online statistics ----------------
         float zm = fixed_shift ? Kc : -CUDART_INF_F, um = -CUDART_INF_F;
         f2 S2 = z2, E2 = z2, ST2 = z2, Sq2 = z2, Eq2 = z2, Xp2 = z2, Y2 = z2;
@@ -382,26 +355,33 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             if (need_sx) maxima(BoolC<true>{});
             else maxima(BoolC<false>{});
             float ca, cb;
-            // lazy shifts: raise a shift only when the chunk's max exceeds it by TAU
+            // lazy, warp-uniform shifts: raise a shift only when the warp's
+            // chunk maximum exceeds it by TAU
             float nz = zm, nu = um;
             bool mv = false;
-            if (need_sx && nmine) {
+            if (need_sx) {
                 upk(P16::unpack(ms), ca, cb);
-                const float bz = zs1(fmaxf(ca, cb));
-                if (bz > zm + STREAM_TAU) {
-                    nz = bz;
-                    mv = true;
+                const float wmx = warp_max_f(nmine ? fmaxf(ca, cb) : -CUDART_INF_F);
+                if (wmx > -CUDART_INF_F) {
+                    const float bz = zs1(wmx);
+                    if (bz > zm + STREAM_TAU) {
+                        nz = bz;
+                        mv = true;
+                    }
                 }
             }
-            if (TEACH && nmine) {
+            if (TEACH) {
                 upk(P16::unpack(mt), ca, cb);
-                const float bu = __fmul_rn(fmaxf(ca, cb), KT);
-                if (bu > um + STREAM_TAU) {
-                    nu = bu;
-                    mv = true;
+                const float wmt = warp_max_f(nmine ? fmaxf(ca, cb) : -CUDART_INF_F);
+                if (wmt > -CUDART_INF_F) {
+                    const float bu = __fmul_rn(wmt, KT);
+                    if (bu > um + STREAM_TAU) {
+                        nu = bu;
+                        mv = true;
+                    }
                 }
             }
-            if (__any_sync(0xffffffffu, mv)) {
+            if (mv) {  // warp-uniform
                 const float d = (zm == -CUDART_INF_F) ? 0.f : zm - nz;
                 const float du = (um == -CUDART_INF_F) ? 0.f : um - nu;
                 const float al = exp2f(d), dTv = d * invT;
@@ -433,6 +413,8 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             }
             const f2 nzm2 = pk1(-zm), num2 = pk1(-um);
             auto sums = [&](auto tierc) {
+                f2 cst[8];
+                if constexpr (CAP && decltype(tierc)::value > 0) load_rare(cst);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     if (i >= nmine) continue;
@@ -440,7 +422,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                     const uint32_t tb[4] = {tw[i].x, tw[i].y, tw[i].z, tw[i].w};
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const f2 d = shifted(P16::unpack(xa[kk]), nzm2, tierc);
+                        const f2 d = shifted(P16::unpack(xa[kk]), nzm2, tierc, cst);
                         const f2 e = ex2p(d);
                         S2 = add2(S2, e);
                         if (ENT) E2 = fma2(e, d, E2);
@@ -463,45 +445,40 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             else if (tier == 1) sums(IntC<1>{});
             else sums(IntC<2>{});
             // the label column's logit, from the thread that holds it
-            if (has_labels && y >= c0 && y < c0 + int64_t(nwc) * EPW) {
-                const int wl = int((y - c0) / EPW);
-                if ((wl - tid) % nthr == 0 && wl >= tid) {
-                    zy = zs1(P16::to_f(reinterpret_cast<const uint16_t*>(sb)[y - c0]));
-                    hasy = 1.f;
-                }
+            if (c == yc && yown) {
+                zy = zs1(P16::to_f(reinterpret_cast<const uint16_t*>(sb)[yin]));
+                hasy = 1.f;
             }
             release(r, c);
         }
 
         // ---------------- merge: threads -> warps -> row ----------------
-        TRec tr;
-        tr.zm = zm;
-        tr.um = um;
-        tr.S = hsum(S2);
-        tr.E = hsum(E2);
-        tr.ST = hsum(ST2);
-        tr.Sq = hsum(Sq2);
-        tr.Eq = hsum(Eq2);
-        tr.Xp = hsum(Xp2);
-        tr.Y = -hsum(Y2);
-        tr.zy = zy;
-        tr.hasy = hasy;
+        // the shifts are warp-uniform, so a warp's record is a plain sum
+        float v[9] = {hsum(S2), hsum(E2), hsum(ST2), hsum(Sq2), hsum(Eq2), hsum(Xp2),
+                      -hsum(Y2), zy, hasy};
 #pragma unroll
         for (int o = 16; o; o >>= 1)
-            trec_merge<TEACH, RKL, ENT, DCE>(tr, trec_shfl_xor(tr, o), invT);
+#pragma unroll
+            for (int i = 0; i < 9; ++i) {
+                if (i == 1 && !ENT) continue;
+                if ((i >= 2 && i <= 5) && !TEACH) continue;
+                if (i == 4 && !DCE) continue;
+                if (i == 6 && !RKL) continue;
+                v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+            }
         if (lane == 0) {
             float* rec = xch + warp * NREC;
-            rec[R_ZM] = tr.zm;
-            rec[R_UM] = tr.um;
-            rec[R_S] = tr.S;
-            rec[R_E] = tr.E;
-            rec[R_ST] = tr.ST;
-            rec[R_SQ] = tr.Sq;
-            rec[R_EQ] = tr.Eq;
-            rec[R_XP] = tr.Xp;
-            rec[R_Y] = tr.Y;
-            rec[R_ZY] = tr.zy;
-            rec[R_HASY] = tr.hasy;
+            rec[R_ZM] = zm;
+            rec[R_UM] = um;
+            rec[R_S] = v[0];
+            rec[R_E] = ENT ? v[1] : 0.f;
+            rec[R_ST] = TEACH ? v[2] : 0.f;
+            rec[R_SQ] = TEACH ? v[3] : 0.f;
+            rec[R_EQ] = DCE ? v[4] : 0.f;
+            rec[R_XP] = TEACH ? v[5] : 0.f;
+            rec[R_Y] = RKL ? v[6] : 0.f;
+            rec[R_ZY] = v[7];
+            rec[R_HASY] = v[8];
         }
         __syncthreads();
         if (warp == 0) {
@@ -526,11 +503,10 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             if (gg != nullptr) {
                 const int64_t c0 = int64_t(c) * CH;
                 const int nwc = int(((V - c0) < CH ? (V - c0) : CH) / EPW);
-                const int64_t wy = (has_labels && y >= c0 && y < c0 + int64_t(nwc) * EPW)
-                                       ? (y - c0) / EPW : -1;
-                const int iy = int((y - c0) % EPW);
                 DT* grow = gg + r * V + c0;
                 auto grad = [&](auto tierc) {
+                    f2 cst[8];
+                    if constexpr (CAP && decltype(tierc)::value > 0) load_rare(cst);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int w = tid + i * nthr;
@@ -546,7 +522,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                             const f2 xv = P16::unpack(xa[kk]);
                             f2 zs = z2, omt = z2, arg, argT = z2;
                             if constexpr (CAP) {
-                                zs_omt(xv, zs, omt, tierc);
+                                zs_omt(xv, zs, omt, tierc, cst);
                                 arg = add2(zs, nlse2);
                                 if (TEACH) argT = fma2(zs, invT2, nlseT2);
                             } else {
@@ -573,42 +549,45 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                         }
                         *reinterpret_cast<uint4*>(grow + int64_t(w) * EPW) =
                             make_uint4(out[0], out[1], out[2], out[3]);
-                        if (w == wy) {
-                            // the label column: this thread recomputes that one element
-                            // with the label term and overwrites it (program order keeps
-                            // the later store)
-                            const uint16_t* xs16 = reinterpret_cast<const uint16_t*>(sb);
-                            const float xv1 = P16::to_f(xs16[w * EPW + iy]);
-                            float zs, om1 = 1.f;
-                            if (CAP) zs = __fmul_rn(tanh_a2x_1(__fmul_rn(xv1, A2), &om1), Kc);
-                            else zs = __fmul_rn(xv1, K1);
-                            const float arg = zs + h.nlse;
-                            float g1 = ex2f(arg) * (ENTG ? fmaf(h.ps, arg, h.pc) : h.pc);
-                            if (TEACH) {
-                                const float tv1 = P16::to_f(
-                                    reinterpret_cast<const uint16_t*>(sb + opbytes)[w * EPW + iy]);
-                                const float pT = ex2f(fmaf(zs, invT, h.nlseT));
-                                const float q = ex2f(fmaf(tv1, KT, h.nlsq));
-                                float tco = h.tc;
-                                if (RKL) {
-                                    const float dxu = CAP ? fmaf(tv1, -LOG2E, zs) * invT
-                                                          : fmaf(xv1, s, -tv1) * KT;
-                                    tco = fmaf(h.ts, dxu - dlse, h.tc);
-                                }
-                                g1 = fmaf(pT, tco, g1);
-                                g1 = fmaf(q, h.qc, g1);
-                            }
-                            g1 -= k.bc;
-                            if (CAP) g1 *= om1;
-                            reinterpret_cast<uint16_t*>(grow)[int64_t(w) * EPW + iy] =
-                                P16::from_f(g1);
-                        }
                     }
                 };
                 const int tier = !CAP ? 0 : c < 32 ? int((tiers >> (2 * c)) & 3u) : tier_hi;
                 if (tier == 0) grad(IntC<0>{});
                 else if (tier == 1) grad(IntC<1>{});
                 else grad(IntC<2>{});
+                // the label column: the thread whose word holds it recomputes that
+                // one element with the label term and overwrites it (program order
+                // keeps the later store)
+                if (c == yc && yown) {
+                    const int w = ywd;
+                    const int iy = yin - ywd * EPW;
+                    const uint16_t* xs16 = reinterpret_cast<const uint16_t*>(sb);
+                    const float xv1 = P16::to_f(xs16[w * EPW + iy]);
+                    float zs, om1 = 1.f;
+                    if (CAP) zs = __fmul_rn(tanh_a2x_1(__fmul_rn(xv1, A2), &om1), Kc);
+                    else zs = __fmul_rn(xv1, K1);
+                    // (the scalars are read back from the packed constants)
+                    const float arg = zs + lo_of(nlse2);
+                    float g1 = ex2f(arg) * (ENTG ? fmaf(lo_of(ps2), arg, lo_of(pc2)) : lo_of(pc2));
+                    if (TEACH) {
+                        const float tv1 = P16::to_f(
+                            reinterpret_cast<const uint16_t*>(sb + opbytes)[w * EPW + iy]);
+                        const float pT = ex2f(fmaf(zs, lo_of(invT2), lo_of(nlseT2)));
+                        const float q = ex2f(fmaf(tv1, lo_of(KT2), lo_of(nlsq2)));
+                        float tco = lo_of(tc2);
+                        if (RKL) {
+                            const float dxu = CAP ? fmaf(tv1, -LOG2E, zs) * lo_of(invT2)
+                                                  : fmaf(xv1, s, -tv1) * lo_of(KT2);
+                            tco = fmaf(lo_of(ts2), dxu + lo_of(ndlse2), lo_of(tc2));
+                        }
+                        g1 = fmaf(pT, tco, g1);
+                        g1 = fmaf(q, lo_of(qc2), g1);
+                    }
+                    g1 -= k.bc;
+                    if (CAP) g1 *= om1;
+                    reinterpret_cast<uint16_t*>(grow)[int64_t(w) * EPW + iy] =
+                        P16::from_f(g1);
+                }
             }
             release(r, K2x - 1 - c);
         }
