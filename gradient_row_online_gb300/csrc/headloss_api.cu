@@ -18,6 +18,10 @@ const void* rows_kernel_fp16(int feat);
 const void* rows_kernel_fp32(int feat);
 const void* stream_kernel_bf16(int feat);
 const void* stream_kernel_fp16(int feat);
+const void* rows_kernel_bf16_acc(int feat);
+const void* rows_kernel_fp16_acc(int feat);
+const void* stream_kernel_bf16_acc(int feat);
+const void* stream_kernel_fp16_acc(int feat);
 
 // Valid rows of the call (0 <= label < V); a label >= V raises E_LABEL.
 // One block: the count is an exact integer whatever the order.
@@ -49,10 +53,12 @@ __global__ void __launch_bounds__(1024) count_valid_kernel(const int64_t* labels
 struct FinalizeArgs {
     uint32_t flags;
     float w_ce, w_z, w_dce, w_fkl, w_rkl, w_grpo, w_ent;
+    double divisor;  // > 0: normaliser of the loss slots (a split batch)
 };
 
 // Sums the per-cluster partials in cluster order (fp64) and writes the
-// sixteen scalars (means over valid rows; unselected slots 0).
+// sixteen scalars (means over valid rows, or loss sums over the caller's
+// divisor; unselected slots 0).
 __global__ void finalize_kernel(const double* partials, int nclusters, const long long* n_valid,
                                 FinalizeArgs a, float* out) {
     __shared__ double tot[NACC];
@@ -67,15 +73,16 @@ __global__ void finalize_kernel(const double* partials, int nclusters, const lon
     double o[16];
     for (int i = 0; i < 16; ++i) o[i] = 0.0;
     const double n = double(*n_valid);
+    const double nl = a.divisor > 0.0 ? a.divisor : n;  // loss slots
     o[HEADLOSS_SLOT_N_VALID] = n;
     if (n > 0.0) {
         const uint32_t f = a.flags;
-        if (f & L_CE) o[HEADLOSS_SLOT_CE] = tot[A_CE] / n;
-        if (f & L_Z) o[HEADLOSS_SLOT_Z] = tot[A_Z] / n;
-        if (f & L_DIST_CE) o[HEADLOSS_SLOT_DIST_CE] = tot[A_DCE] / n;
-        if (f & L_FKL) o[HEADLOSS_SLOT_FKL] = tot[A_FKL] / n;
-        if (f & L_RKL) o[HEADLOSS_SLOT_RKL] = tot[A_RKL] / n;
-        if (f & L_GRPO) o[HEADLOSS_SLOT_GRPO] = tot[A_GRPO] / n;
+        if (f & L_CE) o[HEADLOSS_SLOT_CE] = tot[A_CE] / nl;
+        if (f & L_Z) o[HEADLOSS_SLOT_Z] = tot[A_Z] / nl;
+        if (f & L_DIST_CE) o[HEADLOSS_SLOT_DIST_CE] = tot[A_DCE] / nl;
+        if (f & L_FKL) o[HEADLOSS_SLOT_FKL] = tot[A_FKL] / nl;
+        if (f & L_RKL) o[HEADLOSS_SLOT_RKL] = tot[A_RKL] / nl;
+        if (f & L_GRPO) o[HEADLOSS_SLOT_GRPO] = tot[A_GRPO] / nl;
         if (f & L_GRPO_STATS) {
             o[HEADLOSS_SLOT_NEW_LOGPROB] = tot[A_LP] / n;
             o[HEADLOSS_SLOT_RATIO] = tot[A_RATIO] / n;
@@ -87,7 +94,7 @@ __global__ void finalize_kernel(const double* partials, int nclusters, const lon
             o[HEADLOSS_SLOT_ADV_STD] = var > 0.0 ? sqrt(var) : 0.0;
             o[HEADLOSS_SLOT_N_CLIPPED] = tot[A_NCLIP];
         }
-        if (f & L_ENTROPY) o[HEADLOSS_SLOT_ENTROPY] = tot[A_ENT] / n;
+        if (f & L_ENTROPY) o[HEADLOSS_SLOT_ENTROPY] = tot[A_ENT] / nl;
         double total = 0.0;
         if (f & L_CE) total += double(a.w_ce) * o[HEADLOSS_SLOT_CE];
         if (f & L_Z) total += double(a.w_z) * o[HEADLOSS_SLOT_Z];
@@ -153,14 +160,20 @@ int feature_set(const headloss* h) {
     return f;
 }
 
+// The kernel of `kind` for `dtype` and the feature set `feat` (F_ACC selects
+// the accumulating instantiation; the fp32 kernel reads the flag at run time).
 const void* kernel_for(int kind, int dtype, int feat) {
+    const bool acc = (feat & F_ACC) != 0;
+    feat &= ~F_ACC;
     if (kind == HEADLOSS_KERNEL_STREAM) {
         switch (dtype) {
-            case HEADLOSS_BF16: return stream_kernel_bf16(feat);
-            case HEADLOSS_FP16: return stream_kernel_fp16(feat);
+            case HEADLOSS_BF16: return acc ? stream_kernel_bf16_acc(feat) : stream_kernel_bf16(feat);
+            case HEADLOSS_FP16: return acc ? stream_kernel_fp16_acc(feat) : stream_kernel_fp16(feat);
             default: return nullptr;
         }
     }
+    if (acc && dtype == HEADLOSS_BF16) return rows_kernel_bf16_acc(feat & F_BASE);
+    if (acc && dtype == HEADLOSS_FP16) return rows_kernel_fp16_acc(feat & F_BASE);
     switch (dtype) {
         case HEADLOSS_BF16: return rows_kernel_bf16(feat & F_BASE);
         case HEADLOSS_FP16: return rows_kernel_fp16(feat & F_BASE);
@@ -362,8 +375,8 @@ bool pick_stream(const headloss* h, const Plan* cand, int ncand, Plan* best) {
 // student-only (its second read, partly from DRAM, costs more than the
 // resident kernel's barriers).  So: streaming for 16-bit rows with a teacher
 // whose resident plan needs three or more CTAs per row; resident otherwise.
-int make_plan(headloss* h, int64_t V, int dtype, Plan* out) {
-    const int feat = feature_set(h);
+int make_plan(headloss* h, int64_t V, int dtype, Plan* out, int acc = 0) {
+    const int feat = feature_set(h) | (acc ? int(F_ACC) : 0);
     if (h->plan.V == V && h->plan.dtype == dtype && h->plan.feat == feat) {
         *out = h->plan;
         return HEADLOSS_OK;
@@ -522,7 +535,25 @@ int headloss_forward_backward(headloss_t h, const void* logits, int64_t N, int64
                               const int64_t* labels, const void* teacher_logits,
                               const float* old_logprobs, const float* advantages, void* grad_out,
                               float* scalars_out, headloss_stream_t stream) {
+    return headloss_forward_backward_ext(h, logits, N, V, dtype, labels, teacher_logits,
+                                         old_logprobs, advantages, grad_out, scalars_out,
+                                         nullptr, stream);
+}
+
+int headloss_forward_backward_ext(headloss_t h, const void* logits, int64_t N, int64_t V,
+                                  int dtype, const int64_t* labels, const void* teacher_logits,
+                                  const float* old_logprobs, const float* advantages,
+                                  void* grad_out, float* scalars_out,
+                                  const headloss_call_ext* ext, headloss_stream_t stream) {
+    headloss_call_ext x = {nullptr, nullptr, 0, 0.0};
+    if (ext) x = *ext;
     if (!h || !scalars_out || N < 0 || V < 1 || V >= (int64_t(1) << 31)) return HEADLOSS_ERR_ARG;
+    if (!(x.divisor >= 0.0) || !isfinite(x.divisor)) return HEADLOSS_ERR_ARG;
+    if (x.accumulate != 0 && x.accumulate != 1) return HEADLOSS_ERR_ARG;
+    if (x.accumulate && !grad_out) return HEADLOSS_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(x.new_logprobs) & 3u) ||
+        (reinterpret_cast<uintptr_t>(x.row_loss) & 3u))
+        return HEADLOSS_ERR_ALIGN;
     if (N > 0 && !logits) return HEADLOSS_ERR_ARG;
     if (dtype < 0 || dtype > 2) return HEADLOSS_ERR_DTYPE;
     const uint32_t f = h->flags;
@@ -532,6 +563,7 @@ int headloss_forward_backward(headloss_t h, const void* logits, int64_t N, int64
             return HEADLOSS_ERR_MISSING_INPUT;
         if ((f & (L_GRPO | L_GRPO_STATS)) && (!old_logprobs || !advantages))
             return HEADLOSS_ERR_MISSING_INPUT;
+        if (x.new_logprobs && !labels) return HEADLOSS_ERR_MISSING_INPUT;
     }
     const bool teach = (f & (L_DIST_CE | L_FKL | L_RKL)) != 0;
     if (!aligned16(logits) || (teach && !aligned16(teacher_logits)) ||
@@ -543,12 +575,18 @@ int headloss_forward_backward(headloss_t h, const void* logits, int64_t N, int64
         const int64_t bytes = N * V * elem_size(dtype);
         if (g0 < t0 + bytes && t0 < g0 + bytes) return HEADLOSS_ERR_ARG;
     }
+    if (x.accumulate && N > 0) {  // accumulating into the logits themselves is refused
+        const char* g0 = static_cast<const char*>(grad_out);
+        const char* x0 = static_cast<const char*>(logits);
+        const int64_t bytes = N * V * elem_size(dtype);
+        if (g0 < x0 + bytes && x0 < g0 + bytes) return HEADLOSS_ERR_ARG;
+    }
     std::lock_guard<std::mutex> g(h->mu);
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return HEADLOSS_ERR_CUDA;
     if (dev != h->device) return HEADLOSS_ERR_ARG;
     Plan pl;
-    const int rc = make_plan(h, V, dtype, &pl);
+    const int rc = make_plan(h, V, dtype, &pl, x.accumulate);
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
@@ -588,6 +626,10 @@ int headloss_forward_backward(headloss_t h, const void* logits, int64_t N, int64
         p.err = h->err;
         p.wait_ns = h->wait_ns;
         p.drop_row = h->drop_row;
+        p.lp_out = x.new_logprobs;
+        p.rl_out = x.row_loss;
+        p.divisor = x.divisor;
+        p.accumulate = x.accumulate;
 
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
@@ -613,6 +655,7 @@ int headloss_forward_backward(headloss_t h, const void* logits, int64_t N, int64
     fa.w_rkl = h->w.rkl;
     fa.w_grpo = h->w.grpo;
     fa.w_ent = h->w.entropy;
+    fa.divisor = x.divisor;
     finalize_kernel<<<1, 32, 0, s>>>(h->partials, ncl, h->n_valid, fa, scalars_out);
     if (cudaGetLastError() != cudaSuccess) return HEADLOSS_ERR_CUDA;
     return HEADLOSS_OK;

@@ -14,6 +14,10 @@ enum : int {
     F_DCE = 16,     // teacher-entropy sum for the from-distribution CE
     F_ENTG = 32,    // entropy gradient term (entropy weight nonzero)
     F_BASE = 15,
+    // host-side only: the call adds its gradient to grad_out (selects the
+    // accumulating instantiation, which carries F_DCE / F_ENTG whenever
+    // F_TEACH / F_ENT)
+    F_ACC = 64,
 };
 
 // Loss / metric bits (values match enum headloss_flag).
@@ -62,6 +66,10 @@ struct Params {
     int* err;                      // device error word
     unsigned long long wait_ns;    // limit of every mbarrier wait (~2 s)
     int64_t drop_row;              // fault-injection builds only: row whose copy is skipped (-1: none)
+    float* lp_out;                 // N per-row log p(label) (or null)
+    float* rl_out;                 // N per-row total loss (or null)
+    double divisor;                // > 0: normaliser replacing the valid-row count
+    int accumulate;                // 1: add the gradient to grad_out's values
 };
 
 }  // namespace hl

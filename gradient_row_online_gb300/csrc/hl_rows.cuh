@@ -292,7 +292,7 @@ enum Coef { K_LSE2, K_LSET2, K_LSQ2, K_PC, K_PS, K_TC, K_TS, K_QC, K_BC, NCOEF }
 // Runs on one thread.
 template <typename A, bool TEACH, bool RKL, bool ENT, bool CAP>
 __device__ void row_epilogue(const Params& p, const A* recs, int C, bool accumulate,
-                             float old_lp, float adv, double* acc, A* coef) {
+                             float old_lp, float adv, double* acc, A* coef, int64_t row) {
     const A LN2 = A(0.6931471805599453);
     const A invT = A(1) / A(p.T);
     A M = A(-CUDART_INF), Mu = A(-CUDART_INF);
@@ -328,7 +328,7 @@ __device__ void row_epilogue(const Params& p, const A* recs, int C, bool accumul
     const A lS = lg2(S);
     const A lse2 = M + lS;
     const A lse = lse2 * LN2;
-    const double k = double(p.grad_scale) / double(*p.n_valid);
+    const double k = double(p.grad_scale) / (p.divisor > 0.0 ? p.divisor : double(*p.n_valid));
     A H = 0, lST = 0, lSq = 0, dce = 0, fkl = 0, rkl = 0;
     if (ENT) H = LN2 * (lS - E / S);
     if (TEACH) {
@@ -419,6 +419,19 @@ __device__ void row_epilogue(const Params& p, const A* recs, int C, bool accumul
             acc[A_NCLIP] += clipped ? 1.0 : 0.0;
         }
         if (f & L_ENTROPY) acc[A_ENT] += double(H);
+        // per-token outputs
+        if (p.lp_out) p.lp_out[row] = float((zy - lse2) * LN2);
+        if (p.rl_out) {
+            double t = 0.0;
+            if (f & L_CE) t += double(p.w_ce) * double((lse2 - zy) * LN2);
+            if (f & L_Z) t += double(p.w_z) * double(lse) * double(lse);
+            if (f & L_DIST_CE) t += double(p.w_dce) * double(dce);
+            if (f & L_FKL) t += double(p.w_fkl) * double(fkl);
+            if (f & L_RKL) t += double(p.w_rkl) * double(rkl);
+            if (f & L_GRPO) t += double(p.w_grpo) * double(grpo);
+            if (f & L_ENTROPY) t += double(p.w_ent) * double(H);
+            p.rl_out[row] = float(t);
+        }
     }
 }
 

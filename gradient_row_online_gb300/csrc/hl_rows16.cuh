@@ -99,6 +99,28 @@ __device__ __forceinline__ ShiftCoef shift_coefs(const RowCoef& k, bool entg) {
 struct RowLoss {
     float ce, lse, dce, fkl, rkl, grpo, lp, rho, kl3, adv, clipped, H;
 };
+// The per-token outputs of one row (valid rows; masked rows get zeros from
+// write_row_zero).
+__device__ __forceinline__ void write_row_outputs(const Params& p, int64_t row, const RowLoss& rl) {
+    const uint32_t f = p.flags;
+    if (p.lp_out) p.lp_out[row] = rl.lp;
+    if (p.rl_out) {
+        double t = 0.0;
+        if (f & L_CE) t += double(p.w_ce) * double(rl.ce);
+        if (f & L_Z) t += double(p.w_z) * double(rl.lse) * double(rl.lse);
+        if (f & L_DIST_CE) t += double(p.w_dce) * double(rl.dce);
+        if (f & L_FKL) t += double(p.w_fkl) * double(rl.fkl);
+        if (f & L_RKL) t += double(p.w_rkl) * double(rl.rkl);
+        if (f & L_GRPO) t += double(p.w_grpo) * double(rl.grpo);
+        if (f & L_ENTROPY) t += double(p.w_ent) * double(rl.H);
+        p.rl_out[row] = float(t);
+    }
+}
+__device__ __forceinline__ void write_row_zero(const Params& p, int64_t row) {
+    if (p.lp_out) p.lp_out[row] = 0.f;
+    if (p.rl_out) p.rl_out[row] = 0.f;
+}
+
 __device__ __forceinline__ void row_accumulate(uint32_t f, const RowLoss& rl, double* acc) {
     acc[A_NVALID] += 1.0;
     if (f & L_CE) acc[A_CE] += double(rl.ce);
@@ -123,8 +145,7 @@ __device__ __forceinline__ void row_accumulate(uint32_t f, const RowLoss& rl, do
 // `accumulate` its lane 0 also adds the row's losses to the CTA's partial sums.
 template <bool TEACH, bool RKL, bool ENT, bool CAP>
 __device__ RowCoef row_epilogue16(const Params& p, const float* recs, int C, bool accumulate,
-                                  float old_lp, float adv, double* acc, int lane,
-                                  RowLoss* defer = nullptr) {
+                                  float old_lp, float adv, double* acc, int lane, int64_t row) {
     const float LN2 = 0.6931471805599453f;
     const float invT = 1.f / p.T;
     float r[NREC];
@@ -172,7 +193,8 @@ __device__ RowCoef row_epilogue16(const Params& p, const float* recs, int C, boo
     const float lS = log2f(S);
     const float lse2 = M + lS;
     const float lse = lse2 * LN2;
-    const float kk = float(double(p.grad_scale) / double(*p.n_valid));
+    const float kk =
+        float(double(p.grad_scale) / (p.divisor > 0.0 ? p.divisor : double(*p.n_valid)));
     float H = 0.f, lST = 0.f, lSq = 0.f, dce = 0.f, fkl = 0.f, rkl = 0.f;
     if (ENT) H = LN2 * (lS - E / S);
     if (TEACH) {
@@ -245,7 +267,7 @@ __device__ RowCoef row_epilogue16(const Params& p, const float* recs, int C, boo
     k.ts = ts;
     k.qc = qc;
     k.bc = bc;
-    if (lane == 0 && (accumulate || defer != nullptr)) {
+    if (lane == 0 && accumulate) {
         RowLoss rl;
         rl.ce = (lse2 - zy) * LN2;
         rl.lse = lse;
@@ -253,19 +275,19 @@ __device__ RowCoef row_epilogue16(const Params& p, const float* recs, int C, boo
         rl.fkl = fkl;
         rl.rkl = rkl;
         rl.grpo = grpo;
-        rl.lp = lp;
+        rl.lp = (zy - lse2) * LN2;
         rl.rho = rho;
         rl.kl3 = kl3;
         rl.adv = adv;
         rl.clipped = clipped ? 1.f : 0.f;
         rl.H = H;
-        if (defer != nullptr) *defer = rl;
-        else row_accumulate(f, rl, acc);
+        row_accumulate(f, rl, acc);
+        write_row_outputs(p, row, rl);
     }
     return k;
 }
 
-template <typename DT, int FEAT>
+template <typename DT, int FEAT, bool ACC>
 __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constant__ Params p) {
     using P16 = Pack16<DT>;
     constexpr int EPW = 8;
@@ -582,7 +604,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
             else __syncwarp();
             if (warp == 0) {
                 const RowCoef kw = row_epilogue16<TEACH, RKL, ENT, CAP>(
-                    p, xrec, C, rank == 0, old_lp, adv, acc, lane);
+                    p, xrec, C, rank == 0, old_lp, adv, acc, lane, r);
                 if (lane == 0) *reinterpret_cast<RowCoef*>(coefs) = kw;
             }
             ++xc;
@@ -606,6 +628,10 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                     for (int w = tid; w < nw; w += nthr) {
                         const int64_t eb = (wf + w) * EPW;
                         if (w >= wlo && w < whi) {
+                            // accumulating: this word's existing gradient values
+                            uint4 ow = make_uint4(0, 0, 0, 0);
+                            if (ACC) ow = *reinterpret_cast<const uint4*>(gg + eb);
+                            const uint32_t oa[4] = {ow.x, ow.y, ow.z, ow.w};
                             const uint4 a = *reinterpret_cast<const uint4*>(xs_b + size_t(w) * 16);
                             uint4 b = make_uint4(0, 0, 0, 0);
                             if (TEACH)
@@ -645,7 +671,8 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                                     g = fma2(q, qc2, g);
                                 }
                                 // dz/dx = s (1 - tanh^2); s is already in the coefficients
-                                out[kk] = P16::pack(CAP ? mul2(g, omt) : g);
+                                const f2 gw = CAP ? mul2(g, omt) : g;
+                                out[kk] = P16::pack(ACC ? add2(P16::unpack(oa[kk]), gw) : gw);
                             }
                             *reinterpret_cast<uint4*>(gg + eb) =
                                 make_uint4(out[0], out[1], out[2], out[3]);
@@ -673,6 +700,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                                 }
                                 g1 -= k.bc;
                                 if (CAP) g1 *= om1;
+                                if (ACC) g1 = P16::to_f(reinterpret_cast<const uint16_t*>(&ow)[iy]) + g1;
                                 reinterpret_cast<uint16_t*>(gg)[eb + iy] = P16::from_f(g1);
                             }
                         } else {
@@ -705,6 +733,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                                 }
                                 if (eb + i == ey) g -= k.bc;
                                 if (CAP) g *= dz;
+                                if (ACC) g = P16::to_f(reinterpret_cast<const uint16_t*>(gg)[eb + i]) + g;
                                 reinterpret_cast<uint16_t*>(gg)[eb + i] = P16::from_f(g);
                             }
                         }
@@ -713,8 +742,11 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                 if (CAP && poly) passC(BoolC<true>{});
                 else passC(BoolC<false>{});
             }
-        } else if (gg != nullptr) {
-            // a masked row: its gradient row is exact +0
+        } else {
+            if (rank == 0 && tid == 0) write_row_zero(p, r);
+        }
+        if (!valid && gg != nullptr && !ACC) {
+            // a masked row: its gradient row is exact +0 (kept when accumulating)
             for (int w = tid; w < nw; w += nthr) {
                 const int64_t eb = (wf + w) * EPW;
                 if (w >= wlo && w < whi) {

@@ -4,7 +4,7 @@
 namespace hl {
 
 #define HL_CASE(F) \
-    case F: return reinterpret_cast<const void*>(&rows_kernel16<__nv_bfloat16, F>);
+    case F: return reinterpret_cast<const void*>(&rows_kernel16<__nv_bfloat16, F, false>);
 
 const void* rows_kernel_bf16(int feat) {
     switch (feat) {

@@ -4,7 +4,7 @@
 namespace hl {
 
 #define HL_CASE(F) \
-    case F: return reinterpret_cast<const void*>(&rows_kernel16<__half, F>);
+    case F: return reinterpret_cast<const void*>(&rows_kernel16<__half, F, false>);
 
 const void* rows_kernel_fp16(int feat) {
     switch (feat) {

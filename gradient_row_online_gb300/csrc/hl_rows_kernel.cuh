@@ -250,14 +250,19 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
             if (C > 1) cluster_barrier();
             if (tid == 0) {
                 row_epilogue<A, TEACH, RKL, ENT, CAP>(p, xch + (xc & 1) * MAX_CLUSTER * NREC, C,
-                                                      rank == 0, old_lp, adv, acc, coef);
+                                                      rank == 0, old_lp, adv, acc, coef, r);
             }
             ++xc;
             __syncthreads();
         }
 
-        // ---- pass C: the combined gradient, written once ----
-        if (gg != nullptr) {
+        if (!valid && rank == 0 && tid == 0) {  // a masked row's per-token outputs
+            if (p.lp_out) p.lp_out[r] = 0.f;
+            if (p.rl_out) p.rl_out[r] = 0.f;
+        }
+        // ---- pass C: the combined gradient, written once (added to grad_out's
+        // values when accumulating; a masked row then keeps its values) ----
+        if (gg != nullptr && (valid || !p.accumulate)) {
             A lse2 = 0, lseT2 = 0, lsq2 = 0, pc = 0, ps = 0, tc = 0, ts_ = 0, qc = 0, bc = 0;
             if (valid) {
                 lse2 = coef[K_LSE2];
@@ -316,11 +321,19 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
                     for (int i = 0; i < EPW; ++i) gv[i] = A(0);
                 }
                 if (full) {
+                    if (p.accumulate) {
+                        A old[EPW];
+                        Tr::unpack(*reinterpret_cast<const uint4*>(gg + eb), old);
+#pragma unroll
+                        for (int i = 0; i < EPW; ++i) gv[i] = old[i] + gv[i];
+                    }
                     *reinterpret_cast<uint4*>(gg + eb) = Tr::pack(gv);
                 } else {
 #pragma unroll
                     for (int i = 0; i < EPW; ++i)
-                        if (eb + i >= e0 && eb + i < e1) gg[eb + i] = Tr::from_acc(gv[i]);
+                        if (eb + i >= e0 && eb + i < e1)
+                            gg[eb + i] = Tr::from_acc(p.accumulate ? Tr::to_acc(gg[eb + i]) + gv[i]
+                                                                   : gv[i]);
                 }
             }
         }

@@ -54,7 +54,7 @@ __device__ __forceinline__ float warp_max_f(float v) {
 // sums are rescaled: terms stay below 2^TAU, far from fp32 overflow.
 constexpr float STREAM_TAU = 16.f;
 
-template <typename DT, int FEAT>
+template <typename DT, int FEAT, bool ACC>
 __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_constant__ Params p) {
     using P16 = Pack16<DT>;
     constexpr int EPW = 8;
@@ -282,10 +282,11 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         if (has_labels && y >= V && tid == 0) atomicOr(p.err, E_LABEL);
 
         if (!valid) {  // a masked row: consume its entries, write exact +0
+            if (tid == 0) write_row_zero(p, r);
             for (int jl = 0; jl < K2x; ++jl) {
                 acquire();
                 const int cc = jl < K ? jl : K2x - 1 - jl;
-                if (jl >= K && gg != nullptr) {
+                if (jl >= K && gg != nullptr && !ACC) {  // kept when accumulating
                     const int64_t c0 = int64_t(cc) * CH;
                     const int nwc = int(((V - c0) < CH ? (V - c0) : CH) / EPW);
                     for (int w = tid; w < nwc; w += nthr)
@@ -483,7 +484,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         __syncthreads();
         if (warp == 0) {
             const RowCoef kw =
-                row_epilogue16<TEACH, RKL, ENT, CAP>(p, xch, nwarps, true, old_lp, adv, acc, lane);
+                row_epilogue16<TEACH, RKL, ENT, CAP>(p, xch, nwarps, true, old_lp, adv, acc, lane, r);
             if (lane == 0) *reinterpret_cast<RowCoef*>(coefs) = kw;
         }
         __syncthreads();
@@ -504,6 +505,11 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                 const int64_t c0 = int64_t(c) * CH;
                 const int nwc = int(((V - c0) < CH ? (V - c0) : CH) / EPW);
                 DT* grow = gg + r * V + c0;
+                // accumulating: the label element's existing value, read before the
+                // word store below overwrites it
+                float old_y = 0.f;
+                if (ACC && c == yc && yown)
+                    old_y = P16::to_f(reinterpret_cast<const uint16_t*>(grow)[yin]);
                 auto grad = [&](auto tierc) {
                     f2 cst[8];
                     if constexpr (CAP && decltype(tierc)::value > 0) load_rare(cst);
@@ -511,6 +517,9 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                     for (int i = 0; i < 4; ++i) {
                         const int w = tid + i * nthr;
                         if (i >= WPT || w >= nwc) continue;
+                        uint4 ow = make_uint4(0, 0, 0, 0);  // existing values (accumulating)
+                        if (ACC) ow = *reinterpret_cast<const uint4*>(grow + int64_t(w) * EPW);
+                        const uint32_t oa[4] = {ow.x, ow.y, ow.z, ow.w};
                         const uint4 a = *reinterpret_cast<const uint4*>(sb + size_t(w) * 16);
                         uint4 b = make_uint4(0, 0, 0, 0);
                         if (TEACH) b = *reinterpret_cast<const uint4*>(sb + opbytes + size_t(w) * 16);
@@ -545,7 +554,8 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                                 g = fma2(q, qc2, g);
                             }
                             // dz/dx = s (1 - tanh^2); s is already in the coefficients
-                            out[kk] = P16::pack(CAP ? mul2(g, omt) : g);
+                            const f2 gw = CAP ? mul2(g, omt) : g;
+                            out[kk] = P16::pack(ACC ? add2(P16::unpack(oa[kk]), gw) : gw);
                         }
                         *reinterpret_cast<uint4*>(grow + int64_t(w) * EPW) =
                             make_uint4(out[0], out[1], out[2], out[3]);
@@ -585,6 +595,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                     }
                     g1 -= k.bc;
                     if (CAP) g1 *= om1;
+                    if (ACC) g1 = old_y + g1;
                     reinterpret_cast<uint16_t*>(grow)[int64_t(w) * EPW + iy] =
                         P16::from_f(g1);
                 }

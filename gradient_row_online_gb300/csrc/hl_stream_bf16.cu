@@ -6,7 +6,7 @@
 namespace hl {
 
 #define HL_CASE(F) \
-    case F: return reinterpret_cast<const void*>(&stream_kernel16<__nv_bfloat16, F>);
+    case F: return reinterpret_cast<const void*>(&stream_kernel16<__nv_bfloat16, F, false>);
 #define HL_TEACH_SET(B) \
     HL_CASE(B) HL_CASE(B | F_TEACH) HL_CASE(B | F_TEACH | F_DCE) HL_CASE(B | F_TEACH | F_RKL) \
     HL_CASE(B | F_TEACH | F_RKL | F_DCE)

@@ -6,7 +6,7 @@
 namespace hl {
 
 #define HL_CASE(F) \
-    case F: return reinterpret_cast<const void*>(&stream_kernel16<__half, F>);
+    case F: return reinterpret_cast<const void*>(&stream_kernel16<__half, F, false>);
 #define HL_TEACH_SET(B) \
     HL_CASE(B) HL_CASE(B | F_TEACH) HL_CASE(B | F_TEACH | F_DCE) HL_CASE(B | F_TEACH | F_RKL) \
     HL_CASE(B | F_TEACH | F_RKL | F_DCE)

@@ -49,12 +49,19 @@ SLOTS = ("total", "ce", "z", "dist_ce", "fkl", "rkl", "grpo_loss", "new_logprob_
 EXPORTS = ("headloss_create", "headloss_forward_backward", "headloss_get_device_error",
            "headloss_plan", "headloss_force_plan", "headloss_launches_per_call",
            "headloss_destroy", "headloss_strerror", "headloss_version",
-           "headloss_forward_backward_noalloc")
+           "headloss_forward_backward_noalloc", "headloss_forward_backward_ext")
 
 
 # enum headloss_kernel
 HEADLOSS_KERNEL_AUTO, HEADLOSS_KERNEL_RESIDENT, HEADLOSS_KERNEL_STREAM = 0, 1, 2
 KERNELS = {0: "auto", 1: "resident", 2: "stream"}
+
+
+class headloss_call_ext(ctypes.Structure):
+    """struct headloss_call_ext: per-call extras (per-token outputs, gradient
+    accumulation, the divisor of a split batch)."""
+    _fields_ = [("new_logprobs", ctypes.c_void_p), ("row_loss", ctypes.c_void_p),
+                ("accumulate", ctypes.c_int), ("divisor", ctypes.c_double)]
 
 
 class headloss_plan_desc(ctypes.Structure):
@@ -111,6 +118,9 @@ def load_library(path: str = LIB_PATH):
         ctypes.c_uint32, ctypes.POINTER(headloss_weights), ctypes.c_float, ctypes.c_float,
         ctypes.c_float, ctypes.c_float, vp, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp]
     lib.headloss_forward_backward_noalloc.restype = i32
+    lib.headloss_forward_backward_ext.argtypes = [vp, vp, i64, i64, i32, vp, vp, vp, vp, vp, vp,
+                                                  ctypes.POINTER(headloss_call_ext), vp]
+    lib.headloss_forward_backward_ext.restype = i32
     _lib = lib
     return lib
 
@@ -178,6 +188,23 @@ def headloss_forward_backward(h, logits, N, V, dtype, labels, teacher_logits, ol
                                          _ptr(labels), _ptr(teacher_logits), _ptr(old_logprobs),
                                          _ptr(advantages), _ptr(grad_out), _ptr(scalars_out),
                                          _stream(stream)), "headloss_forward_backward")
+
+
+def headloss_forward_backward_ext(h, logits, N, V, dtype, labels, teacher_logits, old_logprobs,
+                                  advantages, grad_out, scalars_out, new_logprobs=None,
+                                  row_loss=None, accumulate=False, divisor=0.0,
+                                  stream=None) -> None:
+    """The call with its extras: per-row log p(label) and total loss outputs,
+    gradient accumulation into grad_out, and the divisor of a split batch."""
+    lib = load_library()
+    ext = headloss_call_ext(_ptr(new_logprobs), _ptr(row_loss), int(bool(accumulate)),
+                            float(divisor))
+    _check(lib.headloss_forward_backward_ext(h, _ptr(logits), int(N), int(V), int(dtype),
+                                             _ptr(labels), _ptr(teacher_logits),
+                                             _ptr(old_logprobs), _ptr(advantages),
+                                             _ptr(grad_out), _ptr(scalars_out),
+                                             ctypes.byref(ext), _stream(stream)),
+           "headloss_forward_backward_ext")
 
 
 def headloss_forward_backward_noalloc(flags, weights, temperature, clip_eps, softcap,
@@ -248,14 +275,21 @@ class HeadLoss:
         self.h = headloss_create(flags, weights, temperature, clip_eps, softcap, logits_scale)
 
     def __call__(self, logits, labels=None, teacher_logits=None, old_logprobs=None,
-                 advantages=None, grad_out=None, scalars_out=None, stream=None):
+                 advantages=None, grad_out=None, scalars_out=None, stream=None,
+                 new_logprobs=None, row_loss=None, accumulate=False, divisor=0.0):
         import torch
         N, V = logits.shape
         if scalars_out is None:
             scalars_out = torch.empty(16, dtype=torch.float32, device=logits.device)
-        headloss_forward_backward(self.h, logits, N, V, dtype_code(logits.dtype), labels,
-                                  teacher_logits, old_logprobs, advantages, grad_out,
-                                  scalars_out, stream)
+        if new_logprobs is None and row_loss is None and not accumulate and not divisor:
+            headloss_forward_backward(self.h, logits, N, V, dtype_code(logits.dtype), labels,
+                                      teacher_logits, old_logprobs, advantages, grad_out,
+                                      scalars_out, stream)
+        else:
+            headloss_forward_backward_ext(self.h, logits, N, V, dtype_code(logits.dtype), labels,
+                                          teacher_logits, old_logprobs, advantages, grad_out,
+                                          scalars_out, new_logprobs, row_loss, accumulate,
+                                          divisor, stream)
         return scalars_out
 
     def plan(self, V: int, dtype: int) -> dict:

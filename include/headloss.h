@@ -158,6 +158,58 @@ int headloss_forward_backward(headloss_t h, const void* logits, int64_t N, int64
                               void* grad_out, float* scalars_out, headloss_stream_t stream);
 
 /*
+ * Optional per-call extras of headloss_forward_backward_ext.  Zero-initialise
+ * the struct and set only what is needed; an all-zero struct (or a NULL
+ * pointer) gives exactly headloss_forward_backward.
+ *
+ * new_logprobs:  N fp32 (device) or NULL.  log p(label) of the student
+ *                softmax at T = 1 for every row: the GRPO "new_logprobs"
+ *                output of the fused head loss (Fast-LLM PR #549, "Loss
+ *                coverage").  Masked rows get 0.  Requires labels.
+ * row_loss:      N fp32 (device) or NULL.  The row's total loss,
+ *                sum_k weight_k * loss_k(row) over the selected losses, whose
+ *                mean over valid rows is scalars_out[HEADLOSS_SLOT_TOTAL] (per
+ *                token losses for callers that weight tokens themselves).
+ *                Masked rows get 0.
+ * accumulate:    0 writes grad_out; 1 adds this call's gradient to the values
+ *                already in grad_out (the sum formed in the kernel's compute
+ *                precision -- fp32 for 16-bit logits, fp64 for fp32 logits --
+ *                then one rounding to the output dtype), as in gradient accumulation
+ *                across micro-batches (PR #558, "Validation").  Masked rows
+ *                keep their values.  grad_out must not overlap the logits.
+ * divisor:       > 0: the normaliser of a batch split over several calls
+ *                (PR #549, "Correctness": cross-entropy splits).  It replaces
+ *                the call's own valid-row count in the gradient scale and in
+ *                the loss slots (TOTAL, CE, Z, DIST_CE, FKL, RKL, GRPO,
+ *                ENTROPY), so that the gradients and loss slots of the calls
+ *                that make up a batch add up to those of the whole batch when
+ *                every call passes the batch's valid-row count.  The metric
+ *                slots (NEW_LOGPROB .. ADV_STD, N_VALID, N_CLIPPED) stay over
+ *                the call's own rows.  0: the call's own count.  Must be
+ *                finite.
+ */
+typedef struct {
+    float* new_logprobs;
+    float* row_loss;
+    int accumulate;
+    double divisor;
+} headloss_call_ext;
+
+/*
+ * headloss_forward_backward_ext -- headloss_forward_backward with the extras
+ * above (the arguments before `ext` are those of headloss_forward_backward).
+ * Extra errors (host-side, nothing enqueued): ERR_ARG (divisor < 0 or not
+ * finite, accumulate with grad_out NULL or overlapping the logits), ERR_ALIGN
+ * (new_logprobs / row_loss not 4-byte aligned), ERR_MISSING_INPUT
+ * (new_logprobs without labels, N > 0).
+ */
+int headloss_forward_backward_ext(headloss_t h, const void* logits, int64_t N, int64_t V,
+                                  int dtype, const int64_t* labels, const void* teacher_logits,
+                                  const float* old_logprobs, const float* advantages,
+                                  void* grad_out, float* scalars_out,
+                                  const headloss_call_ext* ext, headloss_stream_t stream);
+
+/*
  * headloss_get_device_error -- synchronise `stream`, then read and clear the
  * handle's device error word.  *err receives HEADLOSS_OK, ERR_LABEL_RANGE or
  * ERR_TIMEOUT (the first of those raised since the last read).

@@ -45,6 +45,8 @@ def test_host_only_calls(lib):
     assert lib.headloss_force_plan(None, None) == hlb.HEADLOSS_ERR_ARG
     assert lib.headloss_forward_backward(None, None, 1, 1, 1, None, None, None, None, None,
                                          None, None) == hlb.HEADLOSS_ERR_ARG
+    assert lib.headloss_forward_backward_ext(None, None, 1, 1, 1, None, None, None, None, None,
+                                             None, None, None) == hlb.HEADLOSS_ERR_ARG
     e = ctypes.c_int()
     assert lib.headloss_get_device_error(None, None, ctypes.byref(e)) == hlb.HEADLOSS_ERR_ARG
     # invalid configurations are rejected before any device is touched
