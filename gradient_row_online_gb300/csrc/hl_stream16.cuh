@@ -132,14 +132,11 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
     };
     // zs + nshift of a pair (pass 1), by tier
     // the wide-tier and exp-tier constants live in shared memory (the `red`
-    // area, unused here) and are read where those tiers run, so the common
-    // tier keeps their registers free
+    // area, unused here) and are read at each use (volatile: never hoisted into
+    // registers), so the common tier keeps all registers for itself
     f2* rare = reinterpret_cast<f2*>(red);  // QB[0..5], A22, Kc2
-    auto load_rare = [&](f2* cst) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) cst[i] = rare[i];
-    };
-    auto shifted = [&](f2 xv, f2 nshift, auto tierc, const f2* cst) -> f2 {
+    const volatile f2* cst = rare;
+    auto shifted = [&](f2 xv, f2 nshift, auto tierc) -> f2 {
         constexpr int TI = CAP ? decltype(tierc)::value : -1;
         if constexpr (TI < 0) {
             return fma2(xv, K2, nshift);
@@ -162,7 +159,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         }
     };
     // zs and 1 - tanh^2 of a pair (pass 2, softcap), by tier
-    auto zs_omt = [&](f2 xv, f2& zs, f2& omt, auto tierc, const f2* cst) {
+    auto zs_omt = [&](f2 xv, f2& zs, f2& omt, auto tierc) {
         constexpr int TI = decltype(tierc)::value;
         if constexpr (TI == 0 || TI == 1) {
             const f2 u = mul2(xv, xv);
@@ -298,63 +295,87 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             continue;
         }
 
-        // the label column: its chunk, its offset there, and whether this
-        // thread's words of that chunk hold it
+        // the label column: thread 0 reads its logit now and uses it at the
+        // merge (so the read is not waited for); the thread whose pass-2 word
+        // holds it patches that element after the row's last chunk
         const int yc = has_labels ? int(y / CH) : -1;
         const int yin = has_labels ? int(y - int64_t(yc) * CH) : 0;
         const int ywd = yin / EPW;
         const bool yown = has_labels && ywd >= tid && (ywd - tid) % nthr == 0 &&
                           (ywd - tid) / nthr < WPT;
+        uint16_t xy_bits = 0;
+        if (has_labels && tid == 0) xy_bits = reinterpret_cast<const uint16_t*>(xg)[r * V + y];
 
         // ---------------- pass 1: online statistics ----------------
         float zm = fixed_shift ? Kc : -CUDART_INF_F, um = -CUDART_INF_F;
         f2 S2 = z2, E2 = z2, ST2 = z2, Sq2 = z2, Eq2 = z2, Xp2 = z2, Y2 = z2;
-        float zy = 0.f, hasy = 0.f;
         uint64_t tiers = 0;  // softcap: 2 bits per chunk (chunks 0..31) of this warp
         int tier_hi = 0;     // softcap: highest tier of chunks 32.. of this warp
+        const bool need_sx = !CAP || !fixed_shift;
+        // one pair's contribution to the sums, given its shifted logit d
+        auto accum = [&](f2 d, uint32_t tbits, f2 num2) {
+            const f2 e = ex2p(d);
+            S2 = add2(S2, e);
+            if (ENT) E2 = fma2(e, d, E2);
+            if (TEACH) {
+                const f2 dT = mul2(d, invT2);
+                const f2 eT = ex2p(dT);
+                ST2 = add2(ST2, eT);
+                const f2 du = fma2(P16::unpack(tbits), KT2, num2);
+                const f2 eq = ex2p(du);
+                Sq2 = add2(Sq2, eq);
+                if (DCE) Eq2 = fma2(eq, du, Eq2);
+                const f2 wd = sub2(du, dT);
+                Xp2 = fma2(eq, wd, Xp2);
+                if (RKL) Y2 = fma2(eT, wd, Y2);
+            }
+        };
         for (int c = 0; c < K; ++c) {
             const unsigned char* sb = acquire();
             const int64_t c0 = int64_t(c) * CH;
             const int nwc = int(((V - c0) < CH ? (V - c0) : CH) / EPW);
-            uint4 xw[4], tw[4];
-            int nmine = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int w = tid + i * nthr;
-                if (i < WPT && w < nwc) {
-                    xw[i] = *reinterpret_cast<const uint4*>(sb + size_t(w) * 16);
-                    if (TEACH) tw[i] = *reinterpret_cast<const uint4*>(sb + opbytes + size_t(w) * 16);
-                    nmine = i + 1;
-                }
-            }
+            // a full chunk gives every thread four words: the hot path
+            const bool full = WPT == 4 && nwc == 4 * nthr;
+            const bool mine = full || tid < nwc;
             // chunk maxima of this thread's words on packed pairs: max |x|
             // (softcap tier), signed max x (shift, unless fixed), max t
             uint32_t ma = 0u, ms = P16::NEG_INF2, mt = P16::NEG_INF2;
-            auto maxima = [&](auto sxc) {
-                constexpr bool SX = decltype(sxc)::value;
+            auto maxw = [&](const uint4& a, const uint4& b, auto sxc) {
+                if (CAP)
+                    ma = P16::absmax2(ma, P16::absmax2(P16::absmax2(a.x, a.y),
+                                                       P16::absmax2(a.z, a.w)));
+                if (decltype(sxc)::value)
+                    ms = P16::max2(ms, P16::max2(P16::max2(a.x, a.y), P16::max2(a.z, a.w)));
+                if (TEACH)
+                    mt = P16::max2(mt, P16::max2(P16::max2(b.x, b.y), P16::max2(b.z, b.w)));
+            };
+            uint4 xw[4], tw[4];
+            if (full) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    if (i < nmine) {
-                        const uint4 a = xw[i];
-                        if (CAP) {
-                            ma = P16::absmax2(ma, P16::absmax2(P16::absmax2(a.x, a.y),
-                                                               P16::absmax2(a.z, a.w)));
-                        }
-                        if (SX) {
-                            ms = P16::max2(ms, P16::max2(P16::max2(a.x, a.y),
-                                                         P16::max2(a.z, a.w)));
-                        }
-                        if (TEACH) {
-                            const uint4 b = tw[i];
-                            mt = P16::max2(mt, P16::max2(P16::max2(b.x, b.y),
-                                                         P16::max2(b.z, b.w)));
-                        }
-                    }
+                    const int w = tid + i * nthr;
+                    xw[i] = *reinterpret_cast<const uint4*>(sb + size_t(w) * 16);
+                    if (TEACH) tw[i] = *reinterpret_cast<const uint4*>(sb + opbytes + size_t(w) * 16);
+                    else tw[i] = make_uint4(0, 0, 0, 0);
                 }
-            };
-            const bool need_sx = !CAP || !fixed_shift;
-            if (need_sx) maxima(BoolC<true>{});
-            else maxima(BoolC<false>{});
+                if (need_sx) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) maxw(xw[i], tw[i], BoolC<true>{});
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) maxw(xw[i], tw[i], BoolC<false>{});
+                }
+            } else {
+#pragma unroll 1
+                for (int i = 0; i < WPT; ++i) {
+                    const int w = tid + i * nthr;
+                    if (w >= nwc) break;
+                    const uint4 a = *reinterpret_cast<const uint4*>(sb + size_t(w) * 16);
+                    const uint4 b = TEACH ? *reinterpret_cast<const uint4*>(sb + opbytes + size_t(w) * 16)
+                                          : make_uint4(0, 0, 0, 0);
+                    maxw(a, b, BoolC<true>{});
+                }
+            }
             float ca, cb;
             // lazy, warp-uniform shifts: raise a shift only when the warp's
             // chunk maximum exceeds it by TAU
@@ -362,7 +383,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             bool mv = false;
             if (need_sx) {
                 upk(P16::unpack(ms), ca, cb);
-                const float wmx = warp_max_f(nmine ? fmaxf(ca, cb) : -CUDART_INF_F);
+                const float wmx = warp_max_f(mine ? fmaxf(ca, cb) : -CUDART_INF_F);
                 if (wmx > -CUDART_INF_F) {
                     const float bz = zs1(wmx);
                     if (bz > zm + STREAM_TAU) {
@@ -373,7 +394,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             }
             if (TEACH) {
                 upk(P16::unpack(mt), ca, cb);
-                const float wmt = warp_max_f(nmine ? fmaxf(ca, cb) : -CUDART_INF_F);
+                const float wmt = warp_max_f(mine ? fmaxf(ca, cb) : -CUDART_INF_F);
                 if (wmt > -CUDART_INF_F) {
                     const float bu = __fmul_rn(wmt, KT);
                     if (bu > um + STREAM_TAU) {
@@ -413,45 +434,42 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                 else tier_hi = tier > tier_hi ? tier : tier_hi;
             }
             const f2 nzm2 = pk1(-zm), num2 = pk1(-um);
-            auto sums = [&](auto tierc) {
-                f2 cst[8];
-                if constexpr (CAP && decltype(tierc)::value > 0) load_rare(cst);
+            if (full && tier == 0) {
+                // hot path: four words, the narrow tier (or no softcap), unrolled
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    if (i >= nmine) continue;
                     const uint32_t xa[4] = {xw[i].x, xw[i].y, xw[i].z, xw[i].w};
                     const uint32_t tb[4] = {tw[i].x, tw[i].y, tw[i].z, tw[i].w};
 #pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        accum(shifted(P16::unpack(xa[kk]), nzm2, IntC<0>{}), tb[kk], num2);
+                }
+            } else {
+                // cold path: a partial chunk or a wider tier, one word at a time
+#pragma unroll 1
+                for (int i = 0; i < WPT; ++i) {
+                    const int w = tid + i * nthr;
+                    if (w >= nwc) break;
+                    const uint4 a = *reinterpret_cast<const uint4*>(sb + size_t(w) * 16);
+                    const uint4 b = TEACH ? *reinterpret_cast<const uint4*>(sb + opbytes + size_t(w) * 16)
+                                          : make_uint4(0, 0, 0, 0);
+                    const uint32_t xa[4] = {a.x, a.y, a.z, a.w};
+                    const uint32_t tb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const f2 d = shifted(P16::unpack(xa[kk]), nzm2, tierc, cst);
-                        const f2 e = ex2p(d);
-                        S2 = add2(S2, e);
-                        if (ENT) E2 = fma2(e, d, E2);
-                        if (TEACH) {
-                            const f2 dT = mul2(d, invT2);
-                            const f2 eT = ex2p(dT);
-                            ST2 = add2(ST2, eT);
-                            const f2 du = fma2(P16::unpack(tb[kk]), KT2, num2);
-                            const f2 eq = ex2p(du);
-                            Sq2 = add2(Sq2, eq);
-                            if (DCE) Eq2 = fma2(eq, du, Eq2);
-                            const f2 wd = sub2(du, dT);
-                            Xp2 = fma2(eq, wd, Xp2);
-                            if (RKL) Y2 = fma2(eT, wd, Y2);
-                        }
+                        const f2 xv = P16::unpack(xa[kk]);
+                        f2 d;
+                        if (!CAP || tier == 0) d = shifted(xv, nzm2, IntC<0>{});
+                        else if (tier == 1) d = shifted(xv, nzm2, IntC<1>{});
+                        else d = shifted(xv, nzm2, IntC<2>{});
+                        accum(d, tb[kk], num2);
                     }
                 }
-            };
-            if (tier == 0) sums(IntC<0>{});
-            else if (tier == 1) sums(IntC<1>{});
-            else sums(IntC<2>{});
-            // the label column's logit, from the thread that holds it
-            if (c == yc && yown) {
-                zy = zs1(P16::to_f(reinterpret_cast<const uint16_t*>(sb)[yin]));
-                hasy = 1.f;
             }
             release(r, c);
         }
+        const float zy = (has_labels && tid == 0) ? zs1(P16::to_f(xy_bits)) : 0.f;
+        const float hasy = (has_labels && tid == 0) ? 1.f : 0.f;
 
         // ---------------- merge: threads -> warps -> row ----------------
         // the shifts are warp-uniform, so a warp's record is a plain sum
@@ -498,109 +516,124 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         const f2 pc2 = pk1(h.pc), ps2 = pk1(h.ps), tc2 = pk1(h.tc), ts2 = pk1(h.ts);
         const f2 qc2 = pk1(h.qc), s2 = pk1(s), ndlse2 = pk1(-dlse);
         const f2 nKT2 = pk1(-KT);
+        // accumulating: the label element's existing value, read before this
+        // row's word stores overwrite it
+        float old_y = 0.f;
+        if (ACC && yown && gg != nullptr)
+            old_y = P16::to_f(reinterpret_cast<const uint16_t*>(gg)[r * V + y]);
+        // the gradient of one word (8 elements), without the label term
+        auto grad_word = [&](uint4 a, uint4 b, uint4 ow, auto tierc) -> uint4 {
+            const uint32_t xa[4] = {a.x, a.y, a.z, a.w};
+            const uint32_t tb[4] = {b.x, b.y, b.z, b.w};
+            const uint32_t oa[4] = {ow.x, ow.y, ow.z, ow.w};
+            uint32_t out[4];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const f2 xv = P16::unpack(xa[kk]);
+                f2 zs = z2, omt = z2, arg, argT = z2;
+                if constexpr (CAP) {
+                    zs_omt(xv, zs, omt, tierc);
+                    arg = add2(zs, nlse2);
+                    if (TEACH) argT = fma2(zs, invT2, nlseT2);
+                } else {
+                    arg = fma2(xv, K2, nlse2);
+                    if (TEACH) argT = fma2(xv, KinvT2, nlseT2);
+                }
+                f2 g = mul2(ex2p(arg), ENTG ? fma2(ps2, arg, pc2) : pc2);
+                if (TEACH) {
+                    const f2 tv = P16::unpack(tb[kk]);
+                    const f2 pT = ex2p(argT);
+                    const f2 q = ex2p(fma2(tv, KT2, nlsq2));
+                    f2 tco = tc2;
+                    if (RKL) {
+                        // log pT - log q from the logit difference
+                        const f2 dxu = CAP ? fma2(zs, invT2, mul2(tv, nKT2))
+                                           : mul2(fma2(xv, s2, sub2(z2, tv)), KT2);
+                        tco = fma2(ts2, add2(dxu, ndlse2), tc2);
+                    }
+                    g = fma2(pT, tco, g);
+                    g = fma2(q, qc2, g);
+                }
+                // dz/dx = s (1 - tanh^2); s is already in the coefficients
+                const f2 gw = CAP ? mul2(g, omt) : g;
+                out[kk] = P16::pack(ACC ? add2(P16::unpack(oa[kk]), gw) : gw);
+            }
+            return make_uint4(out[0], out[1], out[2], out[3]);
+        };
         for (int cr = 0; cr < K; ++cr) {
             const int c = K - 1 - cr;
             const unsigned char* sb = acquire();
             if (gg != nullptr) {
                 const int64_t c0 = int64_t(c) * CH;
                 const int nwc = int(((V - c0) < CH ? (V - c0) : CH) / EPW);
+                const bool full = WPT == 4 && nwc == 4 * nthr;
                 DT* grow = gg + r * V + c0;
-                // accumulating: the label element's existing value, read before the
-                // word store below overwrites it
-                float old_y = 0.f;
-                if (ACC && c == yc && yown)
-                    old_y = P16::to_f(reinterpret_cast<const uint16_t*>(grow)[yin]);
-                auto grad = [&](auto tierc) {
-                    f2 cst[8];
-                    if constexpr (CAP && decltype(tierc)::value > 0) load_rare(cst);
+                const int tier = !CAP ? 0 : c < 32 ? int((tiers >> (2 * c)) & 3u) : tier_hi;
+                if (full && tier == 0) {
+                    // hot path: four words, the narrow tier (or no softcap), unrolled
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int w = tid + i * nthr;
-                        if (i >= WPT || w >= nwc) continue;
-                        uint4 ow = make_uint4(0, 0, 0, 0);  // existing values (accumulating)
+                        uint4 ow = make_uint4(0, 0, 0, 0);
                         if (ACC) ow = *reinterpret_cast<const uint4*>(grow + int64_t(w) * EPW);
-                        const uint32_t oa[4] = {ow.x, ow.y, ow.z, ow.w};
                         const uint4 a = *reinterpret_cast<const uint4*>(sb + size_t(w) * 16);
-                        uint4 b = make_uint4(0, 0, 0, 0);
-                        if (TEACH) b = *reinterpret_cast<const uint4*>(sb + opbytes + size_t(w) * 16);
-                        const uint32_t xa[4] = {a.x, a.y, a.z, a.w};
-                        const uint32_t tb[4] = {b.x, b.y, b.z, b.w};
-                        uint32_t out[4];
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const f2 xv = P16::unpack(xa[kk]);
-                            f2 zs = z2, omt = z2, arg, argT = z2;
-                            if constexpr (CAP) {
-                                zs_omt(xv, zs, omt, tierc, cst);
-                                arg = add2(zs, nlse2);
-                                if (TEACH) argT = fma2(zs, invT2, nlseT2);
-                            } else {
-                                arg = fma2(xv, K2, nlse2);
-                                if (TEACH) argT = fma2(xv, KinvT2, nlseT2);
-                            }
-                            f2 g = mul2(ex2p(arg), ENTG ? fma2(ps2, arg, pc2) : pc2);
-                            if (TEACH) {
-                                const f2 tv = P16::unpack(tb[kk]);
-                                const f2 pT = ex2p(argT);
-                                const f2 q = ex2p(fma2(tv, KT2, nlsq2));
-                                f2 tco = tc2;
-                                if (RKL) {
-                                    // log pT - log q from the logit difference
-                                    const f2 dxu = CAP ? fma2(zs, invT2, mul2(tv, nKT2))
-                                                       : mul2(fma2(xv, s2, sub2(z2, tv)), KT2);
-                                    tco = fma2(ts2, add2(dxu, ndlse2), tc2);
-                                }
-                                g = fma2(pT, tco, g);
-                                g = fma2(q, qc2, g);
-                            }
-                            // dz/dx = s (1 - tanh^2); s is already in the coefficients
-                            const f2 gw = CAP ? mul2(g, omt) : g;
-                            out[kk] = P16::pack(ACC ? add2(P16::unpack(oa[kk]), gw) : gw);
-                        }
+                        const uint4 b = TEACH ? *reinterpret_cast<const uint4*>(sb + opbytes + size_t(w) * 16)
+                                              : make_uint4(0, 0, 0, 0);
                         *reinterpret_cast<uint4*>(grow + int64_t(w) * EPW) =
-                            make_uint4(out[0], out[1], out[2], out[3]);
+                            grad_word(a, b, ow, IntC<0>{});
                     }
-                };
-                const int tier = !CAP ? 0 : c < 32 ? int((tiers >> (2 * c)) & 3u) : tier_hi;
-                if (tier == 0) grad(IntC<0>{});
-                else if (tier == 1) grad(IntC<1>{});
-                else grad(IntC<2>{});
-                // the label column: the thread whose word holds it recomputes that
-                // one element with the label term and overwrites it (program order
-                // keeps the later store)
-                if (c == yc && yown) {
-                    const int w = ywd;
-                    const int iy = yin - ywd * EPW;
-                    const uint16_t* xs16 = reinterpret_cast<const uint16_t*>(sb);
-                    const float xv1 = P16::to_f(xs16[w * EPW + iy]);
-                    float zs, om1 = 1.f;
-                    if (CAP) zs = __fmul_rn(tanh_a2x_1(__fmul_rn(xv1, A2), &om1), Kc);
-                    else zs = __fmul_rn(xv1, K1);
-                    // (the scalars are read back from the packed constants)
-                    const float arg = zs + lo_of(nlse2);
-                    float g1 = ex2f(arg) * (ENTG ? fmaf(lo_of(ps2), arg, lo_of(pc2)) : lo_of(pc2));
-                    if (TEACH) {
-                        const float tv1 = P16::to_f(
-                            reinterpret_cast<const uint16_t*>(sb + opbytes)[w * EPW + iy]);
-                        const float pT = ex2f(fmaf(zs, lo_of(invT2), lo_of(nlseT2)));
-                        const float q = ex2f(fmaf(tv1, lo_of(KT2), lo_of(nlsq2)));
-                        float tco = lo_of(tc2);
-                        if (RKL) {
-                            const float dxu = CAP ? fmaf(tv1, -LOG2E, zs) * lo_of(invT2)
-                                                  : fmaf(xv1, s, -tv1) * lo_of(KT2);
-                            tco = fmaf(lo_of(ts2), dxu + lo_of(ndlse2), lo_of(tc2));
-                        }
-                        g1 = fmaf(pT, tco, g1);
-                        g1 = fmaf(q, lo_of(qc2), g1);
+                } else {
+                    // cold path: a partial chunk or a wider tier, one word at a time
+#pragma unroll 1
+                    for (int i = 0; i < WPT; ++i) {
+                        const int w = tid + i * nthr;
+                        if (w >= nwc) break;
+                        uint4 ow = make_uint4(0, 0, 0, 0);
+                        if (ACC) ow = *reinterpret_cast<const uint4*>(grow + int64_t(w) * EPW);
+                        const uint4 a = *reinterpret_cast<const uint4*>(sb + size_t(w) * 16);
+                        const uint4 b = TEACH ? *reinterpret_cast<const uint4*>(sb + opbytes + size_t(w) * 16)
+                                              : make_uint4(0, 0, 0, 0);
+                        uint4 o;
+                        if (!CAP || tier == 0) o = grad_word(a, b, ow, IntC<0>{});
+                        else if (tier == 1) o = grad_word(a, b, ow, IntC<1>{});
+                        else o = grad_word(a, b, ow, IntC<2>{});
+                        *reinterpret_cast<uint4*>(grow + int64_t(w) * EPW) = o;
                     }
-                    g1 -= k.bc;
-                    if (CAP) g1 *= om1;
-                    if (ACC) g1 = old_y + g1;
-                    reinterpret_cast<uint16_t*>(grow)[int64_t(w) * EPW + iy] =
-                        P16::from_f(g1);
                 }
             }
             release(r, K2x - 1 - c);
+        }
+        // the label column: the thread whose word held it recomputes that one
+        // element with the label term (inputs re-read from global memory) and
+        // overwrites it; program order puts this store after its word store
+        if (yown && gg != nullptr) {
+            // the coefficients again from shared memory (no register carries them
+            // through the chunk loop; they stay until the next row's merge)
+            const RowCoef k = *reinterpret_cast<const RowCoef*>(coefs);
+            const ShiftCoef h = shift_coefs(k, ENTG);
+            const float dlse = k.lseT2 - k.lsq2;
+            const float xv1 = P16::to_f(reinterpret_cast<const uint16_t*>(xg)[r * V + y]);
+            float zs, om1 = 1.f;
+            if (CAP) zs = __fmul_rn(tanh_a2x_1(__fmul_rn(xv1, A2), &om1), Kc);
+            else zs = __fmul_rn(xv1, K1);
+            const float arg = zs + h.nlse;
+            float g1 = ex2f(arg) * (ENTG ? fmaf(h.ps, arg, h.pc) : h.pc);
+            if (TEACH) {
+                const float tv1 = P16::to_f(reinterpret_cast<const uint16_t*>(tg)[r * V + y]);
+                const float pT = ex2f(fmaf(zs, invT, h.nlseT));
+                const float q = ex2f(fmaf(tv1, KT, h.nlsq));
+                float tco = h.tc;
+                if (RKL) {
+                    const float dxu = CAP ? fmaf(tv1, -LOG2E, zs) * invT : fmaf(xv1, s, -tv1) * KT;
+                    tco = fmaf(h.ts, dxu - dlse, h.tc);
+                }
+                g1 = fmaf(pT, tco, g1);
+                g1 = fmaf(q, h.qc, g1);
+            }
+            g1 -= k.bc;
+            if (CAP) g1 *= om1;
+            if (ACC) g1 = old_y + g1;
+            reinterpret_cast<uint16_t*>(gg)[r * V + y] = P16::from_f(g1);
         }
     }
 
