@@ -99,36 +99,26 @@ __device__ __forceinline__ ShiftCoef shift_coefs(const RowCoef& k, bool entg) {
 struct RowLoss {
     float ce, lse, dce, fkl, rkl, grpo, lp, rho, kl3, adv, clipped, H;
 };
-// The per-token outputs of one row (valid rows; masked rows get zeros from
-// write_row_zero).
-__device__ __forceinline__ void write_row_outputs(const Params& p, int64_t row, const RowLoss& rl) {
-    const uint32_t f = p.flags;
-    if (p.lp_out) p.lp_out[row] = rl.lp;
-    if (p.rl_out) {
-        double t = 0.0;
-        if (f & L_CE) t += double(p.w_ce) * double(rl.ce);
-        if (f & L_Z) t += double(p.w_z) * double(rl.lse) * double(rl.lse);
-        if (f & L_DIST_CE) t += double(p.w_dce) * double(rl.dce);
-        if (f & L_FKL) t += double(p.w_fkl) * double(rl.fkl);
-        if (f & L_RKL) t += double(p.w_rkl) * double(rl.rkl);
-        if (f & L_GRPO) t += double(p.w_grpo) * double(rl.grpo);
-        if (f & L_ENTROPY) t += double(p.w_ent) * double(rl.H);
-        p.rl_out[row] = float(t);
-    }
-}
+// The per-token outputs of a masked row.
 __device__ __forceinline__ void write_row_zero(const Params& p, int64_t row) {
     if (p.lp_out) p.lp_out[row] = 0.f;
     if (p.rl_out) p.rl_out[row] = 0.f;
 }
 
-__device__ __forceinline__ void row_accumulate(uint32_t f, const RowLoss& rl, double* acc) {
+// Adds one row's loss values to the CTA's fp64 sums and writes its per-token
+// outputs (fused, so no value outlives the row's epilogue any longer than the
+// sums need it).
+__device__ __forceinline__ void row_accumulate(const Params& p, const RowLoss& rl, double* acc,
+                                               int64_t row) {
+    const uint32_t f = p.flags;
+    float t = 0.f;
     acc[A_NVALID] += 1.0;
-    if (f & L_CE) acc[A_CE] += double(rl.ce);
-    if (f & L_Z) acc[A_Z] += double(rl.lse) * double(rl.lse);
-    if (f & L_DIST_CE) acc[A_DCE] += double(rl.dce);
-    if (f & L_FKL) acc[A_FKL] += double(rl.fkl);
-    if (f & L_RKL) acc[A_RKL] += double(rl.rkl);
-    if (f & L_GRPO) acc[A_GRPO] += double(rl.grpo);
+    if (f & L_CE) { acc[A_CE] += double(rl.ce); t = fmaf(p.w_ce, rl.ce, t); }
+    if (f & L_Z) { const double z = double(rl.lse) * double(rl.lse); acc[A_Z] += z; t = fmaf(p.w_z, float(z), t); }
+    if (f & L_DIST_CE) { acc[A_DCE] += double(rl.dce); t = fmaf(p.w_dce, rl.dce, t); }
+    if (f & L_FKL) { acc[A_FKL] += double(rl.fkl); t = fmaf(p.w_fkl, rl.fkl, t); }
+    if (f & L_RKL) { acc[A_RKL] += double(rl.rkl); t = fmaf(p.w_rkl, rl.rkl, t); }
+    if (f & L_GRPO) { acc[A_GRPO] += double(rl.grpo); t = fmaf(p.w_grpo, rl.grpo, t); }
     if (f & L_GRPO_STATS) {
         acc[A_LP] += double(rl.lp);
         acc[A_RATIO] += double(rl.rho);
@@ -137,7 +127,9 @@ __device__ __forceinline__ void row_accumulate(uint32_t f, const RowLoss& rl, do
         acc[A_ADV2] += double(rl.adv) * double(rl.adv);
         acc[A_NCLIP] += double(rl.clipped);
     }
-    if (f & L_ENTROPY) acc[A_ENT] += double(rl.H);
+    if (f & L_ENTROPY) { acc[A_ENT] += double(rl.H); t = fmaf(p.w_ent, rl.H, t); }
+    if (p.lp_out) p.lp_out[row] = rl.lp;
+    if (p.rl_out) p.rl_out[row] = t;
 }
 
 // A warp merges the C records of a row (lane k holds record k) and derives
@@ -281,14 +273,16 @@ __device__ RowCoef row_epilogue16(const Params& p, const float* recs, int C, boo
         rl.adv = adv;
         rl.clipped = clipped ? 1.f : 0.f;
         rl.H = H;
-        row_accumulate(f, rl, acc);
-        write_row_outputs(p, row, rl);
+        row_accumulate(p, rl, acc, row);
     }
     return k;
 }
 
+// The body of the resident kernel (one instantiation per feature set and
+// accumulation mode); the two entry points below differ only in their
+// register budget.
 template <typename DT, int FEAT, bool ACC>
-__global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constant__ Params p) {
+__device__ __forceinline__ void rows_body16(const Params& p) {
     using P16 = Pack16<DT>;
     constexpr int EPW = 8;
     constexpr int ES = 2;
@@ -413,6 +407,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
         }
         const bool valid = !has_labels || (y >= 0 && y < V);
         if (has_labels && y >= V && rank == 0 && tid == 0) atomicOr(p.err, E_LABEL);
+        if (!valid && rank == 0 && tid == 0) write_row_zero(p, r);  // per-token outputs
 
         const int st = it % p.nbuf;
         const uint32_t par = uint32_t(it / p.nbuf) & 1u;
@@ -683,20 +678,20 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                                 float zs, om1 = 1.f;
                                 if (CAP) zs = __fmul_rn(tanh_a2x_1(__fmul_rn(xv1, A2), &om1), Kc);
                                 else zs = __fmul_rn(xv1, K);
-                                const float arg = zs + h.nlse;
-                                float g1 = ex2f(arg) * (ENT ? fmaf(h.ps, arg, h.pc) : h.pc);
+                                const float arg = zs + lo_of(nlse2);
+                                float g1 = ex2f(arg) * (ENT ? fmaf(lo_of(ps2), arg, lo_of(pc2)) : lo_of(pc2));
                                 if (TEACH) {
                                     const float tv1 = P16::to_f(ts[w * EPW + iy]);
-                                    const float pT = ex2f(fmaf(zs, invT, h.nlseT));
-                                    const float q = ex2f(fmaf(tv1, KT, h.nlsq));
-                                    float tco = h.tc;
+                                    const float pT = ex2f(fmaf(zs, invT, lo_of(nlseT2)));
+                                    const float q = ex2f(fmaf(tv1, KT, lo_of(nlsq2)));
+                                    float tco = lo_of(tc2);
                                     if (RKL) {
                                         const float dxu = CAP ? fmaf(tv1, -LOG2E, zs) * invT
                                                               : fmaf(xv1, s, -tv1) * KT;
-                                        tco = fmaf(h.ts, dxu - dlse, h.tc);
+                                        tco = fmaf(lo_of(ts2), dxu - dlse, lo_of(tc2));
                                     }
                                     g1 = fmaf(pT, tco, g1);
-                                    g1 = fmaf(q, h.qc, g1);
+                                    g1 = fmaf(q, lo_of(qc2), g1);
                                 }
                                 g1 -= k.bc;
                                 if (CAP) g1 *= om1;
@@ -716,20 +711,20 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                                 } else {
                                     zs = __fmul_rn(xv, K);
                                 }
-                                const float arg = zs + h.nlse;
-                                float g = ex2f(arg) * (ENT ? fmaf(h.ps, arg, h.pc) : h.pc);
+                                const float arg = zs + lo_of(nlse2);
+                                float g = ex2f(arg) * (ENT ? fmaf(lo_of(ps2), arg, lo_of(pc2)) : lo_of(pc2));
                                 if (TEACH) {
                                     const float tv = P16::to_f(ts[w * EPW + i]);
-                                    const float pT = ex2f(fmaf(zs, invT, h.nlseT));
-                                    const float q = ex2f(fmaf(tv, KT, h.nlsq));
-                                    float tco = h.tc;
+                                    const float pT = ex2f(fmaf(zs, invT, lo_of(nlseT2)));
+                                    const float q = ex2f(fmaf(tv, KT, lo_of(nlsq2)));
+                                    float tco = lo_of(tc2);
                                     if (RKL) {
                                         const float dxu = CAP ? fmaf(tv, -LOG2E, zs) * invT
                                                               : fmaf(xv, s, -tv) * KT;
-                                        tco = fmaf(h.ts, dxu - dlse, h.tc);
+                                        tco = fmaf(lo_of(ts2), dxu - dlse, lo_of(tc2));
                                     }
                                     g = fmaf(pT, tco, g);
-                                    g = fmaf(q, h.qc, g);
+                                    g = fmaf(q, lo_of(qc2), g);
                                 }
                                 if (eb + i == ey) g -= k.bc;
                                 if (CAP) g *= dz;
@@ -742,10 +737,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
                 if (CAP && poly) passC(BoolC<true>{});
                 else passC(BoolC<false>{});
             }
-        } else {
-            if (rank == 0 && tid == 0) write_row_zero(p, r);
-        }
-        if (!valid && gg != nullptr && !ACC) {
+        } else if (gg != nullptr && !ACC) {
             // a masked row: its gradient row is exact +0 (kept when accumulating)
             for (int w = tid; w < nw; w += nthr) {
                 const int64_t eb = (wf + w) * EPW;
@@ -771,6 +763,11 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constan
         for (int i = 0; i < NACC; ++i) out[i] = acc[i];
     }
     if (C > 1) cluster_barrier();
+}
+
+template <typename DT, int FEAT, bool ACC>
+__global__ void __launch_bounds__(THREADS, 1) rows_kernel16(const __grid_constant__ Params p) {
+    rows_body16<DT, FEAT, ACC>(p);
 }
 
 }  // namespace hl
