@@ -59,17 +59,21 @@ struct FinalizeArgs {
 // Sums the per-cluster partials in cluster order (fp64) and writes the
 // sixteen scalars (means over valid rows, or loss sums over the caller's
 // divisor; unselected slots 0).
-__global__ void finalize_kernel(const double* partials, int nclusters, const long long* n_valid,
-                                FinalizeArgs a, float* out) {
+// One warp per slot (blockDim = 32 * NACC): lane l sums clusters l, l + 32,
+// ..., then a butterfly adds the 32 lane sums.  Assignment and order are fixed,
+// so the result is bit-identical from call to call.
+__global__ void __launch_bounds__(32 * NACC) finalize_kernel(const double* partials, int nclusters,
+                                                             const long long* n_valid,
+                                                             FinalizeArgs a, float* out) {
     __shared__ double tot[NACC];
-    const int t = threadIdx.x;
-    if (t < NACC) {
-        double s = 0.0;
-        for (int c = 0; c < nclusters; ++c) s += partials[size_t(c) * NACC + t];
-        tot[t] = s;
-    }
+    const int t = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    double s = 0.0;
+    for (int c = lane; c < nclusters; c += 32) s += partials[size_t(c) * NACC + t];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) tot[t] = s;
     __syncthreads();
-    if (t != 0) return;
+    if (threadIdx.x != 0) return;
     double o[16];
     for (int i = 0; i < 16; ++i) o[i] = 0.0;
     const double n = double(*n_valid);
@@ -656,7 +660,7 @@ int headloss_forward_backward_ext(headloss_t h, const void* logits, int64_t N, i
     fa.w_grpo = h->w.grpo;
     fa.w_ent = h->w.entropy;
     fa.divisor = x.divisor;
-    finalize_kernel<<<1, 32, 0, s>>>(h->partials, ncl, h->n_valid, fa, scalars_out);
+    finalize_kernel<<<1, 32 * NACC, 0, s>>>(h->partials, ncl, h->n_valid, fa, scalars_out);
     if (cudaGetLastError() != cudaSuccess) return HEADLOSS_ERR_CUDA;
     return HEADLOSS_OK;
 }
