@@ -12,7 +12,10 @@
 //   - softcap: z = s*c*tanh(x/c) lies in [-s*c, s*c], so the student needs no
 //     max (the shift is s*c); tanh comes from an odd polynomial on the FMA
 //     pipe when the slice's |x| / c stays within its fitted range, else from
-//     tanh(y) = 1 - 2 / (exp(2y) + 1) (ex2 + rcp);
+//     w = exp(-2|y|): |tanh| = (1 - w) / (1 + w) (ex2 + rcp);
+//   - pass C takes each exponential at an offset of 2^sg with its coefficient
+//     scaled by 2^-sg (shift_coefs), so gradients in bf16's subnormal range
+//     survive ex2's flush to zero;
 //   - 16-byte words wholly inside the slice take the packed path; only the
 //     (at most two) partial words at a ragged slice edge take a scalar path;
 //   - after the cluster exchange warp 0 merges the C partial records (C lanes
@@ -279,8 +282,7 @@ __device__ RowCoef row_epilogue16(const Params& p, const float* recs, int C, boo
 }
 
 // The body of the resident kernel (one instantiation per feature set and
-// accumulation mode); the two entry points below differ only in their
-// register budget.
+// accumulation mode), called by the kernel entry below.
 template <typename DT, int FEAT, bool ACC>
 __device__ __forceinline__ void rows_body16(const Params& p) {
     using P16 = Pack16<DT>;
