@@ -7,8 +7,11 @@ count, or a function of means), so the global value follows from one
 all-reduce of per-rank sums, second moments and counts.
 
 Gradients: the library normalises each rank's gradient by its own valid-row
-count.  For the gradient of the global mean instead, give every rank
-grad_scale * n_valid_local / n_valid_global (see `global_grad_scale`).
+count.  For the gradient of the global mean instead, either give every rank
+grad_scale * n_valid_local / n_valid_global (see `global_grad_scale`), or
+pass the global count as the call's divisor (headloss_forward_backward_ext;
+see `global_divisor`): then each rank's gradient is already its share of the
+global mean and its loss slots are partial sums that `sum_loss_slots` adds.
 """
 from __future__ import annotations
 
@@ -54,3 +57,26 @@ def global_grad_scale(n_valid_local: int, grad_scale: float = 1.0, group=None) -
     dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
     total = float(t.item())
     return grad_scale * (n_valid_local / total) if total > 0 else 0.0
+
+
+# loss slots: partial sums over the global divisor when every rank passes it
+LOSS_SLOTS = (TOTAL, CE, Z, DIST_CE, FKL, RKL, GRPO, ENTROPY)
+
+
+def global_divisor(labels: torch.Tensor, V: int, group=None) -> float:
+    """The batch's valid-row count over all ranks (0 <= label < V), by one
+    all-reduce: the divisor every rank passes to headloss_forward_backward_ext."""
+    n = ((labels >= 0) & (labels < V)).sum().to(torch.float64).reshape(1).cpu()
+    dist.all_reduce(n, op=dist.ReduceOp.SUM, group=group)
+    return float(n.item())
+
+
+def sum_loss_slots(scalars: torch.Tensor, group=None) -> torch.Tensor:
+    """Global loss slots (fp64, 16; metric slots zero) from this rank's scalars
+    of a call made with the global divisor: the loss slots add across ranks."""
+    s = scalars.detach().to(torch.float64).reshape(16)
+    v = torch.zeros(16, dtype=torch.float64, device=s.device)
+    for i in LOSS_SLOTS:
+        v[i] = s[i]
+    dist.all_reduce(v, op=dist.ReduceOp.SUM, group=group)
+    return v

@@ -79,3 +79,54 @@ def test_two_gloo_ranks_combine_to_the_whole_batch():
     # each rank's rescaled gradient is its half of the whole batch's gradient
     g = np.concatenate([results[0][2], results[1][2]])
     assert np.allclose(g, g_ref, rtol=1e-12, atol=1e-15)
+
+
+def _rank_divisor(rank, world, port, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from gradient_row_online_gb300.distributed import global_divisor, sum_loss_slots
+        x, labels, t, old, adv = _problem()
+        half = slice(rank * 20, (rank + 1) * 20)
+        D = global_divisor(torch.from_numpy(labels[half]), x.shape[1])
+        cfg = orc.make_cfg(ALL, W, temperature=1.5, clip_eps=0.2, grad_scale=1.0)
+        # what a call with divisor D writes: the oracle's per-row records of this
+        # rank's rows, with the gradient normalised by D
+        rec, g, _ = orc.rows(cfg, x[half], labels[half], t[half], old[half], adv[half], int(D),
+                             True, False)
+        valid = rec[:, orc.RF["valid"]] > 0
+        loss = {1: "ce", 2: "z", 3: "dist_ce", 4: "fkl", 5: "rkl", 6: "grpo", 13: "entropy"}
+        s = np.zeros(16)
+        for slot, field in loss.items():
+            s[slot] = rec[valid, orc.RF[field]].sum() / D
+        s[0] = sum(W[f] * s[slot] for slot, f in loss.items())
+        q.put((rank, D, sum_loss_slots(torch.from_numpy(s)).numpy(), g))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_with_the_global_divisor():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_divisor, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    results = [q.get(timeout=120) for _ in range(2)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    results.sort(key=lambda r: r[0])
+    x, labels, t, old, adv = _problem()
+    cfg = orc.make_cfg(ALL, W, temperature=1.5, clip_eps=0.2, grad_scale=1.0)
+    ref, _, g_ref, _ = orc.forward_backward(cfg, x, labels, t, old, adv)
+    n_total = float(((labels >= 0) & (labels < x.shape[1])).sum())
+    for rank, D, sums, _ in results:
+        assert D == n_total
+        for slot in (0, 1, 2, 3, 4, 5, 6, 13):
+            assert np.isclose(sums[slot], ref[slot], rtol=1e-12, atol=1e-12), (slot, sums, ref)
+    # each rank's gradient rows are the whole batch's gradient rows, unscaled
+    g = np.concatenate([results[0][3], results[1][3]])
+    assert np.allclose(g, g_ref, rtol=1e-12, atol=1e-15)
+
