@@ -3,18 +3,25 @@
 // One CTA owns whole rows; no cluster, so no CTA ever waits for another SM.
 // A row is streamed through a ring of shared-memory chunk slots twice:
 //
-//   pass 1  chunks 0 .. K-1: online row statistics.  Each thread keeps its
-//           own shifts (student: s*c*log2e under softcap, else a lazily
-//           raised running maximum; teacher: a lazily raised running
-//           maximum) and rescales its sums only when a chunk's maximum
-//           rises more than TAU above the shift, which after the first
-//           chunk almost never happens;
-//   merge   the thread records merge across the warp (butterfly), then across
-//           the CTA's warps, and warp 0 derives the row's losses and gradient
-//           coefficients (the same epilogue as the resident kernel);
+//   pass 1  chunks 0 .. K-1: online row statistics.  Each warp keeps one
+//           shift per operand for all its lanes (student: s*c*log2e under
+//           softcap, else a lazily raised running maximum; teacher: a lazily
+//           raised running maximum) and rescales its sums only when a
+//           chunk's maximum rises more than TAU above the shift, which after
+//           the first chunk almost never happens;
+//   merge   with warp-uniform shifts a warp's record is a plain butterfly
+//           sum; warp 0 merges the warps' records and derives the row's
+//           losses and gradient coefficients (the resident kernel's epilogue);
 //   pass 2  chunks K-1 .. 0 (reverse order, so the chunks read most recently
 //           -- the ones most likely still in L2 -- come back first): the
 //           combined gradient, written once from registers.
+//
+// Full chunks in the narrow softcap tier (or without softcap) take a hot
+// path: four words per thread, unrolled, no per-word predicate, no tier
+// dispatch.  Partial chunks and the wider tiers take a rolled cold path.  The
+// label column's logit is read once per row from global memory, and its
+// gradient element is patched after the row's last chunk by the thread that
+// wrote its word.
 //
 // Softcap transform, per (warp, chunk): zs = s*c*log2e*tanh(x/c) is x * Q(x^2)
 // with the scale folded into the polynomial Q when the chunk's max |x| / c is
