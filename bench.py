@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import glob
 import json
 import os
@@ -74,11 +75,19 @@ def peaks():
 
 
 def kernel_source_hash():
+    """Hash of the kernel sources' code (comments and blank lines stripped, so
+    an edit to a comment does not mark recorded counters stale)."""
     h = hashlib.sha256()
     for fn in sorted(glob.glob(os.path.join(ROOT, "gradient_row_online_gb300", "csrc", "*"))):
-        with open(fn, "rb") as f:
-            h.update(os.path.basename(fn).encode())
-            h.update(f.read())
+        if not fn.endswith((".cu", ".cuh", ".h")):
+            continue
+        with open(fn) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        code = "\n".join(l.rstrip() for l in src.splitlines() if l.strip())
+        h.update(os.path.basename(fn).encode())
+        h.update(code.encode())
     return h.hexdigest()[:16]
 
 
