@@ -30,6 +30,8 @@ CASES = [
      dict(kernel=RESIDENT, cluster=2, stages=1, threads=256)),
     (("ce", "z", "entropy"), torch.float16, 15.0, None),
     (("ce", "grpo", "grpo_stats", "dist_ce", "rkl", "entropy"), torch.float32, 20.0, None),
+    (("ce", "z", "fkl", "rkl", "entropy"), torch.float16, 30.0,
+     dict(kernel=STREAM, stages=2, threads=512, chunk_words=1)),
 ]
 
 

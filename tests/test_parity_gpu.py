@@ -123,6 +123,19 @@ def test_stream_structured_rows(softcap, scale, V):
         structured_check(wl, plan=plan)
 
 
+# fp16 rows through the streaming kernel: its own unpack and packed abs-max,
+# every softcap tier, teacher and reverse KL
+@pytest.mark.parametrize("softcap,scale", [(0.0, 0.7), (30.0, 0.5), (10.0, 1.0)])
+def test_stream_structured_rows_fp16(softcap, scale):
+    plan = dict(kernel=STREAM, stages=3, threads=256, chunk_words=1)
+    wl = small(ALL_LOSSES, N=24, V=4104, dtype=torch.float16, softcap=softcap,
+               logits_scale=scale, weights=dict(FULL_W, entropy=0.0))
+    structured_check(wl, plan=plan)
+    full_check(small(ALL_LOSSES, N=23, V=20008, dtype=torch.float16, softcap=softcap,
+                     logits_scale=scale), plan=dict(kernel=STREAM, stages=3, threads=256,
+                                                    chunk_words=4))
+
+
 @pytest.mark.parametrize("softcap,scale", [(0.0, 1.0), (30.0, 0.5), (15.0, 1.3)])
 def test_stream_structured_rows_default_plan(softcap, scale):
     wl = small(ALL_LOSSES, N=40, V=128256, softcap=softcap, logits_scale=scale,
