@@ -25,8 +25,13 @@ const void* stream_kernel_fp16_acc(int feat);
 
 // Valid rows of the call (0 <= label < V); a label >= V raises E_LABEL.
 // One block: the count is an exact integer whatever the order.
+// It also stores the gradient factor grad_scale / (divisor, else the count)
+// once for the row kernels, as an fp32 quotient (fp64 division is slow here
+// and this kernel runs ahead of the row kernel).
 __global__ void __launch_bounds__(1024) count_valid_kernel(const int64_t* labels, int64_t N,
-                                                           int64_t V, long long* out, int* err) {
+                                                           int64_t V, long long* out, int* err,
+                                                           float grad_scale, double divisor,
+                                                           float* kscale) {
     __shared__ long long part[32];
     long long c = 0;
     int bad = 0;
@@ -47,6 +52,8 @@ __global__ void __launch_bounds__(1024) count_valid_kernel(const int64_t* labels
         long long tot = 0;
         for (int w = 0; w < int(blockDim.x >> 5); ++w) tot += part[w];
         *out = tot;
+        const float den = divisor > 0.0 ? float(divisor) : float(tot);
+        *kscale = den > 0.f ? __fdiv_rn(grad_scale, den) : 0.f;
     }
 }
 
@@ -80,25 +87,28 @@ __global__ void __launch_bounds__(32 * NACC) finalize_kernel(const double* parti
     const double nl = a.divisor > 0.0 ? a.divisor : n;  // loss slots
     o[HEADLOSS_SLOT_N_VALID] = n;
     if (n > 0.0) {
+        // one fp64 division per normaliser (each is slow on this GPU), then
+        // products: the fp32 outputs see no difference
+        const double rn = 1.0 / n, rnl = a.divisor > 0.0 ? 1.0 / nl : rn;
         const uint32_t f = a.flags;
-        if (f & L_CE) o[HEADLOSS_SLOT_CE] = tot[A_CE] / nl;
-        if (f & L_Z) o[HEADLOSS_SLOT_Z] = tot[A_Z] / nl;
-        if (f & L_DIST_CE) o[HEADLOSS_SLOT_DIST_CE] = tot[A_DCE] / nl;
-        if (f & L_FKL) o[HEADLOSS_SLOT_FKL] = tot[A_FKL] / nl;
-        if (f & L_RKL) o[HEADLOSS_SLOT_RKL] = tot[A_RKL] / nl;
-        if (f & L_GRPO) o[HEADLOSS_SLOT_GRPO] = tot[A_GRPO] / nl;
+        if (f & L_CE) o[HEADLOSS_SLOT_CE] = tot[A_CE] * rnl;
+        if (f & L_Z) o[HEADLOSS_SLOT_Z] = tot[A_Z] * rnl;
+        if (f & L_DIST_CE) o[HEADLOSS_SLOT_DIST_CE] = tot[A_DCE] * rnl;
+        if (f & L_FKL) o[HEADLOSS_SLOT_FKL] = tot[A_FKL] * rnl;
+        if (f & L_RKL) o[HEADLOSS_SLOT_RKL] = tot[A_RKL] * rnl;
+        if (f & L_GRPO) o[HEADLOSS_SLOT_GRPO] = tot[A_GRPO] * rnl;
         if (f & L_GRPO_STATS) {
-            o[HEADLOSS_SLOT_NEW_LOGPROB] = tot[A_LP] / n;
-            o[HEADLOSS_SLOT_RATIO] = tot[A_RATIO] / n;
-            o[HEADLOSS_SLOT_CLIP_FRAC] = tot[A_NCLIP] / n;
-            o[HEADLOSS_SLOT_KL_K3] = tot[A_KL3] / n;
-            const double am = tot[A_ADV] / n;
-            const double var = tot[A_ADV2] / n - am * am;
+            o[HEADLOSS_SLOT_NEW_LOGPROB] = tot[A_LP] * rn;
+            o[HEADLOSS_SLOT_RATIO] = tot[A_RATIO] * rn;
+            o[HEADLOSS_SLOT_CLIP_FRAC] = tot[A_NCLIP] * rn;
+            o[HEADLOSS_SLOT_KL_K3] = tot[A_KL3] * rn;
+            const double am = tot[A_ADV] * rn;
+            const double var = tot[A_ADV2] * rn - am * am;
             o[HEADLOSS_SLOT_ADV_MEAN] = am;
             o[HEADLOSS_SLOT_ADV_STD] = var > 0.0 ? sqrt(var) : 0.0;
             o[HEADLOSS_SLOT_N_CLIPPED] = tot[A_NCLIP];
         }
-        if (f & L_ENTROPY) o[HEADLOSS_SLOT_ENTROPY] = tot[A_ENT] / nl;
+        if (f & L_ENTROPY) o[HEADLOSS_SLOT_ENTROPY] = tot[A_ENT] * rnl;
         double total = 0.0;
         if (f & L_CE) total += double(a.w_ce) * o[HEADLOSS_SLOT_CE];
         if (f & L_Z) total += double(a.w_z) * o[HEADLOSS_SLOT_Z];
@@ -141,6 +151,7 @@ struct headloss {
     double* partials;
     int partials_cap;  // clusters (resident) or CTAs (streaming)
     long long* n_valid;
+    float* kscale;  // 8 bytes after n_valid
     int* err;
     headloss_plan_desc forced;  // zero fields: the planner decides
     Plan plan;                  // cache of the last plan
@@ -483,6 +494,7 @@ int headloss_create(uint32_t flags, const headloss_weights* w, float temperature
     }
     h->partials = static_cast<double*>(h->ws);
     h->n_valid = reinterpret_cast<long long*>(static_cast<char*>(h->ws) + pbytes);
+    h->kscale = reinterpret_cast<float*>(static_cast<char*>(h->ws) + pbytes + 8);
     h->err = reinterpret_cast<int*>(static_cast<char*>(h->ws) + pbytes + 64);
     if (cudaMemset(h->ws, 0, pbytes + 256) != cudaSuccess) {
         cudaFree(h->ws);
@@ -594,7 +606,8 @@ int headloss_forward_backward_ext(headloss_t h, const void* logits, int64_t N, i
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-    count_valid_kernel<<<1, 1024, 0, s>>>(labels, N, V, h->n_valid, h->err);
+    count_valid_kernel<<<1, 1024, 0, s>>>(labels, N, V, h->n_valid, h->err, h->w.grad_scale,
+                                          x.divisor, h->kscale);
 
     int ncl = 0;
     if (N > 0) {
@@ -627,6 +640,7 @@ int headloss_forward_backward_ext(headloss_t h, const void* logits, int64_t N, i
         p.grad_scale = h->w.grad_scale;
         p.partials = h->partials;
         p.n_valid = h->n_valid;
+        p.kscale = h->kscale;
         p.err = h->err;
         p.wait_ns = h->wait_ns;
         p.drop_row = h->drop_row;
@@ -783,6 +797,7 @@ extern "C" int headloss_forward_backward_noalloc(
     h.partials = static_cast<double*>(scratch);
     h.partials_cap = NOALLOC_MAX_SLOTS < 4 * sms ? NOALLOC_MAX_SLOTS : 4 * sms;
     h.n_valid = reinterpret_cast<long long*>(static_cast<char*>(scratch) + NOALLOC_PARTIAL_BYTES);
+    h.kscale = reinterpret_cast<float*>(static_cast<char*>(scratch) + NOALLOC_PARTIAL_BYTES + 8);
     h.err = reinterpret_cast<int*>(static_cast<char*>(scratch) + NOALLOC_PARTIAL_BYTES + 64);
     h.forced = headloss_plan_desc{0, 0, 0, 0, 0};
     if (N > 0) {

@@ -63,6 +63,7 @@ struct Params {
     float w_ce, w_z, w_dce, w_fkl, w_rkl, w_grpo, w_ent, grad_scale;
     double* partials;              // [clusters][NACC]
     const long long* n_valid;      // valid-row count of this call
+    const float* kscale;           // grad_scale / (divisor or valid-row count), set by the count kernel
     int* err;                      // device error word
     unsigned long long wait_ns;    // limit of every mbarrier wait (~2 s)
     int64_t drop_row;              // fault-injection builds only: row whose copy is skipped (-1: none)

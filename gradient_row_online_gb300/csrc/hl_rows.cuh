@@ -230,8 +230,9 @@ struct DTraits<float> {
 // Shared-memory bytes beyond the stage buffers (mbarriers, exchange records,
 // reduction scratch, row coefficients), for an accumulator of `acc_bytes`.
 __host__ __device__ constexpr int smem_fixed_bytes(int acc_bytes) {
+    // the last 32 words: a row's coefficients, then its losses waiting to be summed
     return 8 * MAX_STAGES + 8 * NACC +
-           acc_bytes * (2 * MAX_CLUSTER * NREC + NWARPS * NREC + 2 * NWARPS + 16) +
+           acc_bytes * (2 * MAX_CLUSTER * NREC + NWARPS * NREC + 2 * NWARPS + 32) +
            4 * MAX_STAGES;
 }
 

@@ -62,6 +62,11 @@ __device__ __forceinline__ TanhD2 tanh_poly2(f2 y) {
 struct RowCoef {
     float lse2, lseT2, lsq2, pc, ps, tc, ts, qc, bc;
 };
+// The 32-word coefficient area of both row kernels' shared memory: a row's
+// RowCoef at word 0, its RowLoss (waiting to be summed) at word 16; the
+// streaming kernel keeps the call's grad_scale / n at KK_SLOT (read from
+// global memory once per CTA).
+constexpr int KK_SLOT = 31;
 
 // The gradient pass takes each exponential as 2^(arg + sg) and scales its
 // coefficient by 2^-sg, so terms whose exponential lies below fp32's normal
@@ -108,39 +113,69 @@ __device__ __forceinline__ void write_row_zero(const Params& p, int64_t row) {
     if (p.rl_out) p.rl_out[row] = 0.f;
 }
 
-// Adds one row's loss values to the CTA's fp64 sums and writes its per-token
+// The CTA's running sums of row values: fp32 with a Kahan compensation term
+// per slot (acc[i] the sum, acc[NACC + i] the compensation), so the error
+// stays at a few fp32 roundings however many rows a CTA takes.  fp64 would be
+// exact enough without compensation, but fp64 arithmetic is slow on this GPU
+// and a row's sums sit on the path between its two passes.  The counts are
+// integers, exact in fp32 up to 2^24 rows per CTA.
+__device__ __forceinline__ void kahan_add(float* acc, int i, float x) {
+    const float y = __fsub_rn(x, acc[NACC + i]);
+    const float t = __fadd_rn(acc[i], y);
+    acc[NACC + i] = __fsub_rn(__fsub_rn(t, acc[i]), y);
+    acc[i] = t;
+}
+// Writes a CTA's sums to its fp64 partial slots (sum minus compensation).
+__device__ __forceinline__ void store_partials(const float* acc, double* out) {
+#pragma unroll
+    for (int i = 0; i < NACC; ++i) out[i] = double(acc[i]) - double(acc[NACC + i]);
+}
+
+// Adds one row's loss values to the CTA's sums and writes its per-token
 // outputs (fused, so no value outlives the row's epilogue any longer than the
 // sums need it).
-__device__ __forceinline__ void row_accumulate(const Params& p, const RowLoss& rl, double* acc,
+__device__ __forceinline__ void row_accumulate(const Params& p, const RowLoss& rl, float* acc,
                                                int64_t row) {
     const uint32_t f = p.flags;
     float t = 0.f;
-    acc[A_NVALID] += 1.0;
-    if (f & L_CE) { acc[A_CE] += double(rl.ce); t = fmaf(p.w_ce, rl.ce, t); }
-    if (f & L_Z) { const double z = double(rl.lse) * double(rl.lse); acc[A_Z] += z; t = fmaf(p.w_z, float(z), t); }
-    if (f & L_DIST_CE) { acc[A_DCE] += double(rl.dce); t = fmaf(p.w_dce, rl.dce, t); }
-    if (f & L_FKL) { acc[A_FKL] += double(rl.fkl); t = fmaf(p.w_fkl, rl.fkl, t); }
-    if (f & L_RKL) { acc[A_RKL] += double(rl.rkl); t = fmaf(p.w_rkl, rl.rkl, t); }
-    if (f & L_GRPO) { acc[A_GRPO] += double(rl.grpo); t = fmaf(p.w_grpo, rl.grpo, t); }
+    acc[A_NVALID] += 1.f;
+    if (f & L_CE) { kahan_add(acc, A_CE, rl.ce); t = fmaf(p.w_ce, rl.ce, t); }
+    if (f & L_Z) { const float z = rl.lse * rl.lse; kahan_add(acc, A_Z, z); t = fmaf(p.w_z, z, t); }
+    if (f & L_DIST_CE) { kahan_add(acc, A_DCE, rl.dce); t = fmaf(p.w_dce, rl.dce, t); }
+    if (f & L_FKL) { kahan_add(acc, A_FKL, rl.fkl); t = fmaf(p.w_fkl, rl.fkl, t); }
+    if (f & L_RKL) { kahan_add(acc, A_RKL, rl.rkl); t = fmaf(p.w_rkl, rl.rkl, t); }
+    if (f & L_GRPO) { kahan_add(acc, A_GRPO, rl.grpo); t = fmaf(p.w_grpo, rl.grpo, t); }
     if (f & L_GRPO_STATS) {
-        acc[A_LP] += double(rl.lp);
-        acc[A_RATIO] += double(rl.rho);
-        acc[A_KL3] += double(rl.kl3);
-        acc[A_ADV] += double(rl.adv);
-        acc[A_ADV2] += double(rl.adv) * double(rl.adv);
-        acc[A_NCLIP] += double(rl.clipped);
+        kahan_add(acc, A_LP, rl.lp);
+        kahan_add(acc, A_RATIO, rl.rho);
+        kahan_add(acc, A_KL3, rl.kl3);
+        kahan_add(acc, A_ADV, rl.adv);
+        kahan_add(acc, A_ADV2, rl.adv * rl.adv);
+        acc[A_NCLIP] += rl.clipped;
     }
-    if (f & L_ENTROPY) { acc[A_ENT] += double(rl.H); t = fmaf(p.w_ent, rl.H, t); }
+    if (f & L_ENTROPY) { kahan_add(acc, A_ENT, rl.H); t = fmaf(p.w_ent, rl.H, t); }
     if (p.lp_out) p.lp_out[row] = rl.lp;
     if (p.rl_out) p.rl_out[row] = t;
 }
 
 // A warp merges the C records of a row (lane k holds record k) and derives
-// the row's gradient coefficients (identical in every lane); with
-// `accumulate` its lane 0 also adds the row's losses to the CTA's partial sums.
-template <bool TEACH, bool RKL, bool ENT, bool CAP>
+// the row's gradient coefficients (lane 0's result defines the row).  With
+// `accumulate` its lane 0 also adds the row's losses to the CTA's partial
+// sums; with `defer` non-null lane 0 stores them there instead, for the
+// caller to add once the coefficients are out.  kk = grad_scale / n comes
+// from the caller (read once per CTA).  This sits between the two passes
+// with the CTA's other warps waiting.  FAST takes the logs, exponentials and
+// reciprocals as one MUFU op each (lse to ~2^-21 relative, far inside the
+// 16-bit outputs' rounding); measured, that pays in the streaming kernel,
+// while the resident kernel, whose co-resident CTAs keep the MUFU pipe busy,
+// is faster with the library functions.
+template <bool TEACH, bool RKL, bool ENT, bool CAP, bool FAST>
 __device__ RowCoef row_epilogue16(const Params& p, const float* recs, int C, bool accumulate,
-                                  float old_lp, float adv, double* acc, int lane, int64_t row) {
+                                  float old_lp, float adv, float* acc, int lane, int64_t row,
+                                  float kk, RowLoss* defer = nullptr) {
+    auto lg2_ = [](float v) { return FAST ? lg2f(v) : log2f(v); };
+    auto ex2_ = [](float v) { return FAST ? ex2f(v) : exp2f(v); };
+    auto div_ = [](float a, float b) { return FAST ? a * rcpf(b) : a / b; };
     const float LN2 = 0.6931471805599453f;
     const float invT = 1.f / p.T;
     float r[NREC];
@@ -150,22 +185,24 @@ __device__ RowCoef row_epilogue16(const Params& p, const float* recs, int C, boo
     const bool live = have && r[R_S] > 0.f;
     float M = live ? r[R_ZM] : -CUDART_INF_F;
     float Mu = (live && TEACH) ? r[R_UM] : -CUDART_INF_F;
+    // butterfly levels below C only: lanes 0 .. C-1 (lane 0 included) see all records
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {  // every lane needs the row max: reduce over all 32
+    for (int o = 16; o; o >>= 1) {
+        if (o >= C) continue;
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         if (TEACH) Mu = fmaxf(Mu, __shfl_xor_sync(0xffffffffu, Mu, o));
     }
     float c[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // S E ST Sq Eq Xp Y zy
     if (live) {
         const float d = r[R_ZM] - M;
-        const float al = exp2f(d);
+        const float al = ex2_(d);
         c[0] = al * r[R_S];
         if (ENT) c[1] = al * (r[R_E] + d * r[R_S]);
         if (TEACH) {
             const float dT = d * invT;
-            const float alT = exp2f(dT);
+            const float alT = ex2_(dT);
             const float du = r[R_UM] - Mu;
-            const float be = exp2f(du);
+            const float be = ex2_(du);
             c[2] = alT * r[R_ST];
             c[3] = be * r[R_SQ];
             c[4] = be * (r[R_EQ] + du * r[R_SQ]);
@@ -175,29 +212,27 @@ __device__ RowCoef row_epilogue16(const Params& p, const float* recs, int C, boo
     }
     if (have && r[R_HASY] > 0.f) c[7] = r[R_ZY];
 #pragma unroll
-    for (int o = 16; o; o >>= 1)  // up to 32 records (one per warp of a streaming CTA)
+    for (int o = 16; o; o >>= 1) {  // up to 32 records (one per warp of a streaming CTA)
+        if (o >= C) continue;
 #pragma unroll
         for (int i = 0; i < 8; ++i) c[i] += __shfl_xor_sync(0xffffffffu, c[i], o);
-    // lane 0's sums (a fixed order) define the row for the whole warp
-#pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = __shfl_sync(0xffffffffu, c[i], 0);
+    }
 
     const float S = c[0], E = c[1], ST = c[2], Sq = c[3], Eq = c[4], Xp = c[5], Y = c[6];
     const float zy = c[7];
     const uint32_t f = p.flags;
-    const float lS = log2f(S);
+    const float lS = lg2_(S);
     const float lse2 = M + lS;
     const float lse = lse2 * LN2;
-    const float kk =
-        float(double(p.grad_scale) / (p.divisor > 0.0 ? p.divisor : double(*p.n_valid)));
     float H = 0.f, lST = 0.f, lSq = 0.f, dce = 0.f, fkl = 0.f, rkl = 0.f;
-    if (ENT) H = LN2 * (lS - E / S);
+    if (ENT) H = LN2 * (lS - div_(E, S));
     if (TEACH) {
-        lST = log2f(ST);
-        lSq = log2f(Sq);
-        fkl = LN2 * (Xp / Sq - lSq + lST);
-        dce = LN2 * (Xp / Sq + lST - Eq / Sq);
-        if (RKL) rkl = LN2 * (Y / ST - lST + lSq);
+        lST = lg2_(ST);
+        lSq = lg2_(Sq);
+        const float xq = div_(Xp, Sq);
+        fkl = LN2 * (xq - lSq + lST);
+        dce = LN2 * (xq + lST - div_(Eq, Sq));
+        if (RKL) rkl = LN2 * (div_(Y, ST) - lST + lSq);
     }
     RowCoef k{};
     float pc = 0.f, ps = 0.f, tc = 0.f, ts = 0.f, qc = 0.f, bc = 0.f;
@@ -212,7 +247,7 @@ __device__ RowCoef row_epilogue16(const Params& p, const float* recs, int C, boo
         const float eps = p.eps;
         lp = (zy - lse2) * LN2;
         const float lr = lp - old_lp;
-        rho = expf(lr);
+        rho = FAST ? ex2f(lr * 1.4426950408889634f) : expf(lr);
         float rho_c = rho < 1.f - eps ? 1.f - eps : rho;
         rho_c = rho_c > 1.f + eps ? 1.f + eps : rho_c;
         const float unc = rho * adv, clp = rho_c * adv;
@@ -262,7 +297,7 @@ __device__ RowCoef row_epilogue16(const Params& p, const float* recs, int C, boo
     k.ts = ts;
     k.qc = qc;
     k.bc = bc;
-    if (lane == 0 && accumulate) {
+    if (lane == 0 && (accumulate || defer)) {
         RowLoss rl;
         rl.ce = (lse2 - zy) * LN2;
         rl.lse = lse;
@@ -276,7 +311,8 @@ __device__ RowCoef row_epilogue16(const Params& p, const float* recs, int C, boo
         rl.adv = adv;
         rl.clipped = clipped ? 1.f : 0.f;
         rl.H = H;
-        row_accumulate(p, rl, acc, row);
+        if (defer) *defer = rl;
+        else row_accumulate(p, rl, acc, row);
     }
     return k;
 }
@@ -301,8 +337,8 @@ __device__ __forceinline__ void rows_body16(const Params& p) {
     const uint32_t opbytes = uint32_t(W) * 16u;
     const uint32_t stage_bytes = opbytes * OPS;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(stage_bytes) * p.nbuf);
-    double* acc = reinterpret_cast<double*>(bars + MAX_STAGES);  // [NACC], rank 0 only
-    float* xch = reinterpret_cast<float*>(acc + NACC);         // [2][MAX_CLUSTER][NREC]
+    float* acc = reinterpret_cast<float*>(bars + MAX_STAGES);  // [2][NACC], rank 0 only
+    float* xch = acc + 2 * NACC;                               // [2][MAX_CLUSTER][NREC]
     float* red = xch + 2 * MAX_CLUSTER * NREC;                   // [NWARPS][NREC]: sums
     float* redmax = red + NWARPS * NREC;                         // [NWARPS][2]: maxima
     float* coefs = redmax + 2 * NWARPS;                          // RowCoef of the row
@@ -350,8 +386,11 @@ __device__ __forceinline__ void rows_body16(const Params& p) {
     if (tid == 0) {
         for (int b = 0; b < p.nbuf; ++b) mbar_init(smem_addr(&bars[b]), 1);
         fence_mbar_init();
-        for (int i = 0; i < NACC; ++i) acc[i] = 0.0;
+        for (int i = 0; i < 2 * NACC; ++i) acc[i] = 0.f;
     }
+    // grad_scale / n, read once; held in a register (measured faster here
+    // than a shared-memory read per row)
+    const float kk = *p.kscale;
     __syncthreads();
     if (C > 1) cluster_barrier();  // every peer has started before any DSMEM store
 
@@ -599,13 +638,18 @@ __device__ __forceinline__ void rows_body16(const Params& p) {
             }
             if (C > 1) cluster_barrier();
             else __syncwarp();
+            // rank 0's row losses wait in shared memory and are added once the
+            // coefficients are out
+            RowLoss* rls = reinterpret_cast<RowLoss*>(coefs + 16);
             if (warp == 0) {
-                const RowCoef kw = row_epilogue16<TEACH, RKL, ENT, CAP>(
-                    p, xrec, C, rank == 0, old_lp, adv, acc, lane, r);
+                const RowCoef kw = row_epilogue16<TEACH, RKL, ENT, CAP, false>(
+                    p, xrec, C, false, old_lp, adv, acc, lane, r, kk,
+                    rank == 0 ? rls : nullptr);
                 if (lane == 0) *reinterpret_cast<RowCoef*>(coefs) = kw;
             }
             ++xc;
             __syncthreads();
+            if (rank == 0 && tid == 0) row_accumulate(p, *rls, acc, r);
             const RowCoef k = *reinterpret_cast<const RowCoef*>(coefs);
 
             // ---- pass C: the combined gradient, written once ----
@@ -760,9 +804,7 @@ __device__ __forceinline__ void rows_body16(const Params& p) {
             if (lost & (1u << b)) (void)mbar_wait_bounded(smem_addr(&bars[b]), (lost_par >> b) & 1u, p.wait_ns);
     }
     if (rank == 0 && tid == 0) {
-        double* out = p.partials + size_t(cid) * NACC;
-#pragma unroll
-        for (int i = 0; i < NACC; ++i) out[i] = acc[i];
+        store_partials(acc, p.partials + size_t(cid) * NACC);
     }
     if (C > 1) cluster_barrier();
 }

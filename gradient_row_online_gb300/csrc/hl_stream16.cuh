@@ -82,12 +82,15 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
     const uint32_t opbytes = uint32_t(CH) * ES;
     const uint32_t slot_bytes = opbytes * OPS;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(slot_bytes) * S);
-    double* acc = reinterpret_cast<double*>(bars + MAX_STAGES);
-    float* xch = reinterpret_cast<float*>(acc + NACC);  // per-warp records of a row
+    float* acc = reinterpret_cast<float*>(bars + MAX_STAGES);  // [2][NACC]: sums, compensations
+    float* xch = acc + 2 * NACC;                                // per-warp records of a row
     float* red = xch + 2 * MAX_CLUSTER * NREC;
     float* redmax = red + NWARPS * NREC;
     float* coefs = redmax + 2 * NWARPS;
-    int* done = reinterpret_cast<int*>(coefs + 16);     // [MAX_STAGES] warps finished per slot
+    RowLoss* rls = reinterpret_cast<RowLoss*>(coefs + 16);  // a row's losses, summed after the merge
+    int* done = reinterpret_cast<int*>(coefs + 32);     // [MAX_STAGES] warps finished per slot
+    static_assert(sizeof(RowCoef) <= 16 * sizeof(float) && sizeof(RowLoss) <= 16 * sizeof(float),
+                  "coefficient / row-loss areas");
 
     const int64_t N = p.N, V = p.V;
     const int K = int((V + CH - 1) / CH);                // chunks per row
@@ -224,7 +227,8 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             done[b] = 0;
         }
         fence_mbar_init();
-        for (int i = 0; i < NACC; ++i) acc[i] = 0.0;
+        for (int i = 0; i < 2 * NACC; ++i) acc[i] = 0.f;
+        coefs[KK_SLOT] = *p.kscale;
 #pragma unroll
         for (int i = 0; i < 6; ++i) rare[i] = QB[i];
         rare[6] = A22;
@@ -278,15 +282,48 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
     const bool need_side = (p.flags & (L_GRPO | L_GRPO_STATS)) != 0;
     const int WPT = CH / (EPW * nthr);  // words per thread per chunk (full chunks)
 
+    // A row's side inputs (label, old log-prob, advantage) are staged a row
+    // ahead, per warp, in shared memory after the rare constants: lane 0
+    // loads the next row's during the merge and stores them after it, so a
+    // row starts on a shared-memory read instead of a global load.
+    struct Side {
+        int64_t y;
+        float o, a;
+    };
+    static_assert(16 + (2 + 2) * NWARPS <= NWARPS * NREC, "side-input stash");
+    int64_t* ystash = reinterpret_cast<int64_t*>(red + 16);     // [NWARPS]
+    float* sstash = reinterpret_cast<float*>(ystash + NWARPS);  // [NWARPS][2]
+    auto side_load = [&](int64_t rn) -> Side {
+        Side sd{0, 0.f, 0.f};
+        if (rn < N) {
+            if (has_labels) sd.y = p.labels[rn];
+            if (need_side) {
+                sd.o = p.old_lp[rn];
+                sd.a = p.adv[rn];
+            }
+        }
+        return sd;
+    };
+    auto side_store = [&](const Side& sd) {
+        ystash[warp] = sd.y;
+        sstash[2 * warp] = sd.o;
+        sstash[2 * warp + 1] = sd.a;
+    };
+    if (lane == 0) side_store(side_load(blockIdx.x));
+
     for (int64_t r = blockIdx.x; r < N; r += G) {
-        const int64_t y = has_labels ? p.labels[r] : 0;
-        const float old_lp = need_side ? p.old_lp[r] : 0.f;
-        const float adv = need_side ? p.adv[r] : 0.f;
+        __syncwarp();
+        const int64_t y = ystash[warp];
+        const float old_lp = sstash[2 * warp];
+        const float adv = sstash[2 * warp + 1];
+        __syncwarp();
         const bool valid = !has_labels || (y >= 0 && y < V);
         if (has_labels && y >= V && tid == 0) atomicOr(p.err, E_LABEL);
 
         if (!valid) {  // a masked row: consume its entries, write exact +0
             if (tid == 0) write_row_zero(p, r);
+            Side nxt{};
+            if (lane == 0) nxt = side_load(r + G);
             for (int jl = 0; jl < K2x; ++jl) {
                 acquire();
                 const int cc = jl < K ? jl : K2x - 1 - jl;
@@ -299,6 +336,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                 }
                 release(r, jl);
             }
+            if (lane == 0) side_store(nxt);
             continue;
         }
 
@@ -479,6 +517,8 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         const float hasy = (has_labels && tid == 0) ? 1.f : 0.f;
 
         // ---------------- merge: threads -> warps -> row ----------------
+        Side nxt{};
+        if (lane == 0) nxt = side_load(r + G);  // stored after the merge
         // the shifts are warp-uniform, so a warp's record is a plain sum
         float v[9] = {hsum(S2), hsum(E2), hsum(ST2), hsum(Sq2), hsum(Eq2), hsum(Xp2),
                       -hsum(Y2), zy, hasy};
@@ -507,12 +547,16 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             rec[R_HASY] = v[8];
         }
         __syncthreads();
+        // the row's losses wait in shared memory and are added once the
+        // coefficients are out
         if (warp == 0) {
-            const RowCoef kw =
-                row_epilogue16<TEACH, RKL, ENT, CAP>(p, xch, nwarps, true, old_lp, adv, acc, lane, r);
+            const RowCoef kw = row_epilogue16<TEACH, RKL, ENT, CAP, true>(
+                p, xch, nwarps, false, old_lp, adv, acc, lane, r, coefs[KK_SLOT], rls);
             if (lane == 0) *reinterpret_cast<RowCoef*>(coefs) = kw;
         }
         __syncthreads();
+        if (lane == 0) side_store(nxt);
+        if (tid == 0) row_accumulate(p, *rls, acc, r);
         const RowCoef k = *reinterpret_cast<const RowCoef*>(coefs);
 
         // ---------------- pass 2: the gradient, reverse chunk order ----------------
@@ -651,9 +695,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             if (lost & (1u << b)) (void)mbar_wait_bounded(smem_addr(&bars[b]), (lost_par >> b) & 1u, p.wait_ns);
     }
     if (tid == 0) {
-        double* out = p.partials + size_t(blockIdx.x) * NACC;
-#pragma unroll
-        for (int i = 0; i < NACC; ++i) out[i] = acc[i];
+        store_partials(acc, p.partials + size_t(blockIdx.x) * NACC);
     }
 }
 
