@@ -146,3 +146,22 @@ def forward_backward(cfg: _Cfg, x, labels=None, teacher=None, old_logprobs=None,
     rec, grad, gmag = rows(cfg, x, labels, teacher, old_logprobs, advantages, None, want_grad,
                            want_gmag, n_threads)
     return reduce(cfg, rec), rec, grad, gmag
+
+
+def lm_head_forward_backward(cfg: _Cfg, hidden, weight, labels=None, teacher=None,
+                             old_logprobs=None, advantages=None, n_threads: int = 0):
+    """The LM head in front of the loss, written out plainly: logits = hidden @ weight^T
+    (fp64), the loss of ``forward_backward`` on those logits, and the gradients of
+    grad_scale * total with respect to hidden (N x D) and weight (V x D) by the chain
+    rule through the linear map (dH = G @ weight, dW = G^T @ hidden, G the logits
+    gradient).  The teacher enters as logits, as in ``forward_backward``.
+
+    Returns (scalars[16], per-row records, dH, dW, logits, G)."""
+    h = _f64(hidden)
+    w = _f64(weight)
+    if h.ndim != 2 or w.ndim != 2 or h.shape[1] != w.shape[1]:
+        raise ValueError("hidden is N x D and weight is V x D")
+    x = h @ w.T
+    scalars, rec, g, _ = forward_backward(cfg, x, labels, teacher, old_logprobs, advantages,
+                                          want_grad=True, n_threads=n_threads)
+    return scalars, rec, g @ w, g.T @ h, x, g

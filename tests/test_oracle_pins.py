@@ -348,3 +348,85 @@ def test_rejects_missing_inputs():
         orc.forward_backward(orc.make_cfg(orc.GRPO), x, np.zeros(2, np.int64))
     with pytest.raises(ValueError):
         orc.forward_backward(orc.make_cfg(orc.CE), x, np.array([0, 4], np.int64))
+
+
+# ------------------------------------------------- LM head in front of the loss
+
+def _lm_head_problem(seed, n=3, D=4, V=5):
+    rng = np.random.default_rng(300 + seed)
+    hid = rng.normal(0.0, 1.0, (n, D))
+    wt = rng.normal(0.0, 0.8, (V, D))
+    labels = rng.integers(0, V, n).astype(np.int64)
+    labels[1] = -100
+    t = hid @ wt.T + rng.normal(0.0, 1.0, (n, V))
+    adv = rng.normal(0.0, 1.0, n)
+    x = hid @ wt.T
+    lp = _torch_lp(0.8 * 4.0 * np.tanh(x / 4.0), labels)
+    while True:  # old log-probs away from the clip kinks
+        old = lp + rng.normal(0, 0.3, n)
+        lr = lp - old
+        if np.all(np.abs(np.abs(lr) - np.log(1.2)) > 0.02) and np.all(
+                np.abs(lr - np.log(0.8)) > 0.02):
+            break
+    return hid, wt, labels, t, old, adv
+
+
+@pytest.mark.parametrize("flags", [orc.CE | orc.Z, orc.FKL | orc.RKL | orc.DIST_CE,
+                                   orc.GRPO | orc.GRPO_STATS | orc.ENTROPY, ALL])
+def test_lm_head_gradients_match_finite_differences(flags):
+    """dH and dW against central differences of grad_scale * total in every entry
+    of hidden and weight (a transposed or misplaced matmul operand fails)."""
+    hid, wt, labels, t, old, adv = _lm_head_problem(0)
+    cfg = orc.make_cfg(flags, dict(ce=0.9, z=0.3, dist_ce=0.4, fkl=0.6, rkl=0.7, grpo=1.1,
+                                   entropy=0.5),
+                       temperature=1.7, clip_eps=0.2, softcap=4.0, logits_scale=0.8,
+                       grad_scale=1.3)
+    _, _, dH, dW, _, _ = orc.lm_head_forward_backward(cfg, hid, wt, labels, t, old, adv)
+
+    def loss(hh, ww):
+        x = hh @ ww.T
+        return 1.3 * orc.forward_backward(cfg, x, labels, t, old, adv, want_grad=False)[0][0]
+
+    step = 1e-5
+    for a, d in ((hid, dH), (wt, dW)):
+        fd = np.zeros_like(a)
+        for idx in np.ndindex(*a.shape):
+            ap = a.copy(); ap[idx] += step
+            am = a.copy(); am[idx] -= step
+            args_p = (ap, wt) if a is hid else (hid, ap)
+            args_m = (am, wt) if a is hid else (hid, am)
+            fd[idx] = (loss(*args_p) - loss(*args_m)) / (2 * step)
+        assert np.abs(fd - d).max() < 1e-8 * max(1.0, np.abs(d).max()), (flags, a.shape)
+
+
+def test_lm_head_with_identity_weight_is_the_row_loss():
+    """weight = I (D = V): the logits are the hidden states, dH is the logits
+    gradient and dW = G^T hidden."""
+    rng = np.random.default_rng(7)
+    n, V = 4, 6
+    x, labels, t, adv = _rand_problem(rng, n, V)
+    old = rng.normal(-2.0, 0.5, n)
+    cfg = orc.make_cfg(ALL, dict(z=0.2, dist_ce=0.3, fkl=0.4, rkl=0.5, entropy=0.1),
+                       temperature=1.3, softcap=5.0, logits_scale=0.7)
+    s, rec, dH, dW, logits, g = orc.lm_head_forward_backward(cfg, x, np.eye(V), labels, t,
+                                                             old, adv)
+    s2, rec2, g2, _ = orc.forward_backward(cfg, x, labels, t, old, adv)
+    np.testing.assert_array_equal(logits, x)
+    np.testing.assert_array_equal(s, s2)
+    np.testing.assert_array_equal(dH, g2)
+    np.testing.assert_allclose(dW, g2.T @ x, rtol=0, atol=0)
+
+
+def test_lm_head_scaling_identities():
+    """Scaling the weight by a: d/da total(H, aW) at a = 1 equals sum(dW * W) and
+    equals sum(dH * H) (both are the derivative along the logits themselves)."""
+    hid, wt, labels, t, old, adv = _lm_head_problem(1, n=4, D=3, V=7)
+    cfg = orc.make_cfg(orc.CE | orc.Z | orc.FKL | orc.ENTROPY,
+                       dict(z=0.1, fkl=0.5, entropy=0.2), temperature=1.5)
+    _, _, dH, dW, _, _ = orc.lm_head_forward_backward(cfg, hid, wt, labels, t, old, adv)
+    step = 1e-6
+    tot = lambda a: orc.forward_backward(cfg, hid @ (a * wt).T, labels, t, old, adv,
+                                         want_grad=False)[0][0]
+    dda = (tot(1 + step) - tot(1 - step)) / (2 * step)
+    assert abs(dda - np.sum(dW * wt)) < 1e-7 * max(1.0, abs(dda))
+    assert abs(dda - np.sum(dH * hid)) < 1e-7 * max(1.0, abs(dda))
