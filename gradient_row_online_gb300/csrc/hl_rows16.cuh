@@ -102,8 +102,8 @@ __device__ __forceinline__ ShiftCoef shift_coefs(const RowCoef& k, bool entg) {
     return o;
 }
 
-// One row's loss values (natural-log units), added to the CTA's fp64 sums by
-// row_accumulate.
+// One row's loss values (natural-log units), added to the CTA's compensated
+// fp32 sums by row_accumulate.
 struct RowLoss {
     float ce, lse, dce, fkl, rkl, grpo, lp, rho, kl3, adv, clipped, H;
 };
