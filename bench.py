@@ -122,10 +122,12 @@ class ClockSampler:
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, interval_ms=100):
         self.gpu = gpu_index
+        self.interval_ms = interval_ms
         self.proc = None
         self.path = None
+        self.start_at = 0  # file offset where the timed region's samples begin
 
     def __enter__(self):
         try:
@@ -135,8 +137,16 @@ class ClockSampler:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.out,
-                stderr=subprocess.DEVNULL)
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+            # wait (at most 3 s) for the first sample, so that the samples
+            # counted are the ones taken while the timed region runs
+            deadline = time.time() + 3.0
+            while time.time() < deadline and self.proc.poll() is None:
+                if os.path.getsize(self.path) > 0:
+                    break
+                time.sleep(0.005)
+            self.start_at = os.path.getsize(self.path)
         except Exception:
             self.proc = None
         return self
@@ -153,26 +163,35 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or not self.path:
             return None
-        sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            for line in f:
+
+        def parse(lines):
+            out = []
+            for line in lines:
                 parts = [p.strip() for p in line.split(",")]
                 if len(parts) < 9:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
+                    sm, mx = float(parts[1]), float(parts[2])
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
+                out.append((sm, mx, {n for n, v in zip(names, parts[5:9])
+                                     if v.lower() == "active"}))
+            return out
+
+        with open(self.path) as f:
+            text = f.read()
         os.unlink(self.path)
-        if not sm:
+        inside = parse(text[self.start_at:].splitlines())
+        # a region shorter than the sampling interval may hold no sample: then
+        # the last one taken before it stands in, and "samples" says 0
+        use = inside or parse(text[:self.start_at].splitlines())[-1:]
+        if not use:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(u[0] for u in use),
+                "sm_max_mhz": max(u[1] for u in use),
+                "reasons": sorted(set().union(*(u[2] for u in use))),
+                "samples": len(inside), "interval_ms": self.interval_ms}
 
 
 # ------------------------------------------------------------- our arm

@@ -58,3 +58,43 @@ def test_library_arm_fails_loudly_without_a_gpu():
     r = _run(["bench.py", "--workload", "tiny_ce_z_fp32", "--steps", "1", "--warmup", "3"])
     assert r.returncode != 0
     assert r.stdout.strip() == ""
+
+
+def _fake_smi(tmp_path, body):
+    d = tmp_path / "bin"
+    d.mkdir()
+    f = d / "nvidia-smi"
+    f.write_text("#!/bin/bash\n" + body)
+    f.chmod(0o755)
+    return str(d)
+
+
+def test_clock_sampler_counts_only_samples_inside_the_timed_region(tmp_path, monkeypatch):
+    """The sampler waits for nvidia-smi's first line before the region starts,
+    so that line (taken before the region) is not counted; throttle reasons
+    seen inside the region are reported."""
+    import time
+    sys.path.insert(0, ROOT)
+    import bench
+    d = _fake_smi(tmp_path, (
+        "sleep 0.2\n"
+        "echo '0, 1200, 2070, 500.0, 0x0, Active, Not Active, Not Active, Not Active'\n"
+        "sleep 0.1\n"
+        "echo '0, 2070, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active'\n"
+        "sleep 10\n"))
+    monkeypatch.setenv("PATH", d + os.pathsep + os.environ["PATH"])
+    with bench.ClockSampler(0) as c:
+        time.sleep(0.4)
+    s = c.summary()
+    assert s["samples"] == 1 and s["sm_mhz"] == 2070.0 and s["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_sampler_without_nvidia_smi_reports_nothing(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    empty = tmp_path / "empty"
+    empty.mkdir()
+    monkeypatch.setenv("PATH", str(empty))
+    with bench.ClockSampler(0) as c:
+        pass
+    assert c.summary() is None
