@@ -75,11 +75,14 @@ def peaks():
 
 
 def kernel_source_hash():
-    """Hash of the kernel sources' code (comments and blank lines stripped, so
-    an edit to a comment does not mark recorded counters stale)."""
+    """Hash of the loss kernels' sources (hl_* and headloss_* files, comments
+    and blank lines stripped, so an edit to a comment does not mark recorded
+    counters stale; the LM-head GEMM's source is not part of the loss path)."""
     h = hashlib.sha256()
     for fn in sorted(glob.glob(os.path.join(ROOT, "gradient_row_online_gb300", "csrc", "*"))):
         if not fn.endswith((".cu", ".cuh", ".h")):
+            continue
+        if not os.path.basename(fn).startswith(("hl_", "headloss_")):
             continue
         with open(fn) as f:
             src = f.read()

@@ -45,11 +45,12 @@ SLOTS = ("total", "ce", "z", "dist_ce", "fkl", "rkl", "grpo_loss", "new_logprob_
          "ratio_mean", "clip_frac", "kl_k3", "adv_mean", "adv_std", "entropy_mean", "n_valid",
          "n_clipped")
 
-# Every function declared in include/headloss.h.
+# Every function declared in include/headloss.h and include/headloss_lmhead.h.
 EXPORTS = ("headloss_create", "headloss_forward_backward", "headloss_get_device_error",
            "headloss_plan", "headloss_force_plan", "headloss_launches_per_call",
            "headloss_destroy", "headloss_strerror", "headloss_version",
-           "headloss_forward_backward_noalloc", "headloss_forward_backward_ext")
+           "headloss_forward_backward_noalloc", "headloss_forward_backward_ext",
+           "headloss_lmhead_logits")
 
 
 # enum headloss_kernel
@@ -121,6 +122,8 @@ def load_library(path: str = LIB_PATH):
     lib.headloss_forward_backward_ext.argtypes = [vp, vp, i64, i64, i32, vp, vp, vp, vp, vp, vp,
                                                   ctypes.POINTER(headloss_call_ext), vp]
     lib.headloss_forward_backward_ext.restype = i32
+    lib.headloss_lmhead_logits.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp]
+    lib.headloss_lmhead_logits.restype = i32
     _lib = lib
     return lib
 
@@ -221,6 +224,15 @@ def headloss_forward_backward_noalloc(flags, weights, temperature, clip_eps, sof
         flags, w, temperature, clip_eps, softcap, logits_scale, _ptr(logits), int(N), int(V),
         int(dtype), _ptr(labels), _ptr(teacher_logits), _ptr(old_logprobs), _ptr(advantages),
         _ptr(grad_out), _ptr(scalars_out), _stream(stream)), "headloss_forward_backward_noalloc")
+
+
+def headloss_lmhead_logits(hidden, weight, N, D, V, logits, stats, err, stream=None) -> None:
+    """logits = hidden . weight^T and per-(row, 256-column tile) (max, sum exp)
+    statistics (include/headloss_lmhead.h); raises HeadlossError on a bad status."""
+    _check(load_library().headloss_lmhead_logits(_ptr(hidden), _ptr(weight), int(N), int(D),
+                                                 int(V), _ptr(logits), _ptr(stats), _ptr(err),
+                                                 _stream(stream)),
+           "headloss_lmhead_logits")
 
 
 def headloss_get_device_error(h, stream=None) -> int:

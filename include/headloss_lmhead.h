@@ -1,0 +1,53 @@
+/*
+ * headloss_lmhead.h -- the LM-head GEMM in front of the loss (C ABI).
+ *
+ * The monolithic head loss consumes the logits of the language-model head,
+ * logits = hidden . weight^T (ServiceNow Fast-LLM PR #549, "Correctness":
+ * the LM head and tied embeddings are among the axes the head loss is
+ * validated on).  This call computes that GEMM on the GB300's 5th-generation
+ * tensor cores and, in the same pass, the per-row softmax statistics of each
+ * 256-column tile of its output -- the statistics a loss's first pass would
+ * otherwise read the logits back to compute.  It is the first building block
+ * of a fused LM head; the loss calls of headloss.h do not use it yet.
+ *
+ * Status codes are those of headloss.h.
+ */
+#ifndef HEADLOSS_LMHEAD_H
+#define HEADLOSS_LMHEAD_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * headloss_lmhead_logits -- logits and per-tile row statistics.
+ *
+ * hidden:  N x D bf16, row-major, device, 16-byte aligned base.
+ * weight:  V x D bf16, row-major, device, 16-byte aligned base (one row per
+ *          vocabulary entry).
+ * N, D, V: N a multiple of 128, V a multiple of 256, D a multiple of 64.
+ * logits:  N x V bf16, row-major, device, 16-byte aligned (written):
+ *          the fp32 sum over D of hidden[i, :] * weight[j, :], rounded once
+ *          to bf16 (round to nearest even).
+ * stats:   N x (V / 256) pairs of fp32, device (written): for row i and
+ *          column tile k, (m, s) with m = max over the tile's 256 bf16
+ *          logits and s = sum of exp(logit - m) over them.  The row's
+ *          log-sum-exp is m* + log(sum_k s_k * exp(m_k - m*)), m* = max_k m_k.
+ * err:     one int in device memory, zeroed by the caller: bit 0 is set if a
+ *          wait inside the kernel gave up (a copy or an MMA never completed);
+ *          the outputs are then unreliable.
+ * stream:  cudaStream_t (NULL = legacy default stream).  Asynchronous.
+ *
+ * Returns HEADLOSS_OK, HEADLOSS_ERR_ARG (a size not a multiple above, or a
+ * null pointer), HEADLOSS_ERR_ALIGN (a base not 16-byte aligned) or
+ * HEADLOSS_ERR_CUDA (tensor-map encoding or launch failed).  The caller owns
+ * every buffer; the call allocates nothing.
+ */
+int headloss_lmhead_logits(const void* hidden, const void* weight, int N, int D, int V,
+                           void* logits, void* stats, int* err, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HEADLOSS_LMHEAD_H */

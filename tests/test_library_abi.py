@@ -68,3 +68,18 @@ def test_missing_library_fails_loudly(tmp_path):
 
 def test_build_targets_sm_103a_only():
     assert B.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_lmhead_rejects_bad_arguments_before_any_work(lib):
+    """Sizes off the tile grid, null pointers and unaligned bases are refused
+    on the host (no GPU needed)."""
+    ok = 1 << 12  # a 16-byte aligned fake address; never dereferenced here
+    f = lib.headloss_lmhead_logits
+    assert f(ok, ok, 100, 64, 256, ok, ok, ok, None) == hlb.HEADLOSS_ERR_ARG   # N % 128
+    assert f(ok, ok, 128, 60, 256, ok, ok, ok, None) == hlb.HEADLOSS_ERR_ARG   # D % 64
+    assert f(ok, ok, 128, 64, 300, ok, ok, ok, None) == hlb.HEADLOSS_ERR_ARG   # V % 256
+    assert f(None, ok, 128, 64, 256, ok, ok, ok, None) == hlb.HEADLOSS_ERR_ARG
+    assert f(ok, ok, 128, 64, 256, ok, ok, None, None) == hlb.HEADLOSS_ERR_ARG
+    assert f(ok + 2, ok, 128, 64, 256, ok, ok, ok, None) == hlb.HEADLOSS_ERR_ALIGN
+    assert f(ok, ok, 128, 64, 256, ok + 8, ok, ok, None) == hlb.HEADLOSS_ERR_ALIGN
+
