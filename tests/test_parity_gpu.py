@@ -158,6 +158,19 @@ def test_stream_every_loss_subset():
         full_check(small(losses, N=17, V=4104, seed=len(losses)), plan=plan)
 
 
+# the gradient written over the logits by the streaming kernel (its second
+# pass re-reads each chunk from global memory while it stores gradients over
+# the row, and patches the label column last), with a teacher, softcap and a
+# partial last chunk
+@pytest.mark.parametrize("words", [1, 4])
+def test_stream_in_place(words):
+    plan = dict(kernel=STREAM, stages=3, threads=256, chunk_words=words)
+    full_check(small(ALL_LOSSES, N=23, V=20008, softcap=30.0, logits_scale=0.5), plan=plan,
+               inplace=True)
+    full_check(small(("ce", "z", "grpo", "grpo_stats", "entropy"), N=23, V=20008), plan=plan,
+               inplace=True)
+
+
 def test_large_logits_fp32():
     wl = small(("ce", "z", "entropy", "fkl", "rkl"), N=8, V=513, dtype=torch.float32,
                sigma=1e4)
