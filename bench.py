@@ -52,6 +52,10 @@ def parse():
     ap.add_argument("--no-loss-sets", action="store_true")
     ap.add_argument("--no-per-loss", action="store_true",
                     help="skip the per-loss-loop comparison")
+    ap.add_argument("--no-lmhead", action="store_true",
+                    help="skip the LM-head GEMM leg (tensor cores, beside torch.matmul)")
+    ap.add_argument("--lmhead-shape", default="8192,4096,128256",
+                    help="N,D,V of the LM-head GEMM leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall time the CPU-baseline sample is sized for")
     return ap.parse_args()
@@ -72,6 +76,19 @@ def peaks():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def tensor_peak():
+    """Dense bf16 tensor throughput (TFLOP/s) for a kernel timed alone: the
+    measured burst figure, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def kernel_source_hash():
@@ -320,6 +337,8 @@ def run_ours(args, rank, world, local):
         line["loss_sets"] = loss_sets(args, dev, exclude=wl.name, peak=peak)
     if not args.no_per_loss and world == 1:
         line["per_loss_loop"] = per_loss_loop(wl, inp, grad, dev)
+    if not args.no_lmhead and world == 1:
+        line["lm_head_gemm"] = lm_head_gemm(args, dev)
     if not args.no_e2e:
         del grad
         line["e2e"] = e2e(wl, h, inp, args, dev, world)
@@ -414,6 +433,44 @@ def per_loss_loop(wl, inp, grad, dev, steps=5):
     return {"workload": wl.name, "losses": list(wl.losses), "fused_ms": ms_fused,
             "per_loss_ms": ms_loop, "speedup": ms_loop / ms_fused, "calls_in_loop": len(calls),
             "gradient_writes_in_loop": n_bearing}
+
+
+def lm_head_gemm(args, dev, steps=10):
+    """The LM-head GEMM in front of the loss (tcgen05, TMEM, TMA) with its
+    per-tile row statistics, timed beside torch.matmul (cuBLAS) on the same
+    bf16 operands; tensor-pipe roofline against the measured bf16 peak."""
+    from gradient_row_online_gb300 import headloss as hlb
+
+    N, D, V = (int(v) for v in args.lmhead_shape.split(","))
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    hid = (torch.randn(N, D, generator=g, device=dev) * 0.5).to(torch.bfloat16)
+    wt = (torch.randn(V, D, generator=g, device=dev) * (1.0 / D) ** 0.5).to(torch.bfloat16)
+    out = torch.empty(N, V, dtype=torch.bfloat16, device=dev)
+    st = torch.empty(N, V // 256, 2, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    s = torch.cuda.current_stream(dev)
+    ours = lambda: hlb.headloss_lmhead_logits(hid, wt, N, D, V, out, st, err, s)
+    ref = lambda: torch.matmul(hid, wt.T)
+    for fn in (ours, ref, ours, ref, ours, ref):
+        fn()
+    ms = statistics.mean(time_calls(ours, s, steps))
+    ms_ref = statistics.mean(time_calls(ref, s, steps))
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError("LM-head GEMM: a bounded wait gave up")
+    flops = 2.0 * N * D * V
+    peak, kind = tensor_peak()
+    tf = flops / (ms / 1e3) / 1e12
+    res = {"shape": {"N": N, "D": D, "V": V}, "ms": ms, "tflops": tf,
+           "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                        "frac": tf / peak, "peak_kind": kind + " (bf16 burst)"},
+           "torch_matmul_ms": ms_ref, "torch_matmul_tflops": flops / (ms_ref / 1e3) / 1e12,
+           "vs_torch": ms_ref / ms,
+           "outputs": "bf16 logits + per-(row, 256-column tile) fp32 (max, sum exp)"}
+    del hid, wt, out, st
+    torch.cuda.empty_cache()
+    return res
 
 
 def e2e(wl, h, inp, args, dev, world):

@@ -29,17 +29,24 @@ extern "C" {
  * logits:  N x V bf16, row-major, device, 16-byte aligned (written):
  *          the fp32 sum over D of hidden[i, :] * weight[j, :], rounded once
  *          to bf16 (round to nearest even).
- * stats:   N x (V / 256) pairs of fp32, device (written): for row i and
+ * stats:   N x (V / 256) pairs of fp32, device, 8-byte aligned (written): for row i and
  *          column tile k, (m, s) with m = max over the tile's 256 bf16
  *          logits and s = sum of exp(logit - m) over them.  The row's
  *          log-sum-exp is m* + log(sum_k s_k * exp(m_k - m*)), m* = max_k m_k.
- * err:     one int in device memory, zeroed by the caller: bit 0 is set if a
- *          wait inside the kernel gave up (a copy or an MMA never completed);
- *          the outputs are then unreliable.
+ * err:     one int in device memory (4-byte aligned), zeroed by the caller:
+ *          bit 0 is set if a wait inside the kernel gave up (a copy or an MMA
+ *          did not complete within ~2 s); the kernel then stops issuing work,
+ *          waits for what it issued, and the outputs are unreliable.
  * stream:  cudaStream_t (NULL = legacy default stream).  Asynchronous.
  *
+ * The kernel is persistent (one CTA per SM over the 128 x 256 output
+ * tiles): tcgen05.mma on bf16 operands staged by TMA, fp32 accumulation in
+ * two TMEM accumulators (one tile's epilogue overlaps the next tile's MMAs),
+ * logits written by TMA stores from shared memory.
+ *
  * Returns HEADLOSS_OK, HEADLOSS_ERR_ARG (a size not a multiple above, or a
- * null pointer), HEADLOSS_ERR_ALIGN (a base not 16-byte aligned) or
+ * null pointer), HEADLOSS_ERR_ALIGN (a base not 16-byte aligned, stats not
+ * 8-byte or err not 4-byte aligned) or
  * HEADLOSS_ERR_CUDA (tensor-map encoding or launch failed).  The caller owns
  * every buffer; the call allocates nothing.
  */
