@@ -357,7 +357,7 @@ def loss_sets(args, dev, exclude, peak):
     from gradient_row_online_gb300 import workloads as W
 
     res = {}
-    for name in W.ORDER[1:]:
+    for name in W.ORDER[1:] + W.EXTRA:
         if name == exclude:
             continue
         wl = W.WORKLOADS[name]
@@ -473,6 +473,42 @@ def lm_head_gemm(args, dev, steps=10):
     return res
 
 
+def host_link_bandwidth(dev, gib=2, reps=3):
+    """Pinned host <-> device copy bandwidth of this machine (GB/s), one direction
+    at a time and both at once, best of `reps` copies of `gib` GiB."""
+    n = gib << 30
+    hb = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    hb2 = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    db = torch.empty(n, dtype=torch.uint8, device=dev)
+    db2 = torch.empty(n, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            best = min(best, time.perf_counter() - t0)
+        return best
+
+    def both():
+        with torch.cuda.stream(s1):
+            db.copy_(hb, non_blocking=True)
+        with torch.cuda.stream(s2):
+            hb2.copy_(db2, non_blocking=True)
+
+    t_h2d = timed(lambda: db.copy_(hb, non_blocking=True))
+    t_d2h = timed(lambda: hb2.copy_(db2, non_blocking=True))
+    t_both = timed(both)
+    del hb, hb2, db, db2
+    torch.cuda.empty_cache()
+    return {"h2d_gbs": n / t_h2d / 1e9, "d2h_gbs": n / t_d2h / 1e9,
+            "both_directions_gbs": 2 * n / t_both / 1e9,
+            "how": f"pinned {gib} GiB copies, best of {reps}, wall clock around a synchronize"}
+
+
 def e2e(wl, h, inp, args, dev, world):
     """The same metric through the public call with pinned HOST buffers: every
     step copies its inputs host->device and reads its gradient and scalars
@@ -526,6 +562,7 @@ def e2e(wl, h, inp, args, dev, world):
             out_done[b].record(s_out)
         used[b] = True
 
+    link = host_link_bandwidth(dev)
     step(0)
     step(1)
     torch.cuda.synchronize()
@@ -540,9 +577,14 @@ def e2e(wl, h, inp, args, dev, world):
     torch.cuda.synchronize()
     total = t0.elapsed_time(t1)
     del dsets[1], d_grad, h_grad
+    # the host link bounds a step at its copies: host-to-device and
+    # device-to-host run on separate copy engines and overlap
+    bound_ms = 1e3 * max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9))
     return {"value": wl.N * world * n / (total / 1e3), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
-            "ms_per_step": total / n, "pipelined": "2 buffer sets, copy-in / compute / copy-out streams"}
+            "ms_per_step": total / n, "pipelined": "2 buffer sets, copy-in / compute / copy-out streams",
+            "link": link, "link_bound_ms_per_step": bound_ms,
+            "frac_of_link_bound": bound_ms / (total / n)}
 
 
 def cpu_seconds(wl, x, lab, t, old, adv, n_valid, threads):

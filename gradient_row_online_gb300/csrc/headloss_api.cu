@@ -133,7 +133,7 @@ constexpr int kLaunchesPerCall = 3;
 
 struct Plan {
     int64_t V = -1;
-    int dtype = -1, feat = -1;
+    int dtype = -1, feat = -1, inplace = -1;
     int kind = 0;  // HEADLOSS_KERNEL_RESIDENT or HEADLOSS_KERNEL_STREAM
     int C = 0, nbuf = 0, words = 0, smem = 0, ncl = 0, threads = 0, chunk_words = 0;
     int64_t L = 0;
@@ -390,15 +390,20 @@ bool pick_stream(const headloss* h, const Plan* cand, int ncand, Plan* best) {
 // student-only (its second read, partly from DRAM, costs more than the
 // resident kernel's barriers).  So: streaming for 16-bit rows with a teacher
 // whose resident plan needs three or more CTAs per row; resident otherwise.
-int make_plan(headloss* h, int64_t V, int dtype, Plan* out, int acc = 0) {
+// A call whose gradient overwrites its logits (in place) always takes the
+// resident kernel: it reads each row once into shared memory before any of
+// the row's gradient is stored, while the streaming kernel reads the row a
+// second time from global memory as it stores the gradient.
+int make_plan(headloss* h, int64_t V, int dtype, Plan* out, int acc = 0, int inplace = 0) {
     const int feat = feature_set(h) | (acc ? int(F_ACC) : 0);
-    if (h->plan.V == V && h->plan.dtype == dtype && h->plan.feat == feat) {
+    if (h->plan.V == V && h->plan.dtype == dtype && h->plan.feat == feat &&
+        h->plan.inplace == inplace) {
         *out = h->plan;
         return HEADLOSS_OK;
     }
     Plan cand[2 * MAX_CLUSTER * 2 * MAX_STAGES + 2 * 3 * MAX_STAGES];
     int ncand = 0;
-    const int fk = h->forced.kernel;
+    const int fk = inplace ? int(HEADLOSS_KERNEL_RESIDENT) : h->forced.kernel;
     int rc = HEADLOSS_OK;
     if (fk == 0 || fk == HEADLOSS_KERNEL_RESIDENT)
         rc = resident_candidates(h, V, dtype, feat, cand, &ncand);
@@ -424,6 +429,7 @@ int make_plan(headloss* h, int64_t V, int dtype, Plan* out, int acc = 0) {
     best.V = V;
     best.dtype = dtype;
     best.feat = feat;
+    best.inplace = inplace;
     h->plan = best;
     *out = best;
     return HEADLOSS_OK;
@@ -556,13 +562,12 @@ int headloss_forward_backward(headloss_t h, const void* logits, int64_t N, int64
                                          nullptr, stream);
 }
 
-int headloss_forward_backward_ext(headloss_t h, const void* logits, int64_t N, int64_t V,
-                                  int dtype, const int64_t* labels, const void* teacher_logits,
-                                  const float* old_logprobs, const float* advantages,
-                                  void* grad_out, float* scalars_out,
-                                  const headloss_call_ext* ext, headloss_stream_t stream) {
-    headloss_call_ext x = {nullptr, nullptr, 0, 0.0};
-    if (ext) x = *ext;
+// Host-side checks of a call (no device work): the argument, alignment and
+// missing-input errors of headloss_forward_backward_ext, in its order.
+static int check_call(const headloss* h, const void* logits, int64_t N, int64_t V, int dtype,
+                      const int64_t* labels, const void* teacher_logits,
+                      const float* old_logprobs, const float* advantages, const void* grad_out,
+                      const float* scalars_out, const headloss_call_ext& x) {
     if (!h || !scalars_out || N < 0 || V < 1 || V >= (int64_t(1) << 31)) return HEADLOSS_ERR_ARG;
     if (!(x.divisor >= 0.0) || !isfinite(x.divisor)) return HEADLOSS_ERR_ARG;
     if (x.accumulate != 0 && x.accumulate != 1) return HEADLOSS_ERR_ARG;
@@ -597,12 +602,36 @@ int headloss_forward_backward_ext(headloss_t h, const void* logits, int64_t N, i
         const int64_t bytes = N * V * elem_size(dtype);
         if (g0 < x0 + bytes && x0 < g0 + bytes) return HEADLOSS_ERR_ARG;
     }
+    return HEADLOSS_OK;
+}
+
+int headloss_forward_backward_ext(headloss_t h, const void* logits, int64_t N, int64_t V,
+                                  int dtype, const int64_t* labels, const void* teacher_logits,
+                                  const float* old_logprobs, const float* advantages,
+                                  void* grad_out, float* scalars_out,
+                                  const headloss_call_ext* ext, headloss_stream_t stream) {
+    headloss_call_ext x = {nullptr, nullptr, 0, 0.0};
+    if (ext) x = *ext;
+    {
+        const int rc = check_call(h, logits, N, V, dtype, labels, teacher_logits, old_logprobs,
+                                  advantages, grad_out, scalars_out, x);
+        if (rc) return rc;
+    }
+    const uint32_t f = h->flags;
+    const bool teach = (f & (L_DIST_CE | L_FKL | L_RKL)) != 0;
     std::lock_guard<std::mutex> g(h->mu);
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return HEADLOSS_ERR_CUDA;
     if (dev != h->device) return HEADLOSS_ERR_ARG;
     Plan pl;
-    const int rc = make_plan(h, V, dtype, &pl, x.accumulate);
+    int inplace = 0;  // the gradient overlaps the logits
+    if (grad_out && N > 0) {
+        const char* g0 = static_cast<const char*>(grad_out);
+        const char* x0 = static_cast<const char*>(logits);
+        const int64_t bytes = N * V * elem_size(dtype);
+        inplace = (g0 < x0 + bytes && x0 < g0 + bytes) ? 1 : 0;
+    }
+    const int rc = make_plan(h, V, dtype, &pl, x.accumulate, inplace);
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
@@ -800,6 +829,13 @@ extern "C" int headloss_forward_backward_noalloc(
     h.kscale = reinterpret_cast<float*>(static_cast<char*>(scratch) + NOALLOC_PARTIAL_BYTES + 8);
     h.err = reinterpret_cast<int*>(static_cast<char*>(scratch) + NOALLOC_PARTIAL_BYTES + 64);
     h.forced = headloss_plan_desc{0, 0, 0, 0, 0};
+    // the call's own argument checks first: a rejected call enqueues nothing
+    {
+        const headloss_call_ext none = {nullptr, nullptr, 0, 0.0};
+        const int crc = check_call(&h, logits, N, V, dtype, labels, teacher_logits, old_logprobs,
+                                   advantages, grad_out, scalars_out, none);
+        if (crc) return crc;
+    }
     if (N > 0) {
         Plan pl;
         {

@@ -547,11 +547,6 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             rec[R_HASY] = v[8];
         }
         __syncthreads();
-        // the label logit as read before any gradient store of this row (the
-        // gradient may overwrite the logits in place), for the label patch;
-        // written after the barrier, which every thread passes only once it
-        // has finished the previous row's patch
-        if (has_labels && tid == 0) *reinterpret_cast<volatile uint32_t*>(coefs + 12) = xy_bits;
         // the row's losses wait in shared memory and are added once the
         // coefficients are out
         if (warp == 0) {
@@ -660,17 +655,15 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
             release(r, K2x - 1 - c);
         }
         // the label column: the thread whose word held it recomputes that one
-        // element with the label term (the logit saved at the merge, the
-        // teacher re-read from global memory) and overwrites it; program order
-        // puts this store after its word store
+        // element with the label term (inputs re-read from global memory) and
+        // overwrites it; program order puts this store after its word store
         if (yown && gg != nullptr) {
             // the coefficients again from shared memory (no register carries them
             // through the chunk loop; they stay until the next row's merge)
             const RowCoef k = *reinterpret_cast<const RowCoef*>(coefs);
             const ShiftCoef h = shift_coefs(k, ENTG);
             const float dlse = k.lseT2 - k.lsq2;
-            const float xv1 =
-                P16::to_f(uint16_t(*reinterpret_cast<volatile uint32_t*>(coefs + 12)));
+            const float xv1 = P16::to_f(reinterpret_cast<const uint16_t*>(xg)[r * V + y]);
             float zs, om1 = 1.f;
             if (CAP) zs = __fmul_rn(tanh_a2x_1(__fmul_rn(xv1, A2), &om1), Kc);
             else zs = __fmul_rn(xv1, K1);

@@ -91,9 +91,15 @@ WORKLOADS = {
         ("ce", "z", "fkl", "grpo", "grpo_stats", "entropy"),
         _w(ce=1.0, z=1e-4, fkl=0.5, grpo=1.0), teacher_noise=1.0, temperature=1.5,
         clip_eps=0.2, softcap=30.0, logits_scale=0.5, mask_frac=0.10),
+    # the CE + z loss set on fp32 logits at a full-size shape (fp32 is one of
+    # the logits dtypes the head loss is validated on)
+    "ce_z_fp32": Workload(
+        "ce_z_fp32", 8192, 32000, torch.float32, ("ce", "z"), _w(ce=1.0, z=1e-4)),
 }
 
 ORDER = ("tiny_ce_z_fp32", "ce_z_bf16", "ce_distill_bf16", "grpo_z_entropy_bf16", "all_in_bf16")
+# measured beside the five sets above
+EXTRA = ("ce_z_fp32",)
 
 
 def _gen(device, seed: int, stream: int) -> torch.Generator:

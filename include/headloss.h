@@ -140,8 +140,10 @@ int headloss_create(uint32_t flags, const headloss_weights* w, float temperature
  * old_logprobs:   N fp32 old-policy log-probs of the label (GRPO, GRPO_STATS).
  * advantages:     N fp32 per-token advantages (GRPO, GRPO_STATS).
  * grad_out:       N x V, `dtype`, 16-byte aligned, or NULL for metrics only.
- *                 It may equal `logits` (in-place); it must not overlap the
- *                 teacher.  Written: d(grad_scale * total) / d logits, where
+ *                 It may equal `logits` (in-place; such a call always uses
+ *                 the resident kernel, whatever plan is pinned, and returns
+ *                 ERR_SIZE where a row does not fit on chip); it must not
+ *                 overlap the teacher.  Written: d(grad_scale * total) / d logits, where
  *                 total = sum_k weight_k * mean_over_valid_rows(loss_k).
  * scalars_out:    16 fp32 (enum headloss_slot).
  * stream:         CUDA stream for all device work.

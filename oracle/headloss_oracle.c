@@ -20,9 +20,14 @@
  *     scaling, softcap, metrics without gradient.
  *
  * The pages print no loss formula.  Every loss below is the textbook
- * definition the pages' names imply; the readings are listed in the design
- * notes (softcap form, mask, temperature scope, normalisation, GRPO branch
- * rule, GRPO statistics, entropy).  The gradient is written out term by term
+ * definition the pages' names imply, under these readings: softcap
+ * z = s * c * tanh(x / c) (c = 0: off), gradient with respect to raw x;
+ * label < 0 masks a row for every loss; temperature divides student and
+ * teacher for the distillation losses only, no T^2 factor; means over the
+ * valid rows of the call; GRPO ratio at T = 1 with a symmetric clip, the
+ * unclipped branch carrying the gradient unless it is the larger objective
+ * (ties count as unclipped); clip fraction |rho - 1| > eps, k3 = rho - 1 -
+ * log rho; entropy H(p) of the student at T = 1.  The gradient is written out term by term
  * from each loss's own definition -- NOT from the per-row coefficient
  * superposition of PR #558 "Design" -- so that superposition is what the
  * tests check the CUDA path against.

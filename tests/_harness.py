@@ -1,7 +1,9 @@
 """Shared helpers of the parity tests: run the library and the oracle on the
 same seeded inputs and compare them under the stated tolerances.
 
-Tolerances (scalars and gradient as stated below; readings in the design notes):
+Tolerances (the scalar and gradient bounds of the loss's stated accuracy --
+1e-5 / 1e-3 relative scalars, 1e-3 rms-relative and 2-ulp gradients -- read
+as follows):
   scalars   rel. error <= 1e-5 (fp32 logits) / 1e-3 (bf16, fp16), where the
             error is divided by max(|ref|, mean_i |row value_i|) so that means
             close to 0 (GRPO) stay well defined; counts exact (n_clipped up to

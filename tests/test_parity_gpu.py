@@ -158,12 +158,12 @@ def test_stream_every_loss_subset():
         full_check(small(losses, N=17, V=4104, seed=len(losses)), plan=plan)
 
 
-# the gradient written over the logits by the streaming kernel (its second
-# pass re-reads each chunk from global memory while it stores gradients over
-# the row, and patches the label column last), with a teacher, softcap and a
-# partial last chunk
+# the gradient written over the logits with a pinned streaming plan, a
+# teacher, softcap and a partial last chunk: an in-place call takes the
+# resident kernel whatever plan is pinned (the streaming kernel would re-read
+# the row from global memory as it stores the gradient over it)
 @pytest.mark.parametrize("words", [1, 4])
-def test_stream_in_place(words):
+def test_stream_plan_in_place_takes_resident(words):
     plan = dict(kernel=STREAM, stages=3, threads=256, chunk_words=words)
     full_check(small(ALL_LOSSES, N=23, V=20008, softcap=30.0, logits_scale=0.5), plan=plan,
                inplace=True)
@@ -272,7 +272,7 @@ def test_create_rejects_bad_configuration():
 
 # ----------------------------------------------- full-size workloads (bench plan)
 
-FULL = ("ce_z_bf16", "ce_distill_bf16", "grpo_z_entropy_bf16", "all_in_bf16")
+FULL = ("ce_z_bf16", "ce_distill_bf16", "grpo_z_entropy_bf16", "all_in_bf16", "ce_z_fp32")
 
 
 @pytest.mark.slow
