@@ -12,6 +12,7 @@ the logits the library sees.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 import threading
@@ -165,3 +166,73 @@ def lm_head_forward_backward(cfg: _Cfg, hidden, weight, labels=None, teacher=Non
     scalars, rec, g, _ = forward_backward(cfg, x, labels, teacher, old_logprobs, advantages,
                                           want_grad=True, n_threads=n_threads)
     return scalars, rec, g @ w, g.T @ h, x, g
+
+
+def gspo_forward_backward(x, labels, old_logprobs, advantages, seg_offsets, clip_eps,
+                          weight: float = 1.0, grad_scale: float = 1.0, softcap: float = 0.0,
+                          logits_scale: float = 1.0, n_threads: int = 0):
+    """GSPO, the sequence-level clipped policy objective, written out plainly.
+
+    Reading (the pages name the objective and its per-segment form, not its
+    formula; this is the objective of the GSPO method itself):
+      - tokens [off_i, off_{i+1}) form segment i (seg_offsets: n_seq + 1
+        increasing offsets, 0 .. N); a token is valid when 0 <= label < V;
+      - lp_t = log p(label_t) of the student softmax at T = 1 (softcap and
+        scale applied as for every loss), from the row oracle;
+      - over the valid tokens T_i of a segment (L_i of them):
+        s_i = exp((1 / L_i) sum_t (lp_t - old_t)) -- the geometric mean of the
+        token ratios; A_i = mean of the tokens' advantages;
+        obj_i = min(s_i A_i, clip(s_i, 1 - eps, 1 + eps) A_i);
+      - G = segments with at least one valid token; loss = -(1/G) sum_i obj_i;
+      - the unclipped branch carries the gradient unless it is the larger
+        objective (ties count as unclipped);
+      - d(weight * grad_scale * loss)/d lp_t = -weight * grad_scale * A_i s_i
+        act_i / (G L_i), and the logits gradient of token t is that times
+        d lp_t / d x_t (the chain rule through the row's log-softmax).
+
+    Returns (scalars, coeff, grad): scalars = (loss, ratio_mean, clip_frac,
+    n_segments); coeff = d(weight * grad_scale * loss)/d lp per token (0 on
+    masked tokens); grad = N x V logits gradient."""
+    x = _f64(x)
+    n, V = x.shape
+    lab = np.ascontiguousarray(labels, dtype=np.int64)
+    old = _f64(old_logprobs)
+    adv = _f64(advantages)
+    off = np.asarray(seg_offsets, dtype=np.int64)
+    if off.ndim != 1 or off[0] != 0 or off[-1] != n or np.any(np.diff(off) < 0):
+        raise ValueError("seg_offsets: increasing offsets from 0 to N")
+    # per-token log p(label) (the GRPO statistics' new log-prob) and d(-lp)/dx
+    # (the gradient of a cross-entropy of weight 1 normalised by 1) from the
+    # row oracle; the statistics' own ratio inputs are unused here
+    cfg = make_cfg(CE | GRPO_STATS, dict(ce=1.0, grpo=0.0), softcap=softcap,
+                   logits_scale=logits_scale, grad_scale=1.0)
+    zeros = np.zeros(n)
+    rec, neg_dlp, _ = rows(cfg, x, lab, None, zeros, zeros, n_valid_total=1, want_grad=True,
+                           n_threads=n_threads)
+    lp = rec[:, RF["logprob"]]
+    valid = rec[:, RF["valid"]] > 0
+    segs = []
+    for i in range(len(off) - 1):
+        t = np.arange(off[i], off[i + 1])
+        t = t[valid[t]]
+        if t.size == 0:
+            continue
+        L = t.size
+        s = math.exp(float(np.sum(lp[t] - old[t])) / L)
+        A = float(np.mean(adv[t]))
+        sc = min(max(s, 1.0 - clip_eps), 1.0 + clip_eps)
+        unc, clp = s * A, sc * A
+        act = unc <= clp or (1.0 - clip_eps <= s <= 1.0 + clip_eps)
+        segs.append((t, L, s, A, min(unc, clp), act, abs(s - 1.0) > clip_eps))
+    G = len(segs)
+    coeff = np.zeros(n)
+    if G == 0:
+        return np.zeros(4), coeff, np.zeros((n, V))
+    loss = -sum(sg[4] for sg in segs) / G
+    for t, L, s, A, _, act, _ in segs:
+        if act:
+            coeff[t] = -weight * grad_scale * A * s / (G * L)
+    grad = -coeff[:, None] * neg_dlp
+    scalars = np.array([loss, sum(sg[2] for sg in segs) / G, sum(sg[6] for sg in segs) / G,
+                        float(G)])
+    return scalars, coeff, grad
