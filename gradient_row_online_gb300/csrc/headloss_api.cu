@@ -393,7 +393,8 @@ bool pick_stream(const headloss* h, const Plan* cand, int ncand, Plan* best) {
 // A call whose gradient overwrites its logits (in place) always takes the
 // resident kernel: it reads each row once into shared memory before any of
 // the row's gradient is stored, while the streaming kernel reads the row a
-// second time from global memory as it stores the gradient.
+// second time from global memory as it stores the gradient.  So does a call
+// with a per-token coefficient (only the resident kernels apply one).
 int make_plan(headloss* h, int64_t V, int dtype, Plan* out, int acc = 0, int inplace = 0) {
     const int feat = feature_set(h) | (acc ? int(F_ACC) : 0);
     if (h->plan.V == V && h->plan.dtype == dtype && h->plan.feat == feat &&
@@ -573,7 +574,8 @@ static int check_call(const headloss* h, const void* logits, int64_t N, int64_t 
     if (x.accumulate != 0 && x.accumulate != 1) return HEADLOSS_ERR_ARG;
     if (x.accumulate && !grad_out) return HEADLOSS_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(x.new_logprobs) & 3u) ||
-        (reinterpret_cast<uintptr_t>(x.row_loss) & 3u))
+        (reinterpret_cast<uintptr_t>(x.row_loss) & 3u) ||
+        (reinterpret_cast<uintptr_t>(x.token_coeff) & 3u))
         return HEADLOSS_ERR_ALIGN;
     if (N > 0 && !logits) return HEADLOSS_ERR_ARG;
     if (dtype < 0 || dtype > 2) return HEADLOSS_ERR_DTYPE;
@@ -584,7 +586,7 @@ static int check_call(const headloss* h, const void* logits, int64_t N, int64_t 
             return HEADLOSS_ERR_MISSING_INPUT;
         if ((f & (L_GRPO | L_GRPO_STATS)) && (!old_logprobs || !advantages))
             return HEADLOSS_ERR_MISSING_INPUT;
-        if (x.new_logprobs && !labels) return HEADLOSS_ERR_MISSING_INPUT;
+        if ((x.new_logprobs || x.token_coeff) && !labels) return HEADLOSS_ERR_MISSING_INPUT;
     }
     const bool teach = (f & (L_DIST_CE | L_FKL | L_RKL)) != 0;
     if (!aligned16(logits) || (teach && !aligned16(teacher_logits)) ||
@@ -610,7 +612,7 @@ int headloss_forward_backward_ext(headloss_t h, const void* logits, int64_t N, i
                                   const float* old_logprobs, const float* advantages,
                                   void* grad_out, float* scalars_out,
                                   const headloss_call_ext* ext, headloss_stream_t stream) {
-    headloss_call_ext x = {nullptr, nullptr, 0, 0.0};
+    headloss_call_ext x = {nullptr, nullptr, 0, 0.0, nullptr};
     if (ext) x = *ext;
     {
         const int rc = check_call(h, logits, N, V, dtype, labels, teacher_logits, old_logprobs,
@@ -631,7 +633,8 @@ int headloss_forward_backward_ext(headloss_t h, const void* logits, int64_t N, i
         const int64_t bytes = N * V * elem_size(dtype);
         inplace = (g0 < x0 + bytes && x0 < g0 + bytes) ? 1 : 0;
     }
-    const int rc = make_plan(h, V, dtype, &pl, x.accumulate, inplace);
+    // a per-token coefficient is applied by the resident kernels only
+    const int rc = make_plan(h, V, dtype, &pl, x.accumulate, inplace || x.token_coeff ? 1 : 0);
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
@@ -677,6 +680,7 @@ int headloss_forward_backward_ext(headloss_t h, const void* logits, int64_t N, i
         p.rl_out = x.row_loss;
         p.divisor = x.divisor;
         p.accumulate = x.accumulate;
+        p.tok = x.token_coeff;
 
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
@@ -831,7 +835,7 @@ extern "C" int headloss_forward_backward_noalloc(
     h.forced = headloss_plan_desc{0, 0, 0, 0, 0};
     // the call's own argument checks first: a rejected call enqueues nothing
     {
-        const headloss_call_ext none = {nullptr, nullptr, 0, 0.0};
+        const headloss_call_ext none = {nullptr, nullptr, 0, 0.0, nullptr};
         const int crc = check_call(&h, logits, N, V, dtype, labels, teacher_logits, old_logprobs,
                                    advantages, grad_out, scalars_out, none);
         if (crc) return crc;

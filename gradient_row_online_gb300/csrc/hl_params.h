@@ -71,6 +71,8 @@ struct Params {
     float* rl_out;                 // N per-row total loss (or null)
     double divisor;                // > 0: normaliser replacing the valid-row count
     int accumulate;                // 1: add the gradient to grad_out's values
+    const float* tok;              // N per-row d(total)/d(log p(label)) added on the label
+                                   // column (GSPO's per-token coefficient), or null
 };
 
 }  // namespace hl

@@ -642,10 +642,19 @@ __device__ __forceinline__ void rows_body16(const Params& p) {
             // coefficients are out
             RowLoss* rls = reinterpret_cast<RowLoss*>(coefs + 16);
             if (warp == 0) {
-                const RowCoef kw = row_epilogue16<TEACH, RKL, ENT, CAP, false>(
+                RowCoef kw = row_epilogue16<TEACH, RKL, ENT, CAP, false>(
                     p, xrec, C, false, old_lp, adv, acc, lane, r, kk,
                     rank == 0 ? rls : nullptr);
-                if (lane == 0) *reinterpret_cast<RowCoef*>(coefs) = kw;
+                if (lane == 0) {
+                    if (p.tok != nullptr) {
+                        // a per-token coefficient c = d(total)/d(log p(label)):
+                        // c (delta_label - p), scaled like every coefficient
+                        const float c = p.tok[r] * p.s;
+                        kw.pc -= c;
+                        kw.bc -= c;
+                    }
+                    *reinterpret_cast<RowCoef*>(coefs) = kw;
+                }
             }
             ++xc;
             __syncthreads();

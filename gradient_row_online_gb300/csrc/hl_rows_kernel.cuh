@@ -251,6 +251,13 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
             if (tid == 0) {
                 row_epilogue<A, TEACH, RKL, ENT, CAP>(p, xch + (xc & 1) * MAX_CLUSTER * NREC, C,
                                                       rank == 0, old_lp, adv, acc, coef, r);
+                if (p.tok != nullptr) {  // per-token coefficient on the label column
+                    // (the scale is in the coefficients only without softcap;
+                    // with softcap it is in the per-element derivative)
+                    const A c = A(p.tok[r]) * (CAP ? A(1) : A(p.s));
+                    coef[K_PC] -= c;
+                    coef[K_BC] -= c;
+                }
             }
             ++xc;
             __syncthreads();

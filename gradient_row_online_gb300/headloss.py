@@ -50,7 +50,7 @@ EXPORTS = ("headloss_create", "headloss_forward_backward", "headloss_get_device_
            "headloss_plan", "headloss_force_plan", "headloss_launches_per_call",
            "headloss_destroy", "headloss_strerror", "headloss_version",
            "headloss_forward_backward_noalloc", "headloss_forward_backward_ext",
-           "headloss_lmhead_logits")
+           "headloss_gspo_seam", "headloss_lmhead_logits")
 
 
 # enum headloss_kernel
@@ -62,7 +62,8 @@ class headloss_call_ext(ctypes.Structure):
     """struct headloss_call_ext: per-call extras (per-token outputs, gradient
     accumulation, the divisor of a split batch)."""
     _fields_ = [("new_logprobs", ctypes.c_void_p), ("row_loss", ctypes.c_void_p),
-                ("accumulate", ctypes.c_int), ("divisor", ctypes.c_double)]
+                ("accumulate", ctypes.c_int), ("divisor", ctypes.c_double),
+                ("token_coeff", ctypes.c_void_p)]
 
 
 class headloss_plan_desc(ctypes.Structure):
@@ -92,7 +93,7 @@ def load_library(path: str = LIB_PATH):
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with gradient_row_online_gb300.build.build()")
     lib = ctypes.CDLL(path)
-    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
     ip = ctypes.POINTER(ctypes.c_int)
     lib.headloss_create.argtypes = [ctypes.c_uint32, ctypes.POINTER(headloss_weights),
                                     ctypes.c_float, ctypes.c_float, ctypes.c_float,
@@ -124,6 +125,9 @@ def load_library(path: str = LIB_PATH):
     lib.headloss_forward_backward_ext.restype = i32
     lib.headloss_lmhead_logits.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp]
     lib.headloss_lmhead_logits.restype = i32
+    lib.headloss_gspo_seam.argtypes = [vp, vp, vp, vp, i64, i64, vp, i32, f32, f32, f32, vp, vp,
+                                       vp]
+    lib.headloss_gspo_seam.restype = i32
     _lib = lib
     return lib
 
@@ -196,12 +200,13 @@ def headloss_forward_backward(h, logits, N, V, dtype, labels, teacher_logits, ol
 def headloss_forward_backward_ext(h, logits, N, V, dtype, labels, teacher_logits, old_logprobs,
                                   advantages, grad_out, scalars_out, new_logprobs=None,
                                   row_loss=None, accumulate=False, divisor=0.0,
-                                  stream=None) -> None:
+                                  token_coeff=None, stream=None) -> None:
     """The call with its extras: per-row log p(label) and total loss outputs,
-    gradient accumulation into grad_out, and the divisor of a split batch."""
+    gradient accumulation into grad_out, the divisor of a split batch, and a
+    per-token coefficient on the label column (GSPO's, from headloss_gspo_seam)."""
     lib = load_library()
     ext = headloss_call_ext(_ptr(new_logprobs), _ptr(row_loss), int(bool(accumulate)),
-                            float(divisor))
+                            float(divisor), _ptr(token_coeff))
     _check(lib.headloss_forward_backward_ext(h, _ptr(logits), int(N), int(V), int(dtype),
                                              _ptr(labels), _ptr(teacher_logits),
                                              _ptr(old_logprobs), _ptr(advantages),
@@ -233,6 +238,17 @@ def headloss_lmhead_logits(hidden, weight, N, D, V, logits, stats, err, stream=N
                                                  int(V), _ptr(logits), _ptr(stats), _ptr(err),
                                                  _stream(stream)),
            "headloss_lmhead_logits")
+
+
+def headloss_gspo_seam(new_logprobs, old_logprobs, advantages, labels, N, V, seg_offsets, n_seg,
+                       clip_eps, weight, grad_scale, token_coeff, scalars_out,
+                       stream=None) -> None:
+    """GSPO's per-segment seam (include/headloss.h): the sequence ratios and
+    the per-token coefficient for the backward call; raises on a bad status."""
+    _check(load_library().headloss_gspo_seam(
+        _ptr(new_logprobs), _ptr(old_logprobs), _ptr(advantages), _ptr(labels), int(N), int(V),
+        _ptr(seg_offsets), int(n_seg), float(clip_eps), float(weight), float(grad_scale),
+        _ptr(token_coeff), _ptr(scalars_out), _stream(stream)), "headloss_gspo_seam")
 
 
 def headloss_get_device_error(h, stream=None) -> int:

@@ -189,12 +189,22 @@ int headloss_forward_backward(headloss_t h, const void* logits, int64_t N, int64
  *                slots (NEW_LOGPROB .. ADV_STD, N_VALID, N_CLIPPED) stay over
  *                the call's own rows.  0: the call's own count.  Must be
  *                finite.
+ * token_coeff:   N fp32 (device) or NULL.  A per-row coefficient c_i =
+ *                d(total)/d(log p(label_i)) computed outside the call -- GSPO's
+ *                per-token coefficient from headloss_gspo_seam -- superposed on
+ *                the gradient as c_i (delta(j, label) - p_j) on the label
+ *                column the label-based losses share (PR #558, "Design": the
+ *                GSPO seam hands the kernel a per-token coefficient that
+ *                superposes with the in-kernel losses).  grad_scale does not
+ *                multiply it (the seam already did).  Masked rows ignore it.
+ *                Requires labels; such a call uses the resident kernel.
  */
 typedef struct {
     float* new_logprobs;
     float* row_loss;
     int accumulate;
     double divisor;
+    const float* token_coeff;
 } headloss_call_ext;
 
 /*
@@ -202,8 +212,8 @@ typedef struct {
  * above (the arguments before `ext` are those of headloss_forward_backward).
  * Extra errors (host-side, nothing enqueued): ERR_ARG (divisor < 0 or not
  * finite, accumulate with grad_out NULL or overlapping the logits), ERR_ALIGN
- * (new_logprobs / row_loss not 4-byte aligned), ERR_MISSING_INPUT
- * (new_logprobs without labels, N > 0).
+ * (new_logprobs / row_loss / token_coeff not 4-byte aligned),
+ * ERR_MISSING_INPUT (new_logprobs or token_coeff without labels, N > 0).
  */
 int headloss_forward_backward_ext(headloss_t h, const void* logits, int64_t N, int64_t V,
                                   int dtype, const int64_t* labels, const void* teacher_logits,
@@ -289,6 +299,49 @@ int headloss_forward_backward_noalloc(uint32_t flags, const headloss_weights* w,
                                       const int64_t* labels, const void* teacher_logits,
                                       const float* old_logprobs, const float* advantages,
                                       void* grad_out, float* scalars_out, headloss_stream_t stream);
+
+/*
+ * headloss_gspo_seam -- GSPO's per-segment seam: the sequence-level ratio,
+ * its clipped objective and the per-token coefficient the backward call
+ * superposes (headloss_call_ext.token_coeff).  GSPO runs in three steps, as
+ * in ServiceNow Fast-LLM PR #558 "Design" (forward, eager segment seam,
+ * load-mode backward) and PR #549 "Loss coverage":
+ *   1. headloss_forward_backward_ext with new_logprobs (grad_out may be NULL);
+ *   2. this call;
+ *   3. headloss_forward_backward_ext with token_coeff (and the other losses).
+ * The objective: segment i is rows [seg_offsets[i], seg_offsets[i+1]); over
+ * its valid rows T_i (0 <= label < V; L_i of them)
+ *   s_i = exp((1/L_i) sum_t (new_t - old_t))   (geometric mean of token ratios)
+ *   A_i = mean of advantages_t over T_i
+ *   obj_i = min(s_i A_i, clip(s_i, 1 - clip_eps, 1 + clip_eps) A_i)
+ * and the loss is -(1/G) sum_i obj_i over the G segments that hold a valid
+ * row.  The unclipped branch carries the gradient unless it is the larger
+ * objective (ties count as unclipped).
+ *
+ * new_logprobs:  N fp32 (device): log p(label) per row at T = 1 (step 1).
+ * old_logprobs:  N fp32, advantages: N fp32 (one advantage per sequence
+ *                broadcast to its rows), labels: N int64 -- all device.
+ * N, V:          rows and vocabulary size (V decides which labels are valid).
+ * seg_offsets:   n_seg + 1 int64 (device), non-decreasing from 0 to N.
+ *                Offsets outside [0, N] are clamped and a decreasing pair is
+ *                an empty segment; overlapping segments are not detected.
+ * clip_eps:      >= 0.  weight, grad_scale: finite; the coefficient is that
+ *                of weight * grad_scale * loss.
+ * token_coeff:   N fp32 (device, written): c_t = d(weight * grad_scale *
+ *                loss)/d(new_t) = -weight * grad_scale * A_i s_i / (G L_i)
+ *                for a valid row of a segment on its unclipped branch, else 0.
+ * scalars_out:   4 fp32 (device, written): loss, mean s_i, fraction of
+ *                segments with |s_i - 1| > clip_eps, G.
+ * Two launches on `stream`, deterministic (fp64, fixed-order sums); no
+ * allocation.  Errors (nothing enqueued): ERR_ARG (N < 0, V < 1, n_seg < 1,
+ * clip_eps < 0, a non-finite weight, a NULL pointer), ERR_ALIGN (fp32 arrays
+ * not 4-byte, int64 arrays not 8-byte aligned), ERR_CUDA.
+ */
+int headloss_gspo_seam(const float* new_logprobs, const float* old_logprobs,
+                       const float* advantages, const int64_t* labels, int64_t N, int64_t V,
+                       const int64_t* seg_offsets, int n_seg, float clip_eps, float weight,
+                       float grad_scale, float* token_coeff, float* scalars_out,
+                       headloss_stream_t stream);
 
 /* Kernel launches one headloss_forward_backward call enqueues (constant). */
 int headloss_launches_per_call(void);
