@@ -22,6 +22,7 @@ const void* rows_kernel_bf16_acc(int feat);
 const void* rows_kernel_fp16_acc(int feat);
 const void* stream_kernel_bf16_acc(int feat);
 const void* stream_kernel_fp16_acc(int feat);
+const void* onepass_kernel_bf16(int feat);
 
 // Valid rows of the call (0 <= label < V); a label >= V raises E_LABEL.
 // One block: the count is an exact integer whatever the order.
@@ -734,6 +735,91 @@ int headloss_get_device_error(headloss_t h, headloss_stream_t stream, int* err) 
     if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess) return HEADLOSS_ERR_CUDA;
     *err = (v & E_LABEL) ? HEADLOSS_ERR_LABEL_RANGE
                          : ((v & E_TIMEOUT) ? HEADLOSS_ERR_TIMEOUT : HEADLOSS_OK);
+    return HEADLOSS_OK;
+}
+
+// The loss's gradient pass alone, from the per-tile row statistics of the
+// LM-head GEMM (include/headloss.h documents the call).
+int headloss_forward_backward_rowstats(headloss_t h, const void* logits, int64_t N, int64_t V,
+                                       int dtype, const int64_t* labels,
+                                       const float* old_logprobs, const float* advantages,
+                                       const void* row_stats, void* grad_out, float* scalars_out,
+                                       headloss_stream_t stream) {
+    const headloss_call_ext none = {nullptr, nullptr, 0, 0.0, nullptr};
+    if (!h) return HEADLOSS_ERR_ARG;
+    const uint32_t f = h->flags;
+    if (f & (L_DIST_CE | L_FKL | L_RKL)) return HEADLOSS_ERR_ARG;  // no teacher here
+    {
+        const int rc = check_call(h, logits, N, V, dtype, labels, nullptr, old_logprobs,
+                                  advantages, grad_out, scalars_out, none);
+        if (rc) return rc;
+    }
+    if (dtype != HEADLOSS_BF16) return HEADLOSS_ERR_DTYPE;
+    if (V % 256) return HEADLOSS_ERR_ARG;
+    if (N > 0 && !row_stats) return HEADLOSS_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(row_stats) & 15u) return HEADLOSS_ERR_ALIGN;
+    std::lock_guard<std::mutex> g(h->mu);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return HEADLOSS_ERR_CUDA;
+    if (dev != h->device) return HEADLOSS_ERR_ARG;
+    int feat = feature_set(h) & (F_ENT | F_SOFTCAP | F_ENTG);
+    const void* kernel = onepass_kernel_bf16(feat);
+    if (!kernel) return HEADLOSS_ERR_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    count_valid_kernel<<<1, 1024, 0, s>>>(labels, N, V, h->n_valid, h->err, h->w.grad_scale, 0.0,
+                                          h->kscale);
+    int grid = 0;
+    if (N > 0) {
+        // four warps per row (each a quarter of its words), eight warps per
+        // CTA, three CTAs per SM resident
+        const int64_t want = (4 * N + 7) / 8;
+        const int64_t cap = 3 * int64_t(h->num_sms) < h->partials_cap ? 3 * int64_t(h->num_sms)
+                                                                      : h->partials_cap;
+        grid = int(want < cap ? want : cap);
+        Params p = {};
+        p.x = logits;
+        p.t = nullptr;
+        p.g = grad_out;
+        p.labels = labels;
+        p.old_lp = (f & (L_GRPO | L_GRPO_STATS)) ? old_logprobs : nullptr;
+        p.adv = (f & (L_GRPO | L_GRPO_STATS)) ? advantages : nullptr;
+        p.N = N;
+        p.V = V;
+        p.C = 1;
+        p.flags = f;
+        p.s = h->s;
+        p.softcap = h->softcap;
+        p.T = h->T;
+        p.eps = h->eps;
+        p.w_ce = h->w.ce;
+        p.w_z = h->w.z;
+        p.w_grpo = h->w.grpo;
+        p.w_ent = h->w.entropy;
+        p.grad_scale = h->w.grad_scale;
+        p.partials = h->partials;
+        p.n_valid = h->n_valid;
+        p.kscale = h->kscale;
+        p.err = h->err;
+        p.wait_ns = h->wait_ns;
+        p.drop_row = -1;
+        int nt = int(V / 256);
+        const void* rs = row_stats;
+        void* args[] = {&p, &rs, &nt};
+        if (cudaLaunchKernel(kernel, dim3(grid), dim3(256), args, 0, s) != cudaSuccess)
+            return HEADLOSS_ERR_CUDA;
+    }
+    FinalizeArgs fa;
+    fa.flags = f;
+    fa.w_ce = h->w.ce;
+    fa.w_z = h->w.z;
+    fa.w_dce = 0.f;
+    fa.w_fkl = 0.f;
+    fa.w_rkl = 0.f;
+    fa.w_grpo = h->w.grpo;
+    fa.w_ent = h->w.entropy;
+    fa.divisor = 0.0;
+    finalize_kernel<<<1, 32 * NACC, 0, s>>>(h->partials, grid, h->n_valid, fa, scalars_out);
+    if (cudaGetLastError() != cudaSuccess) return HEADLOSS_ERR_CUDA;
     return HEADLOSS_OK;
 }
 

@@ -28,6 +28,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "headloss.h"
@@ -194,11 +195,21 @@ __device__ __forceinline__ void tile_of(int i, int MT, int NT, int& m, int& n) {
     }
 }
 
+// Statistics of one (row, tile) from its bf16 logits.  MODE 0: (m, s) with
+// m the max logit and s = sum exp(x - m).  MODE 1: the loss's first-pass
+// record of the capped, scaled logits zs = s c tanh(x / c) log2(e) (c = 0:
+// s x log2(e)), base 2: (m2, S, E) with m2 = max zs, S = sum 2^(zs - m2),
+// E = sum 2^(zs - m2) (zs - m2).
+struct Xform {
+    float c, invc, k;  // softcap (0: off), 1 / c, s * c * log2(e) (c = 0: s * log2(e))
+};
+
+template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     lmhead_gemm_kernel(const __grid_constant__ CUtensorMap map_h,
                        const __grid_constant__ CUtensorMap map_w,
                        const __grid_constant__ CUtensorMap map_o, int D, int MT, int NT,
-                       float2* __restrict__ stats, int* err) {
+                       void* __restrict__ stats_out, Xform xf, int* err) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -315,7 +326,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!wait_phase(su32(&tfull[acc]), uint32_t(j >> 1) & 1u, abort, err)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const uint32_t tbase = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc * BN);
-            float mx = -INFINITY, ssum = 0.f;
+            float mx = -INFINITY, ssum = 0.f, esum = 0.f;
             for (int g = 0; g < BN / OUT_COLS; ++g, ++step) {
                 unsigned char* ob = outb + (step & 1) * OUT_BYTES;
                 // the store that last read this buffer has finished reading it
@@ -333,12 +344,32 @@ __global__ void __launch_bounds__(THREADS, 1)
                         pk[t] = *reinterpret_cast<const uint32_t*>(&b2);
                         v[2 * t] = __low2float(b2);
                         v[2 * t + 1] = __high2float(b2);
+                        if (MODE == 1) {  // zs of the bf16 logits
+                            v[2 * t] = xf.c > 0.f ? xf.k * tanhf(v[2 * t] * xf.invc) : xf.k * v[2 * t];
+                            v[2 * t + 1] = xf.c > 0.f ? xf.k * tanhf(v[2 * t + 1] * xf.invc)
+                                                      : xf.k * v[2 * t + 1];
+                        }
                         cm = fmaxf(cm, fmaxf(v[2 * t], v[2 * t + 1]));
                     }
                     const float nm = fmaxf(mx, cm);
-                    ssum *= exp2f((mx - nm) * 1.4426950408889634f);
+                    if (MODE == 0) {
+                        ssum *= exp2f((mx - nm) * 1.4426950408889634f);
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) ssum += exp2f((v[t] - nm) * 1.4426950408889634f);
+                        for (int t = 0; t < 32; ++t) ssum += exp2f((v[t] - nm) * 1.4426950408889634f);
+                    } else {
+                        // rescale the running sums to the new max, then add the chunk
+                        const float dm = mx == -INFINITY ? 0.f : mx - nm;
+                        const float al = exp2f(dm);
+                        esum = al * (esum + dm * ssum);
+                        ssum *= al;
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) {
+                            const float d = v[t] - nm;
+                            const float e = exp2f(d);
+                            ssum += e;
+                            esum = fmaf(e, d, esum);
+                        }
+                    }
                     mx = nm;
                     // row `lane`, 16-byte chunks 4h .. 4h+3 of this 128-byte row,
                     // placed by the 128-byte swizzle (chunk index ^ row % 8)
@@ -361,7 +392,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(su32(&tempty[acc]));
-            stats[size_t(m * BM + 32 * q + lane) * NT + n] = make_float2(mx, ssum);
+            const size_t si = size_t(m * BM + 32 * q + lane) * NT + n;
+            if (MODE == 0) static_cast<float2*>(stats_out)[si] = make_float2(mx, ssum);
+            else static_cast<float4*>(stats_out)[si] = make_float4(mx, ssum, esum, 0.f);
         }
         if (lane == 0) bulk_wait_all();  // stores complete before shared memory is released
         __syncwarp();
@@ -406,16 +439,18 @@ int make_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows,
 
 }  // namespace hl_lmhead
 
-// The C ABI call (include/headloss_lmhead.h documents it).
-extern "C" int headloss_lmhead_logits(const void* hidden, const void* weight, int N, int D, int V,
-                                      void* logits, void* stats, int* err, void* stream) {
-    using namespace hl_lmhead;
+namespace hl_lmhead {
+
+int launch(int mode, const void* hidden, const void* weight, int N, int D, int V, float softcap,
+           float logits_scale, void* logits, void* stats, int* err, void* stream) {
     if (N <= 0 || D <= 0 || V <= 0 || N % BM || V % BN || D % BK) return HEADLOSS_ERR_ARG;
     if (!hidden || !weight || !logits || !stats || !err) return HEADLOSS_ERR_ARG;
+    if (!(softcap >= 0.f) || !isfinite(softcap) || !(logits_scale > 0.f) || !isfinite(logits_scale))
+        return HEADLOSS_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(weight) |
          reinterpret_cast<uintptr_t>(logits)) & 15)
         return HEADLOSS_ERR_ALIGN;
-    if (reinterpret_cast<uintptr_t>(stats) & 7) return HEADLOSS_ERR_ALIGN;
+    if (reinterpret_cast<uintptr_t>(stats) & (mode == 0 ? 7 : 15)) return HEADLOSS_ERR_ALIGN;
     if (reinterpret_cast<uintptr_t>(err) & 3) return HEADLOSS_ERR_ALIGN;
     CUtensorMap mh, mw, mo;
     if (make_map(&mh, hidden, N, D, BM, BK) || make_map(&mw, weight, V, D, BN, BK) ||
@@ -425,13 +460,40 @@ extern "C" int headloss_lmhead_logits(const void* hidden, const void* weight, in
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return HEADLOSS_ERR_CUDA;
-    if (cudaFuncSetAttribute(lmhead_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES) != cudaSuccess)
+    const void* fn = mode == 0 ? reinterpret_cast<const void*>(&lmhead_gemm_kernel<0>)
+                               : reinterpret_cast<const void*>(&lmhead_gemm_kernel<1>);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+        cudaSuccess)
         return HEADLOSS_ERR_CUDA;
     const int MT = N / BM, NT = V / BN;
     const int tiles = MT * NT;
     const int grid = tiles < sms ? tiles : sms;
-    lmhead_gemm_kernel<<<grid, THREADS, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(
-        mh, mw, mo, D, MT, NT, static_cast<float2*>(stats), err);
+    Xform xf;
+    xf.c = softcap;
+    xf.invc = softcap > 0.f ? 1.f / softcap : 0.f;
+    xf.k = (softcap > 0.f ? logits_scale * softcap : logits_scale) * 1.4426950408889634f;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (mode == 0)
+        lmhead_gemm_kernel<0><<<grid, THREADS, SMEM_BYTES, s>>>(mh, mw, mo, D, MT, NT, stats, xf,
+                                                                 err);
+    else
+        lmhead_gemm_kernel<1><<<grid, THREADS, SMEM_BYTES, s>>>(mh, mw, mo, D, MT, NT, stats, xf,
+                                                                 err);
     return cudaGetLastError() == cudaSuccess ? HEADLOSS_OK : HEADLOSS_ERR_CUDA;
+}
+
+}  // namespace hl_lmhead
+
+// The C ABI calls (include/headloss_lmhead.h documents them).
+extern "C" int headloss_lmhead_logits(const void* hidden, const void* weight, int N, int D, int V,
+                                      void* logits, void* stats, int* err, void* stream) {
+    return hl_lmhead::launch(0, hidden, weight, N, D, V, 0.f, 1.f, logits, stats, err, stream);
+}
+
+extern "C" int headloss_lmhead_logits_rowstats(const void* hidden, const void* weight, int N,
+                                               int D, int V, float softcap, float logits_scale,
+                                               void* logits, void* row_stats, int* err,
+                                               void* stream) {
+    return hl_lmhead::launch(1, hidden, weight, N, D, V, softcap, logits_scale, logits, row_stats,
+                             err, stream);
 }

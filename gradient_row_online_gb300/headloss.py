@@ -50,7 +50,8 @@ EXPORTS = ("headloss_create", "headloss_forward_backward", "headloss_get_device_
            "headloss_plan", "headloss_force_plan", "headloss_launches_per_call",
            "headloss_destroy", "headloss_strerror", "headloss_version",
            "headloss_forward_backward_noalloc", "headloss_forward_backward_ext",
-           "headloss_gspo_seam", "headloss_lmhead_logits")
+           "headloss_gspo_seam", "headloss_forward_backward_rowstats",
+           "headloss_lmhead_logits", "headloss_lmhead_logits_rowstats")
 
 
 # enum headloss_kernel
@@ -128,6 +129,12 @@ def load_library(path: str = LIB_PATH):
     lib.headloss_gspo_seam.argtypes = [vp, vp, vp, vp, i64, i64, vp, i32, f32, f32, f32, vp, vp,
                                        vp]
     lib.headloss_gspo_seam.restype = i32
+    lib.headloss_lmhead_logits_rowstats.argtypes = [vp, vp, i32, i32, i32, f32, f32, vp, vp, vp,
+                                                    vp]
+    lib.headloss_lmhead_logits_rowstats.restype = i32
+    lib.headloss_forward_backward_rowstats.argtypes = [vp, vp, i64, i64, i32, vp, vp, vp, vp, vp,
+                                                       vp, vp]
+    lib.headloss_forward_backward_rowstats.restype = i32
     _lib = lib
     return lib
 
@@ -238,6 +245,26 @@ def headloss_lmhead_logits(hidden, weight, N, D, V, logits, stats, err, stream=N
                                                  int(V), _ptr(logits), _ptr(stats), _ptr(err),
                                                  _stream(stream)),
            "headloss_lmhead_logits")
+
+
+def headloss_lmhead_logits_rowstats(hidden, weight, N, D, V, softcap, logits_scale, logits,
+                                    row_stats, err, stream=None) -> None:
+    """The LM-head GEMM with the loss's per-tile first-pass records
+    (include/headloss_lmhead.h); raises HeadlossError on a bad status."""
+    _check(load_library().headloss_lmhead_logits_rowstats(
+        _ptr(hidden), _ptr(weight), int(N), int(D), int(V), float(softcap), float(logits_scale),
+        _ptr(logits), _ptr(row_stats), _ptr(err), _stream(stream)),
+        "headloss_lmhead_logits_rowstats")
+
+
+def headloss_forward_backward_rowstats(h, logits, N, V, dtype, labels, old_logprobs, advantages,
+                                       row_stats, grad_out, scalars_out, stream=None) -> None:
+    """The loss's gradient pass alone from the GEMM's row statistics
+    (include/headloss.h); raises HeadlossError on a bad status."""
+    _check(load_library().headloss_forward_backward_rowstats(
+        h, _ptr(logits), int(N), int(V), int(dtype), _ptr(labels), _ptr(old_logprobs),
+        _ptr(advantages), _ptr(row_stats), _ptr(grad_out), _ptr(scalars_out), _stream(stream)),
+        "headloss_forward_backward_rowstats")
 
 
 def headloss_gspo_seam(new_logprobs, old_logprobs, advantages, labels, N, V, seg_offsets, n_seg,

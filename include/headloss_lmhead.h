@@ -53,6 +53,25 @@ extern "C" {
 int headloss_lmhead_logits(const void* hidden, const void* weight, int N, int D, int V,
                            void* logits, void* stats, int* err, void* stream);
 
+/*
+ * headloss_lmhead_logits_rowstats -- the same GEMM with, per (row, 256-column
+ * tile), the loss's first-pass record of the tile instead of (m, s): the
+ * statistics headloss_forward_backward_rowstats (include/headloss.h) consumes.
+ *
+ * softcap, logits_scale: those of the loss handle that will consume the
+ *            statistics (softcap c >= 0, 0 = off; logits_scale s > 0).
+ * row_stats: N x (V / 256) records of 4 fp32, device, 16-byte aligned
+ *            (written): for the bf16 logits x of row i and tile k, with
+ *            zs = s c tanh(x / c) log2(e) (c = 0: zs = s x log2(e)),
+ *            (m2, S, E, 0): m2 = max zs, S = sum 2^(zs - m2),
+ *            E = sum 2^(zs - m2) (zs - m2).
+ * Other arguments, checks and errors as headloss_lmhead_logits (ERR_ARG also
+ * for a negative or non-finite softcap, a non-positive logits_scale).
+ */
+int headloss_lmhead_logits_rowstats(const void* hidden, const void* weight, int N, int D, int V,
+                                    float softcap, float logits_scale, void* logits,
+                                    void* row_stats, int* err, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
