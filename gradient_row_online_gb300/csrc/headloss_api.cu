@@ -23,6 +23,7 @@ const void* rows_kernel_fp16_acc(int feat);
 const void* stream_kernel_bf16_acc(int feat);
 const void* stream_kernel_fp16_acc(int feat);
 const void* onepass_kernel_bf16(int feat);
+int onepass_smem_bytes();
 
 // Valid rows of the call (0 <= label < V); a label >= V raises E_LABEL.
 // One block: the count is an exact integer whatever the order.
@@ -771,10 +772,20 @@ int headloss_forward_backward_rowstats(headloss_t h, const void* logits, int64_t
     int grid = 0;
     if (N > 0) {
         // four warps per row (each a quarter of its words), eight warps per
-        // CTA, three CTAs per SM resident
+        // CTA, as many CTAs as are resident together (two per SM: each
+        // warp's copy ring is 12 KB)
+        const int smem = onepass_smem_bytes();
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return HEADLOSS_ERR_CUDA;
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, size_t(smem)) !=
+                cudaSuccess ||
+            per_sm < 1)
+            return HEADLOSS_ERR_CUDA;
         const int64_t want = (4 * N + 7) / 8;
-        const int64_t cap = 3 * int64_t(h->num_sms) < h->partials_cap ? 3 * int64_t(h->num_sms)
-                                                                      : h->partials_cap;
+        const int64_t res = int64_t(per_sm) * h->num_sms;
+        const int64_t cap = res < h->partials_cap ? res : h->partials_cap;
         grid = int(want < cap ? want : cap);
         Params p = {};
         p.x = logits;
@@ -805,7 +816,8 @@ int headloss_forward_backward_rowstats(headloss_t h, const void* logits, int64_t
         int nt = int(V / 256);
         const void* rs = row_stats;
         void* args[] = {&p, &rs, &nt};
-        if (cudaLaunchKernel(kernel, dim3(grid), dim3(256), args, 0, s) != cudaSuccess)
+        if (cudaLaunchKernel(kernel, dim3(grid), dim3(256), args, size_t(smem), s) !=
+            cudaSuccess)
             return HEADLOSS_ERR_CUDA;
     }
     FinalizeArgs fa;

@@ -15,14 +15,17 @@
 // entropy); the distillation losses pair the row with a teacher row element
 // by element and are not supported here.
 //
-// One warp per row, rows strided over the grid:
-//   merge     lane k merges the records of tiles k, k + 32, ... (running max,
-//             rescaled sums); the 32 lane records go through the row epilogue
-//             shared with the other kernels (losses, coefficients);
-//   gradient  each lane streams 16-byte words of the row (a warp reads and
-//             writes 512 contiguous bytes per step), computes the combined
-//             gradient in fp32 and writes it once; the lane whose word holds
-//             the label column patches that element before the store.
+// Four warps per row, each a quarter of its words (a unit), units strided
+// over the grid:
+//   merge     the row's four warps merge a quarter of the tile records each
+//             (running max, rescaled sums), exchange them through shared
+//             memory, and each takes the 32 lane records through the row
+//             epilogue shared with the other kernels (losses, coefficients);
+//   gradient  the unit's words arrive through the warp's own ring of 4 KB
+//             bulk copies, which runs ahead across units; each lane computes
+//             the combined gradient of its 16-byte words in fp32 and stores
+//             it once; the lane whose word holds the label column patches
+//             that element before the store.
 // Per-warp compensated sums of the row losses are added in warp order into
 // one fp64 partial record per CTA, which the finalize kernel reduces.
 #include "hl_rows16.cuh"
@@ -31,11 +34,14 @@ namespace hl {
 
 constexpr int OP_THREADS = 256;
 constexpr int OP_WARPS = OP_THREADS / 32;
-constexpr int OP_PARTS = 4;   // warps per row, each a quarter of the row's words
-constexpr int OP_UNROLL = 4;  // words per lane in flight
+constexpr int OP_PARTS = 4;         // warps per row, each a quarter of the row's words
+constexpr int OP_SLOTS = 3;         // chunk slots of each warp's ring
+constexpr int OP_CHUNK_WORDS = 256; // 16-byte words per chunk (8 per lane, 4 KB)
+// dynamic shared memory: the warps' rings and their mbarriers
+constexpr int OP_SMEM = OP_WARPS * OP_SLOTS * OP_CHUNK_WORDS * 16 + OP_WARPS * OP_SLOTS * 8;
 
 template <int FEAT>
-__global__ void __launch_bounds__(OP_THREADS, 3) onepass_kernel16(const __grid_constant__ Params p,
+__global__ void __launch_bounds__(OP_THREADS, 2) onepass_kernel16(const __grid_constant__ Params p,
                                                                const float4* __restrict__ rs,
                                                                int NT) {
     using P16 = Pack16<__nv_bfloat16>;
@@ -45,8 +51,12 @@ __global__ void __launch_bounds__(OP_THREADS, 3) onepass_kernel16(const __grid_c
     constexpr int EPW = 8;
 
     __shared__ float recs[OP_WARPS][32 * NREC];
+    // the four part warps' merged tile records (m2, S, E) per lane:
+    // [group][part][field][lane]
+    __shared__ float mrg[OP_WARPS / OP_PARTS][OP_PARTS][3][32];
     __shared__ float accs[OP_WARPS][2 * NACC];
     __shared__ RowLoss rls[OP_WARPS];
+    extern __shared__ __align__(128) unsigned char ring_smem[];
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t N = p.N, V = p.V;
@@ -63,23 +73,112 @@ __global__ void __launch_bounds__(OP_THREADS, 3) onepass_kernel16(const __grid_c
     const float invc = CAP ? 1.f / p.softcap : 0.f;
     const float A2 = CAP ? 2.f * LOG2E * invc : 0.f;
     const float Kc = CAP ? s * p.softcap * LOG2E : 0.f;
-    const float XP = CAP ? HL_TANH_POLY_Y0 * p.softcap : 0.f;  // polynomial range on |x|
-    const f2 K2 = pk1(K1), A22 = pk1(A2), Kc2 = pk1(Kc), invc2 = pk1(invc);
+    // softcap: tanh by tiers, picked per chunk from the records' largest |x|:
+    // A = degree-3 odd polynomial on |x| <= 0.45 c (only while Kc <= 48,
+    // where its fit error stays below fp32 rounding of the exponentials),
+    // B = degree 5 on |x| <= 0.8 c, X = ex2 + rcp (any x)
+    const float XA = (CAP && Kc <= 48.f) ? HL_TANH_A_Y0 * p.softcap : 0.f;
+    const float XB = CAP ? HL_TANH_B_Y0 * p.softcap : 0.f;
+    // zs = x Q(x^2) with Q_k = s log2(e) C_k / c^(2k), formed in double
+    f2 QA[4], QB[6];
+    {
+        const double ic2 = CAP ? 1.0 / (double(p.softcap) * double(p.softcap)) : 0.0;
+        const double ca[4] = {HL_TANH_A_C0, HL_TANH_A_C1, HL_TANH_A_C2, HL_TANH_A_C3};
+        const double cb[6] = {HL_TANH_B_C0, HL_TANH_B_C1, HL_TANH_B_C2,
+                              HL_TANH_B_C3, HL_TANH_B_C4, HL_TANH_B_C5};
+        double f = double(s) * 1.4426950408889634;
+#pragma unroll
+        for (int k = 0; k < 6; ++k) {
+            if (k < 4) QA[k] = pk1(float(ca[k] * f));
+            QB[k] = pk1(float(cb[k] * f));
+            f *= ic2;
+        }
+    }
+    // 1 - tanh^2 = 1 - (zs / Kc)^2 on the polynomial tiers (|tanh| <= 0.67)
+    const f2 mKc2 = pk1(CAP ? -1.f / (Kc * Kc) : 0.f), one2 = pk1(1.f);
+    const f2 K2 = pk1(K1), A22 = pk1(A2), Kc2 = pk1(Kc);
     auto zs1 = [&](float v, float* om) -> float {
         return CAP ? __fmul_rn(tanh_a2x_1(__fmul_rn(v, A2), om), Kc) : __fmul_rn(v, K1);
     };
 
     for (int i = lane; i < 2 * NACC; i += 32) accs[warp][i] = 0.f;
-    __syncwarp();
 
     const int64_t gw = int64_t(blockIdx.x) * OP_WARPS + warp;
     const int64_t nw = int64_t(gridDim.x) * OP_WARPS;
+    const int64_t nunits = N * OP_PARTS;
+
+    // This warp's ring: its units' words stream through OP_SLOTS chunks of
+    // shared memory by bulk copies (lane 0 issues, an mbarrier per slot
+    // counts the bytes), refilled as soon as the warp has used a chunk and
+    // running on across units, so the copies OP_SLOTS chunks ahead are always
+    // in flight whatever the arithmetic is doing.
+    unsigned char* ring = ring_smem + size_t(warp) * OP_SLOTS * OP_CHUNK_WORDS * 16;
+    uint64_t* fullb = reinterpret_cast<uint64_t*>(ring_smem + size_t(OP_WARPS) * OP_SLOTS *
+                                                                  OP_CHUNK_WORDS * 16) +
+                      warp * OP_SLOTS;
+    auto unit_range = [&](int64_t uu, int64_t& rr, int64_t& b0, int64_t& b1) {
+        rr = uu / OP_PARTS;
+        const int pt = int(uu - rr * OP_PARTS);
+        b0 = nwords * pt / OP_PARTS;
+        b1 = nwords * (pt + 1) / OP_PARTS;
+    };
+    // the issuer's stream position (lane 0): unit iu, chunk ic of it
+    int64_t iu = gw;
+    int64_t ic = 0;
+    auto issue_next = [&](int sl) {
+        if (iu >= nunits) return;
+        int64_t rr, b0, b1;
+        unit_range(iu, rr, b0, b1);
+        const int64_t c0 = b0 + ic * OP_CHUNK_WORDS;
+        const int64_t cw = (b1 - c0) < OP_CHUNK_WORDS ? (b1 - c0) : OP_CHUNK_WORDS;
+        const uint32_t bar = smem_addr(&fullb[sl]);
+        mbar_arrive_expect_tx(bar, uint32_t(cw * 16));
+        bulk_g2s(smem_addr(ring + size_t(sl) * OP_CHUNK_WORDS * 16), xg + rr * V + c0 * EPW,
+                 uint32_t(cw * 16), bar);
+        if (c0 + OP_CHUNK_WORDS >= b1) {
+            iu += nw;
+            ic = 0;
+        } else {
+            ++ic;
+        }
+    };
+    if (lane == 0) {
+        for (int sl = 0; sl < OP_SLOTS; ++sl) mbar_init(smem_addr(&fullb[sl]), 1);
+        fence_mbar_init();
+        for (int sl = 0; sl < OP_SLOTS; ++sl) issue_next(sl);
+    }
+    __syncwarp();
+    int slot = 0;
+    uint32_t phase = 0;
+    uint32_t lost = 0, lost_par = 0;
+    // the next chunk of the stream: wait for it, hand back its base
+    auto acquire = [&]() -> const unsigned char* {
+        if (!mbar_wait_bounded(smem_addr(&fullb[slot]), phase, p.wait_ns)) {
+            lost |= 1u << slot;
+            lost_par = (lost_par & ~(1u << slot)) | (phase << slot);
+            if (lane == 0) atomicOr(p.err, E_TIMEOUT);
+        }
+        return ring + size_t(slot) * OP_CHUNK_WORDS * 16;
+    };
+    // the warp is done with the chunk: refill its slot, step the ring
+    auto release = [&]() {
+        __syncwarp();
+        if (lane == 0) {
+            fence_proxy_async();
+            issue_next(slot);
+        }
+        if (++slot == OP_SLOTS) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    };
     // unit u: row u / OP_PARTS, part u % OP_PARTS (a range of the row's words);
     // every part merges the row's records itself, part 0 adds the row's losses
-    for (int64_t u = gw; u < N * OP_PARTS; u += nw) {
+    for (int64_t u = gw; u < nunits; u += nw) {
         const int64_t r = u / OP_PARTS;
         const int part = int(u - r * OP_PARTS);
         const int64_t wb = nwords * part / OP_PARTS, we = nwords * (part + 1) / OP_PARTS;
+        const int64_t nch = (we - wb + OP_CHUNK_WORDS - 1) / OP_CHUNK_WORDS;
         int64_t y = 0;
         float old_lp = 0.f, adv = 0.f;
         if (lane == 0) {
@@ -96,38 +195,69 @@ __global__ void __launch_bounds__(OP_THREADS, 3) onepass_kernel16(const __grid_c
         const bool valid = !has_labels || (y >= 0 && y < V);
         if (has_labels && y >= V && lane == 0 && part == 0) atomicOr(p.err, E_LABEL);
         __nv_bfloat16* grow = gg != nullptr ? gg + r * V : nullptr;
-        if (!valid) {  // a masked row: exact +0 (kept when accumulating)
+        if (!valid) {  // a masked row: exact +0 (kept when accumulating); its chunks pass by
             if (lane == 0 && part == 0) write_row_zero(p, r);
             if (grow != nullptr && !p.accumulate)
                 for (int64_t w = wb + lane; w < we; w += 32)
                     *reinterpret_cast<uint4*>(grow + w * EPW) = make_uint4(0, 0, 0, 0);
+            for (int64_t c = 0; c < nch; ++c) {
+                acquire();
+                release();
+            }
             continue;
         }
 
-        // ---- merge the tiles' records: lane k takes tiles k, k + 32, ... ----
+        // ---- merge the tiles' records: part warp pt, lane k takes tiles
+        // pt 32 + k + 128 j (four loads in flight per lane), then lane k of
+        // every part warp merges the four parts' records of lane k ----
         float M = -CUDART_INF_F, S = 0.f, E = 0.f;
-        const float4* rrow = rs + r * NT;
-        for (int t = lane; t < NT; t += 32) {
-            const float4 q = rrow[t];
-            if (!(q.y > 0.f)) continue;
-            if (q.x > M) {
-                const float d = M == -CUDART_INF_F ? 0.f : M - q.x;  // <= 0
+        auto merge_in = [&](float qm, float qs, float qe) {
+            if (!(qs > 0.f)) return;
+            if (qm > M) {
+                const float d = M == -CUDART_INF_F ? 0.f : M - qm;  // <= 0
                 const float al = exp2f(d);
-                if (ENT) E = al * (E + d * S) + q.z;
-                S = al * S + q.y;
-                M = q.x;
+                if (ENT) E = al * (E + d * S) + qe;
+                S = al * S + qs;
+                M = qm;
             } else {
-                const float d = q.x - M;
+                const float d = qm - M;
                 const float al = exp2f(d);
-                if (ENT) E += al * (q.z + d * q.y);
-                S += al * q.y;
+                if (ENT) E += al * (qe + d * qs);
+                S += al * qs;
             }
+        };
+        const float4* rrow = rs + r * NT;
+        for (int tb = part * 32 + lane; tb < NT; tb += 4 * 128) {
+            float4 q[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                q[j] = tb + 128 * j < NT ? rrow[tb + 128 * j] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) merge_in(q[j].x, q[j].y, q[j].z);
         }
         float zy = 0.f, hasy = 0.f;
         if (lane == 0 && has_labels) {
             zy = zs1(P16::to_f(reinterpret_cast<const uint16_t*>(xg)[r * V + y]), nullptr);
             hasy = 1.f;
         }
+        float(*mg)[3][32] = mrg[warp / OP_PARTS];
+        mg[part][0][lane] = M;
+        mg[part][1][lane] = S;
+        mg[part][2][lane] = E;
+        // the row's four warps (warps 0-3 or 4-7 of the CTA: the same rows in
+        // the same iterations) have all read the label logit and stored their
+        // records before any of them writes the gradient (in place, one of
+        // them overwrites the label logit), and all have read the records
+        // before any stores the next row's
+        const uint32_t gbar = 1 + (warp >> 2);
+        asm volatile("bar.sync %0, 128;" ::"r"(gbar) : "memory");
+        M = -CUDART_INF_F;
+        S = 0.f;
+        E = 0.f;
+#pragma unroll
+        for (int pt = 0; pt < OP_PARTS; ++pt)
+            merge_in(mg[pt][0][lane], mg[pt][1][lane], mg[pt][2][lane]);
+        asm volatile("bar.sync %0, 128;" ::"r"(gbar) : "memory");
         float* rec = recs[warp] + lane * NREC;
         rec[R_ZM] = M;
         rec[R_UM] = 0.f;
@@ -145,88 +275,142 @@ __global__ void __launch_bounds__(OP_THREADS, 3) onepass_kernel16(const __grid_c
             p, recs[warp], 32, false, old_lp, adv, accs[warp], lane, r, kk, &rls[warp]);
         __syncwarp();
         if (lane == 0 && part == 0) row_accumulate(p, rls[warp], accs[warp], r);
-        if (grow == nullptr) continue;
+        if (grow == nullptr) {
+            for (int64_t c = 0; c < nch; ++c) {
+                acquire();
+                release();
+            }
+            continue;
+        }
 
         // ---- the gradient, one read and one write of the row ----
         const ShiftCoef h = shift_coefs(k, ENTG);
         const f2 nlse2 = pk1(h.nlse), pc2 = pk1(h.pc), ps2 = pk1(h.ps);
-        const int64_t ywd = has_labels ? y / EPW : -1;
-        // one word of the row: its gradient, the label element patched
-        auto word = [&](int64_t w, const uint4& a, const uint4& ow) -> uint4 {
+        const int64_t ywd = has_labels ? y / EPW : -1;  // the label's word
+        const int iyw = has_labels ? int(y - ywd * EPW) : 0;
+        // softcap: the tier of chunk c of this unit (c < 32; later chunks take
+        // tier X): lane c takes the largest |x| of the tiles the chunk spans
+        uint32_t mA = 0u, mB = 0u;
+        if (CAP) {
+            float cx = 0.f;
+            if (lane < nch) {
+                const int64_t c0 = wb + int64_t(lane) * OP_CHUNK_WORDS;
+                const int64_t c1 = c0 + OP_CHUNK_WORDS < we ? c0 + OP_CHUNK_WORDS : we;
+                const int64_t t0 = c0 / 32, t1 = (c1 - 1) / 32;  // 32 words a tile
+                const float* xr = reinterpret_cast<const float*>(rrow) + 3;
+#pragma unroll
+                for (int i = 0; i <= OP_CHUNK_WORDS / 32; ++i)
+                    if (t0 + i <= t1) cx = fmaxf(cx, xr[4 * (t0 + i)]);
+            }
+            mA = __ballot_sync(0xffffffffu, cx <= XA);
+            mB = __ballot_sync(0xffffffffu, cx <= XB);
+        }
+        // one word's gradient in tier TI (-1: no softcap)
+        auto word = [&](const uint4& a, const uint4& ow, auto tierc) -> uint4 {
+            constexpr int TI = decltype(tierc)::value;
             const uint32_t xa[4] = {a.x, a.y, a.z, a.w};
             const uint32_t oa[4] = {ow.x, ow.y, ow.z, ow.w};
-            bool poly = true;
-            if (CAP) {
-                const uint32_t am = P16::absmax2(P16::absmax2(a.x, a.y), P16::absmax2(a.z, a.w));
-                float ca, cb;
-                upk(P16::unpack(am), ca, cb);
-                poly = fmaxf(fabsf(ca), fabsf(cb)) <= XP;
-            }
             uint32_t out[4];
 #pragma unroll
             for (int kq = 0; kq < 4; ++kq) {
                 const f2 xv = P16::unpack(xa[kq]);
-                f2 arg, omt = pk1(1.f);
-                if (CAP) {
-                    const TanhD2 td =
-                        poly ? tanh_poly2(mul2(xv, invc2)) : tanh_from_ex2_arg(mul2(xv, A22));
-                    arg = fma2(td.th, Kc2, nlse2);
-                    omt = td.omt;
-                } else {
+                f2 arg, omt = one2;
+                if constexpr (TI < 0) {
                     arg = fma2(xv, K2, nlse2);
+                } else if constexpr (TI <= 1) {
+                    const f2 u = mul2(xv, xv);
+                    f2 q;
+                    if constexpr (TI == 0) {
+                        q = fma2(u, QA[3], QA[2]);
+                        q = fma2(q, u, QA[1]);
+                        q = fma2(q, u, QA[0]);
+                    } else {
+                        q = fma2(u, QB[5], QB[4]);
+                        q = fma2(q, u, QB[3]);
+                        q = fma2(q, u, QB[2]);
+                        q = fma2(q, u, QB[1]);
+                        q = fma2(q, u, QB[0]);
+                    }
+                    const f2 zs = mul2(xv, q);
+                    omt = fma2(zs, mul2(zs, mKc2), one2);
+                    arg = add2(zs, nlse2);
+                } else {
+                    const TanhD2 td = tanh_from_ex2_arg(mul2(xv, A22));
+                    omt = td.omt;
+                    arg = fma2(td.th, Kc2, nlse2);
                 }
                 const f2 g = mul2(ex2p(arg), ENTG ? fma2(ps2, arg, pc2) : pc2);
                 const f2 gw = CAP ? mul2(g, omt) : g;
                 out[kq] = P16::pack(p.accumulate ? add2(P16::unpack(oa[kq]), gw) : gw);
             }
-            if (w == ywd) {
-                // the label column: its element again, with the label term
-                // (halves picked by selects, so the words stay in registers)
-                const int iy = int(y - w * EPW), qy = iy >> 1, sh = (iy & 1) * 16;
-                uint32_t xw = xa[0], owd = oa[0];
-#pragma unroll
-                for (int kq = 1; kq < 4; ++kq)
-                    if (kq == qy) {
-                        xw = xa[kq];
-                        owd = oa[kq];
-                    }
-                const float xv1 = P16::to_f(uint16_t(xw >> sh));
-                float om1 = 1.f;
-                const float zs = zs1(xv1, &om1);
-                const float arg = zs + h.nlse;
-                float g1 = ex2f(arg) * (ENTG ? fmaf(h.ps, arg, h.pc) : h.pc) - k.bc;
-                if (CAP) g1 *= om1;
-                if (p.accumulate) g1 += P16::to_f(uint16_t(owd >> sh));
-                const uint32_t hv = uint32_t(P16::from_f(g1)) << sh;
-                const uint32_t keep = sh ? 0x0000ffffu : 0xffff0000u;
-#pragma unroll
-                for (int kq = 0; kq < 4; ++kq)
-                    if (kq == qy) out[kq] = (out[kq] & keep) | hv;
-            }
             return make_uint4(out[0], out[1], out[2], out[3]);
         };
-        // OP_UNROLL words per lane per step: their loads are all in flight
-        // before the first is used
-        const __nv_bfloat16* xrow = xg + r * V;
-        for (int64_t w0 = wb + lane; w0 < we; w0 += 32 * OP_UNROLL) {
-            uint4 a[OP_UNROLL], ow[OP_UNROLL];
+        // the label column's element again, with the label term (halves
+        // picked by selects, so the words stay in registers)
+        auto patch = [&](const uint4& o, const uint4& a, const uint4& ow) -> uint4 {
+            const uint32_t xa[4] = {a.x, a.y, a.z, a.w};
+            const uint32_t oa[4] = {ow.x, ow.y, ow.z, ow.w};
+            uint32_t out[4] = {o.x, o.y, o.z, o.w};
+            const int qy = iyw >> 1, sh = (iyw & 1) * 16;
+            uint32_t xw = xa[0], owd = oa[0];
 #pragma unroll
-            for (int q = 0; q < OP_UNROLL; ++q) {
-                const int64_t w = w0 + 32 * q;
-                a[q] = make_uint4(0, 0, 0, 0);
-                ow[q] = make_uint4(0, 0, 0, 0);
-                if (w < we) {
-                    a[q] = *reinterpret_cast<const uint4*>(xrow + w * EPW);
-                    if (p.accumulate) ow[q] = *reinterpret_cast<const uint4*>(grow + w * EPW);
+            for (int kq = 1; kq < 4; ++kq)
+                if (kq == qy) {
+                    xw = xa[kq];
+                    owd = oa[kq];
                 }
-            }
+            const float xv1 = P16::to_f(uint16_t(xw >> sh));
+            float om1 = 1.f;
+            const float zs = zs1(xv1, &om1);
+            const float arg = zs + h.nlse;
+            float g1 = ex2f(arg) * (ENTG ? fmaf(h.ps, arg, h.pc) : h.pc) - k.bc;
+            if (CAP) g1 *= om1;
+            if (p.accumulate) g1 += P16::to_f(uint16_t(owd >> sh));
+            const uint32_t hv = uint32_t(P16::from_f(g1)) << sh;
+            const uint32_t keep = sh ? 0x0000ffffu : 0xffff0000u;
 #pragma unroll
-            for (int q = 0; q < OP_UNROLL; ++q) {
-                const int64_t w = w0 + 32 * q;
-                if (w < we) *reinterpret_cast<uint4*>(grow + w * EPW) = word(w, a[q], ow[q]);
+            for (int kq = 0; kq < 4; ++kq)
+                if (kq == qy) out[kq] = (out[kq] & keep) | hv;
+            return make_uint4(out[0], out[1], out[2], out[3]);
+        };
+        // one chunk from the ring: eight words a lane, unrolled; the words
+        // past a short chunk's end are computed and not stored
+        auto chunk = [&](const unsigned char* sb, __nv_bfloat16* gc, int cw, int jy, auto tierc) {
+#pragma unroll
+            for (int i = 0; i < OP_CHUNK_WORDS / 32; ++i) {
+                const int j = lane + 32 * i;
+                const uint4 a = *reinterpret_cast<const uint4*>(sb + size_t(j) * 16);
+                uint4 ow = make_uint4(0, 0, 0, 0);
+                if (p.accumulate && j < cw) ow = *reinterpret_cast<const uint4*>(gc + size_t(j) * EPW);
+                uint4 o = word(a, ow, tierc);
+                if (j == jy) o = patch(o, a, ow);
+                if (j < cw) *reinterpret_cast<uint4*>(gc + size_t(j) * EPW) = o;
             }
+        };
+        for (int64_t c = 0; c < nch; ++c) {
+            const unsigned char* sb = acquire();
+            const int64_t c0 = wb + c * OP_CHUNK_WORDS;
+            const int cw = int((we - c0) < OP_CHUNK_WORDS ? (we - c0) : OP_CHUNK_WORDS);
+            const int jy = (ywd >= c0 && ywd < c0 + cw) ? int(ywd - c0) : -1;
+            __nv_bfloat16* gc = grow + c0 * EPW;
+            if (!CAP) {
+                chunk(sb, gc, cw, jy, std::integral_constant<int, -1>{});
+            } else {
+                const bool inA = c < 32 && ((mA >> c) & 1u), inB = c < 32 && ((mB >> c) & 1u);
+                if (inA) chunk(sb, gc, cw, jy, std::integral_constant<int, 0>{});
+                else if (inB) chunk(sb, gc, cw, jy, std::integral_constant<int, 1>{});
+                else chunk(sb, gc, cw, jy, std::integral_constant<int, 2>{});
+            }
+            release();
         }
     }
+
+    // a slot whose wait gave up may still receive its copy: wait once more
+    // (bounded) before the CTA's shared memory goes away
+    if (lost && lane == 0)
+        for (int b = 0; b < OP_SLOTS; ++b)
+            if (lost & (1u << b))
+                (void)mbar_wait_bounded(smem_addr(&fullb[b]), (lost_par >> b) & 1u, p.wait_ns);
 
     // the warps' sums, in warp order, into the CTA's fp64 partial record
     __syncthreads();
@@ -254,5 +438,7 @@ const void* onepass_kernel_bf16(int feat) {
 }
 
 #undef HL_CASE
+
+int onepass_smem_bytes() { return OP_SMEM; }
 
 }  // namespace hl

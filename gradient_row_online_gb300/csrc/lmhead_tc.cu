@@ -198,8 +198,9 @@ __device__ __forceinline__ void tile_of(int i, int MT, int NT, int& m, int& n) {
 // Statistics of one (row, tile) from its bf16 logits.  MODE 0: (m, s) with
 // m the max logit and s = sum exp(x - m).  MODE 1: the loss's first-pass
 // record of the capped, scaled logits zs = s c tanh(x / c) log2(e) (c = 0:
-// s x log2(e)), base 2: (m2, S, E) with m2 = max zs, S = sum 2^(zs - m2),
-// E = sum 2^(zs - m2) (zs - m2).
+// s x log2(e)), base 2: (m2, S, E, X) with m2 = max zs, S = sum 2^(zs - m2),
+// E = sum 2^(zs - m2) (zs - m2) and X = max |x| (which picks the loss
+// kernel's tanh form).
 struct Xform {
     float c, invc, k;  // softcap (0: off), 1 / c, s * c * log2(e) (c = 0: s * log2(e))
 };
@@ -326,7 +327,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!wait_phase(su32(&tfull[acc]), uint32_t(j >> 1) & 1u, abort, err)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const uint32_t tbase = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc * BN);
-            float mx = -INFINITY, ssum = 0.f, esum = 0.f;
+            float mx = -INFINITY, ssum = 0.f, esum = 0.f, ax = 0.f;
             for (int g = 0; g < BN / OUT_COLS; ++g, ++step) {
                 unsigned char* ob = outb + (step & 1) * OUT_BYTES;
                 // the store that last read this buffer has finished reading it
@@ -344,7 +345,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         pk[t] = *reinterpret_cast<const uint32_t*>(&b2);
                         v[2 * t] = __low2float(b2);
                         v[2 * t + 1] = __high2float(b2);
-                        if (MODE == 1) {  // zs of the bf16 logits
+                        if (MODE == 1) {  // zs of the bf16 logits, their largest |x|
+                            ax = fmaxf(ax, fmaxf(fabsf(v[2 * t]), fabsf(v[2 * t + 1])));
                             v[2 * t] = xf.c > 0.f ? xf.k * tanhf(v[2 * t] * xf.invc) : xf.k * v[2 * t];
                             v[2 * t + 1] = xf.c > 0.f ? xf.k * tanhf(v[2 * t + 1] * xf.invc)
                                                       : xf.k * v[2 * t + 1];
@@ -394,7 +396,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (lane == 0) mbar_arrive(su32(&tempty[acc]));
             const size_t si = size_t(m * BM + 32 * q + lane) * NT + n;
             if (MODE == 0) static_cast<float2*>(stats_out)[si] = make_float2(mx, ssum);
-            else static_cast<float4*>(stats_out)[si] = make_float4(mx, ssum, esum, 0.f);
+            else static_cast<float4*>(stats_out)[si] = make_float4(mx, ssum, esum, ax);
         }
         if (lane == 0) bulk_wait_all();  // stores complete before shared memory is released
         __syncwarp();

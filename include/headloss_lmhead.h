@@ -63,8 +63,9 @@ int headloss_lmhead_logits(const void* hidden, const void* weight, int N, int D,
  * row_stats: N x (V / 256) records of 4 fp32, device, 16-byte aligned
  *            (written): for the bf16 logits x of row i and tile k, with
  *            zs = s c tanh(x / c) log2(e) (c = 0: zs = s x log2(e)),
- *            (m2, S, E, 0): m2 = max zs, S = sum 2^(zs - m2),
- *            E = sum 2^(zs - m2) (zs - m2).
+ *            (m2, S, E, X): m2 = max zs, S = sum 2^(zs - m2),
+ *            E = sum 2^(zs - m2) (zs - m2), X = max |x| (exact: the largest
+ *            magnitude among the tile's bf16 logits).
  * Other arguments, checks and errors as headloss_lmhead_logits (ERR_ARG also
  * for a negative or non-finite softcap, a non-positive logits_scale).
  */

@@ -236,3 +236,32 @@ def gspo_forward_backward(x, labels, old_logprobs, advantages, seg_offsets, clip
     scalars = np.array([loss, sum(sg[2] for sg in segs) / G, sum(sg[6] for sg in segs) / G,
                         float(G)])
     return scalars, coeff, grad
+
+
+def tile_records(x, softcap: float = 0.0, logits_scale: float = 1.0, tile: int = 256):
+    """The first-pass statistics of each (row, tile of ``tile`` columns), written out
+    plainly in fp64: the record the fused LM head's GEMM epilogue emits for the loss
+    (ServiceNow Fast-LLM PR #549, "Approach": the row's softmax statistics built up
+    block by block and merged by their running maximum; "Correctness": the LM head
+    computed in front of the loss).
+
+    With z = s c tanh(x / c) (c = 0: z = s x) and zs = z log2(e) (base 2):
+      m2 = max zs, S = sum 2^(zs - m2), E = sum 2^(zs - m2) (zs - m2), X = max |x|,
+    per tile.  Returns an N x (V / tile) x 4 array (m2, S, E, X)."""
+    x = _f64(x)
+    n, V = x.shape
+    if V % tile:
+        raise ValueError("V must be a multiple of the tile width")
+    z = logits_scale * (softcap * np.tanh(x / softcap) if softcap > 0 else x)
+    zs = z / math.log(2.0)
+    out = np.zeros((n, V // tile, 4))
+    for t in range(V // tile):
+        blk = zs[:, t * tile:(t + 1) * tile]
+        m2 = blk.max(axis=1)
+        d = blk - m2[:, None]
+        e = np.exp2(d)
+        out[:, t, 0] = m2
+        out[:, t, 1] = e.sum(axis=1)
+        out[:, t, 2] = (e * d).sum(axis=1)
+        out[:, t, 3] = np.abs(x[:, t * tile:(t + 1) * tile]).max(axis=1)
+    return out

@@ -430,3 +430,53 @@ def test_lm_head_scaling_identities():
     dda = (tot(1 + step) - tot(1 - step)) / (2 * step)
     assert abs(dda - np.sum(dW * wt)) < 1e-7 * max(1.0, abs(dda))
     assert abs(dda - np.sum(dH * hid)) < 1e-7 * max(1.0, abs(dda))
+
+
+# ------------------------------------------------- per-tile first-pass records
+
+def _merge_records(rec):
+    """Merge a row's tile records by their maxima (the block-wise online form)."""
+    M = rec[:, 0].max()
+    al = np.exp2(rec[:, 0] - M)
+    S = np.sum(al * rec[:, 1])
+    E = np.sum(al * (rec[:, 2] + (rec[:, 0] - M) * rec[:, 1]))
+    return M, S, E
+
+
+@pytest.mark.parametrize("softcap,scale", [(0.0, 1.0), (30.0, 0.5), (3.0, 0.7)])
+def test_tile_records_merge_to_the_row_oracle_lse_and_entropy(softcap, scale):
+    """Merged over a row's tiles, the records give the C row oracle's log-sum-exp
+    (ln 2 (m2 + log2 S)) and entropy (ln 2 (log2 S - E / S))."""
+    rng = np.random.default_rng(3)
+    n, V = 5, 1024
+    x = rng.normal(0.0, 3.0, (n, V))
+    labels = rng.integers(0, V, n).astype(np.int64)
+    rec = orc.tile_records(x, softcap, scale)
+    assert rec.shape == (n, 4, 4)
+    cfg = orc.make_cfg(orc.CE | orc.ENTROPY, dict(entropy=1.0), softcap=softcap,
+                       logits_scale=scale)
+    rr, _, _ = orc.rows(cfg, x, labels, want_grad=False)
+    for i in range(n):
+        M, S, E = _merge_records(rec[i])
+        assert abs(math.log(2) * (M + math.log2(S)) - rr[i, orc.RF["lse"]]) < 1e-12
+        H = math.log(2) * (math.log2(S) - E / S)
+        assert abs(H - rr[i, orc.RF["entropy"]]) < 1e-12
+
+
+def test_tile_records_closed_forms():
+    """A constant tile: S = 256, E = 0; a zero tile with one value b > 0 at
+    scale s (no softcap): m2 = s b log2 e, S = 1 + 255 2^-m2, E = -255 m2 2^-m2;
+    X is the largest magnitude, whatever its sign."""
+    x = np.zeros((2, 512))
+    x[0, :256] = -1.5
+    x[0, 256:] = 0.0
+    x[1, 7] = 2.0
+    x[1, 300] = -4.0
+    rec = orc.tile_records(x, 0.0, 0.5)
+    l2e = 1.0 / math.log(2.0)
+    np.testing.assert_allclose(rec[0, 0], [-0.75 * l2e, 256.0, 0.0, 1.5], rtol=1e-15, atol=0)
+    m2 = 1.0 * l2e
+    np.testing.assert_allclose(rec[1, 0], [m2, 1 + 255 * 2 ** -m2, -255 * m2 * 2 ** -m2, 2.0],
+                               rtol=1e-14)
+    assert rec[1, 1, 3] == 4.0
+    assert rec[1, 1, 0] == 0.0  # the largest zs of tile 1 is a zero logit

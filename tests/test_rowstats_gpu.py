@@ -107,3 +107,33 @@ def test_rowstats_rejects_what_it_does_not_cover():
            None, out)
     assert e.value.status == hlb.HEADLOSS_ERR_ALIGN
     h2.close()
+
+
+@pytest.mark.parametrize("softcap,scale", [(0.0, 1.0), (30.0, 0.5), (3.0, 0.7)])
+def test_gemm_tile_records_against_oracle(softcap, scale):
+    """The GEMM epilogue's per-tile records (m2, S, E, X) against the oracle's
+    plain definition on the same (seeded, identity-reproduced) logits: X exactly
+    (the largest |bf16 logit|), the rest within fp32 rounding of 256-term sums
+    of exponentials (relative 2e-5; E against 2e-5 (S + |E|): all its terms
+    share one sign)."""
+    import oracle as orc
+    N, V = 256, 4096
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    x = (torch.randn(N, V, generator=g, device="cuda") * 3.0).to(torch.bfloat16)
+    x[5, 100:356] = 0.0  # a constant tile
+    x[9, 1000] = 200.0   # a saturating logit
+    eye = torch.eye(V, dtype=torch.bfloat16, device="cuda")
+    logits = torch.empty_like(x)
+    rs = torch.full((N, V // 256, 4), float("nan"), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hlb.headloss_lmhead_logits_rowstats(x, eye, N, V, V, softcap, scale, logits, rs, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(logits.view(torch.int16), x.view(torch.int16))
+    got = rs.double().cpu().numpy()
+    ref = orc.tile_records(x.float().cpu().numpy(), softcap, scale)
+    np.testing.assert_array_equal(got[..., 3], ref[..., 3])
+    np.testing.assert_allclose(got[..., 0], ref[..., 0], rtol=2e-5, atol=2e-5)
+    np.testing.assert_allclose(got[..., 1], ref[..., 1], rtol=2e-5, atol=0)
+    assert np.all(np.abs(got[..., 2] - ref[..., 2]) <= 2e-5 * (ref[..., 1] + np.abs(ref[..., 2])))
