@@ -194,7 +194,14 @@ const void* kernel_for(int kind, int dtype, int feat) {
     switch (dtype) {
         case HEADLOSS_BF16: return rows_kernel_bf16(feat & F_BASE);
         case HEADLOSS_FP16: return rows_kernel_fp16(feat & F_BASE);
-        case HEADLOSS_FP32: return rows_kernel_fp32(feat & F_BASE);
+        case HEADLOSS_FP32:
+            // double-float arithmetic where fp32 pairs carry the precision: no
+            // teacher, no softcap, no entropy gradient term, and no
+            // accumulation (each term is good to ~2^-26 of itself, which an
+            // existing value of the opposite sign could leave exposed)
+            return rows_kernel_fp32(
+                (feat & F_BASE) |
+                ((acc || (feat & (F_TEACH | F_SOFTCAP | F_ENTG))) ? 0 : int(F_DF)));
         default: return nullptr;
     }
 }

@@ -18,6 +18,10 @@ enum : int {
     // accumulating instantiation, which carries F_DCE / F_ENTG whenever
     // F_TEACH / F_ENT)
     F_ACC = 64,
+    // fp32 row kernel only: per-element arithmetic in double-float (fp32
+    // pairs) instead of fp64; for student-only rows without softcap whose
+    // gradient has no entropy term (the entropy may still be a metric)
+    F_DF = 128,
 };
 
 // Loss / metric bits (values match enum headloss_flag).

@@ -33,6 +33,7 @@
 #include <math_constants.h>
 #include <stdint.h>
 
+#include "hl_df.cuh"
 #include "hl_params.h"
 
 namespace hl {
@@ -290,10 +291,19 @@ enum Coef { K_LSE2, K_LSET2, K_LSQ2, K_PC, K_PS, K_TC, K_TS, K_QC, K_BC, NCOEF }
 
 // Merges the C partial records (rank order), derives the row's losses,
 // accumulates them (rank 0 only) and writes the gradient coefficients.
-// Runs on one thread.
-template <typename A, bool TEACH, bool RKL, bool ENT, bool CAP>
+// Runs on one thread.  DFX (fp64 rows of the double-float kernel): its
+// exponentials, logarithm and reciprocals through fp32 operations with
+// fp64 corrections (hl_df.cuh) instead of fp64 library calls, which are slow
+// on GB300; errors stay relative to the quantities that may cancel (the
+// largest record's weight is exactly 1, log2 S near S = 1 is small).
+template <typename A, bool TEACH, bool RKL, bool ENT, bool CAP, bool DFX = false>
 __device__ void row_epilogue(const Params& p, const A* recs, int C, bool accumulate,
                              float old_lp, float adv, double* acc, A* coef, int64_t row) {
+    static_assert(!DFX || (sizeof(A) == 8 && !TEACH && !CAP), "double-float epilogue");
+    auto ex2_ = [](A v) -> A {
+        if constexpr (DFX) return A(df_exp2d(double(v)));
+        else return ex2(v);
+    };
     const A LN2 = A(0.6931471805599453);
     const A invT = A(1) / A(p.T);
     A M = A(-CUDART_INF), Mu = A(-CUDART_INF);
@@ -310,7 +320,7 @@ __device__ void row_epilogue(const Params& p, const A* recs, int C, bool accumul
         if (r[R_HASY] > A(0)) zy = r[R_ZY];
         if (!(r[R_S] > A(0))) continue;
         const A d = r[R_ZM] - M;
-        const A al = ex2(d);
+        const A al = ex2_(d);
         S += al * r[R_S];
         if (ENT) E += al * (r[R_E] + d * r[R_S]);
         if (TEACH) {
@@ -326,12 +336,21 @@ __device__ void row_epilogue(const Params& p, const A* recs, int C, bool accumul
         }
     }
     const uint32_t f = p.flags;
-    const A lS = lg2(S);
+    A lS;
+    if constexpr (DFX) lS = A(df_log2d(double(S)));
+    else lS = lg2(S);
     const A lse2 = M + lS;
     const A lse = lse2 * LN2;
-    const double k = double(p.grad_scale) / (p.divisor > 0.0 ? p.divisor : double(*p.n_valid));
+    const double nv = p.divisor > 0.0 ? p.divisor : double(*p.n_valid);
+    double k;
+    if constexpr (DFX) k = double(p.grad_scale) * df_recipd(nv);
+    else k = double(p.grad_scale) / nv;
     A H = 0, lST = 0, lSq = 0, dce = 0, fkl = 0, rkl = 0;
-    if (ENT) H = LN2 * (lS - E / S);
+    if constexpr (DFX) {
+        if (ENT) H = LN2 * (lS - E * A(df_recipd(double(S))));
+    } else {
+        if (ENT) H = LN2 * (lS - E / S);
+    }
     if (TEACH) {
         lST = lg2(ST);
         lSq = lg2(Sq);
@@ -352,7 +371,8 @@ __device__ void row_epilogue(const Params& p, const A* recs, int C, bool accumul
         const A eps = A(p.eps);
         lp = (zy - lse2) * LN2;
         const A lr = lp - A(old_lp);
-        rho = ex(lr);
+        if constexpr (DFX) rho = A(df_exp2d(double(lr) * (1.0 / DF_LN2)));
+        else rho = ex(lr);
         A rho_c = rho < A(1) - eps ? A(1) - eps : rho;
         rho_c = rho_c > A(1) + eps ? A(1) + eps : rho_c;
         const A unc = rho * A(adv), clp = rho_c * A(adv);

@@ -20,6 +20,8 @@ const void* rows_kernel_fp32(int feat) {
         HL_CASE(F_SOFTCAP | F_TEACH | F_ENT)
         HL_CASE(F_SOFTCAP | F_TEACH | F_RKL)
         HL_CASE(F_SOFTCAP | F_TEACH | F_RKL | F_ENT)
+        HL_CASE(F_DF)
+        HL_CASE(F_DF | F_ENT)
         default: return nullptr;
     }
 }

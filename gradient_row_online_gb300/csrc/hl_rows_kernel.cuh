@@ -1,6 +1,7 @@
 // hl_rows_kernel.cuh -- the persistent cluster-per-row kernel (see hl_rows.cuh
 // for the row pipeline and the sources it follows).
 #pragma once
+#include "hl_df.cuh"
 #include "hl_rows.cuh"
 
 namespace hl {
@@ -16,6 +17,9 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
     constexpr bool ENT = (FEAT & F_ENT) != 0;
     constexpr bool CAP = (FEAT & F_SOFTCAP) != 0;
     constexpr int OPS = TEACH ? 2 : 1;
+    // double-float element arithmetic (fp32 logits, no teacher, no softcap)
+    constexpr bool DFM = (FEAT & F_DF) != 0;
+    static_assert(!DFM || (sizeof(DT) == 4 && !TEACH && !CAP), "double-float feature set");
 
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -56,6 +60,12 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
     const A KT = LOG2E * invT;                             // us = t * KT
 
     auto zs_of = [&](A v) -> A { return CAP ? mul_rn(tnh(v * invc), Kc) : mul_rn(v, K); };
+    // double-float split of an fp64 value (hi = its rounding, lo = the rest)
+    auto split = [](double v) -> DF {
+        const float h = float(v);
+        return {h, float(v - double(h))};
+    };
+    const DF Kd = split(double(K));
 
     if (tid == 0) {
         for (int b = 0; b < p.nbuf; ++b) mbar_init(smem_addr(&bars[b]), 1);
@@ -159,6 +169,21 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
         if (valid) {
             // ---- pass A: slice max of raw student / teacher logits ----
             A mx[2] = {A(-CUDART_INF), A(-CUDART_INF)};
+            if constexpr (DFM) {
+                // fp32 compares (exact), one fp32 block maximum
+                float m1[1] = {-CUDART_INF_F};
+                for (int w = tid; w < nw; w += nthr) {
+                    const int64_t eb = (wf + w) * EPW;
+                    const bool full = eb >= e0 && eb + EPW <= e1;
+                    const float4 q4 = *reinterpret_cast<const float4*>(xs_b + size_t(w) * 16);
+                    const float vv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                    for (int i = 0; i < EPW; ++i)
+                        if (full || (eb + i >= e0 && eb + i < e1)) m1[0] = fmaxf(m1[0], vv[i]);
+                }
+                block_max<float, 1>(m1, reinterpret_cast<float*>(red), lane, warp);
+                mx[0] = A(m1[0]);
+            } else {
             for (int w = tid; w < nw; w += nthr) {
                 const int64_t eb = (wf + w) * EPW;
                 const bool full = eb >= e0 && eb + EPW <= e1;
@@ -175,9 +200,11 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
                 }
             }
             block_max<A, 2>(mx, red, lane, warp);
+            }
             if (tid == 0) {
                 coef[0] = nonempty ? zs_of(mx[0]) : A(-CUDART_INF);
                 coef[1] = (TEACH && nonempty) ? mul_rn(mx[1], KT) : A(-CUDART_INF);
+                if (DFM) coef[2] = mx[0];  // the raw maximum, for the double-float shift
             }
             __syncthreads();
             const A zm = coef[0], um = coef[1];
@@ -187,6 +214,84 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
             // Sq = sum 2^du, Eq = sum 2^du du (du = us - um);
             // Xp = sum 2^du (du - d/T);  Y = -sum 2^(d/T) (du - d/T).
             A sm[7] = {A(0), A(0), A(0), A(0), A(0), A(0), A(0)};
+            if constexpr (DFM) {
+                // S and E in double-float per thread: each term 2^d from
+                // d = v K - v_max K formed to ~2^-48 (and exactly 0 at the
+                // maximum, whose product is formed the same way: a one-column
+                // row's CE is then exactly 0), summed by two-sums; terms below
+                // 2^-126 (beside the maximum's 1) are dropped.  The shift
+                // differs from the record's fp64 zm by ~2^-48 |zm|.
+                const float vmax = float(coef[2]);
+                DF Zd = df_two_prod(vmax, Kd.h);
+                Zd.l = __fmaf_rn(vmax, Kd.l, Zd.l);
+                float Sh = 0.f, Sl = 0.f, Eh = 0.f, El = 0.f;
+                for (int w = tid; w < nw; w += nthr) {
+                    const int64_t eb = (wf + w) * EPW;
+                    const bool full = eb >= e0 && eb + EPW <= e1;
+                    const float4 q4 = *reinterpret_cast<const float4*>(xs_b + size_t(w) * 16);
+                    const float vv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                    for (int i = 0; i < EPW; ++i) {
+                        if (!(full || (eb + i >= e0 && eb + i < e1))) continue;
+                        const DF d = df_scaled_minus(vv[i], Kd, Zd);
+                        int n;
+                        const DF e = df_exp2(d, n);
+                        if (n < -126) continue;
+                        const float sc = df_pow2i(n);
+                        const float eh = __fmul_rn(e.h, sc), el = __fmul_rn(e.l, sc);
+                        const DF s2 = df_two_sum(Sh, eh);
+                        Sh = s2.h;
+                        Sl = __fadd_rn(Sl, __fadd_rn(s2.l, el));
+                        if (ENT) {
+                            DF pe = df_two_prod(eh, d.h);
+                            pe.l = __fmaf_rn(eh, d.l, __fmaf_rn(el, d.h, pe.l));
+                            const DF e2 = df_two_sum(Eh, pe.h);
+                            Eh = e2.h;
+                            El = __fadd_rn(El, __fadd_rn(e2.l, pe.l));
+                        }
+                    }
+                }
+                // block sums in double-float (fp32 shuffles and two-sums),
+                // converted to fp64 once, by warp 0
+                auto add_df = [](float& h, float& l, float oh, float ol) {
+                    const DF t = df_two_sum(h, oh);
+                    h = t.h;
+                    l = __fadd_rn(l, __fadd_rn(t.l, ol));
+                };
+                float* rf = reinterpret_cast<float*>(red);
+#pragma unroll
+                for (int o = 16; o; o >>= 1) {
+                    add_df(Sh, Sl, __shfl_xor_sync(0xffffffffu, Sh, o),
+                           __shfl_xor_sync(0xffffffffu, Sl, o));
+                    if (ENT)
+                        add_df(Eh, El, __shfl_xor_sync(0xffffffffu, Eh, o),
+                               __shfl_xor_sync(0xffffffffu, El, o));
+                }
+                if (lane == 0) {
+                    rf[4 * warp] = Sh;
+                    rf[4 * warp + 1] = Sl;
+                    rf[4 * warp + 2] = Eh;
+                    rf[4 * warp + 3] = El;
+                }
+                __syncthreads();
+                if (warp == 0) {
+                    const int nwarps = nthr >> 5;
+                    Sh = lane < nwarps ? rf[4 * lane] : 0.f;
+                    Sl = lane < nwarps ? rf[4 * lane + 1] : 0.f;
+                    Eh = lane < nwarps ? rf[4 * lane + 2] : 0.f;
+                    El = lane < nwarps ? rf[4 * lane + 3] : 0.f;
+#pragma unroll
+                    for (int o = 16; o; o >>= 1) {
+                        add_df(Sh, Sl, __shfl_xor_sync(0xffffffffu, Sh, o),
+                               __shfl_xor_sync(0xffffffffu, Sl, o));
+                        if (ENT)
+                            add_df(Eh, El, __shfl_xor_sync(0xffffffffu, Eh, o),
+                                   __shfl_xor_sync(0xffffffffu, El, o));
+                    }
+                    sm[0] = double(Sh) + double(Sl);
+                    if (ENT) sm[1] = double(Eh) + double(El);
+                }
+            } else {
             for (int w = tid; w < nw; w += nthr) {
                 const int64_t eb = (wf + w) * EPW;
                 const bool full = eb >= e0 && eb + EPW <= e1;
@@ -216,6 +321,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
                 }
             }
             block_sum<A, 7>(sm, red, lane, warp);
+            }
             A* myrec = xch + ((xc & 1) * MAX_CLUSTER + rank) * NREC;
             if (tid == 0) {
                 A rec[NREC];
@@ -249,7 +355,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
             }
             if (C > 1) cluster_barrier();
             if (tid == 0) {
-                row_epilogue<A, TEACH, RKL, ENT, CAP>(p, xch + (xc & 1) * MAX_CLUSTER * NREC, C,
+                row_epilogue<A, TEACH, RKL, ENT, CAP, DFM>(p, xch + (xc & 1) * MAX_CLUSTER * NREC, C,
                                                       rank == 0, old_lp, adv, acc, coef, r);
                 if (p.tok != nullptr) {  // per-token coefficient on the label column
                     // (the scale is in the coefficients only without softcap;
@@ -284,6 +390,51 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
             }
             const A dlse = lseT2 - lsq2;
             const int64_t ey = (has_labels && valid && y >= col0 && y < col1) ? r * V + y : -1;
+            if (DFM && !p.accumulate) {
+                // double-float kernel: fp32 words in and out.  Non-label
+                // elements: pc 2^(v K - lse2) in double-float, rounded once
+                // (then scaled by 2^n, exactly while normal); the label
+                // element in fp64 (it subtracts bc and may cancel).
+                // (Accumulating calls take the fp64 kernel; this branch never
+                // sees one.)
+                const DF Ld = split(double(lse2)), Pd = split(double(pc));
+                for (int w = tid; w < nw; w += nthr) {
+                    const int64_t eb = (wf + w) * EPW;
+                    const bool full = eb >= e0 && eb + EPW <= e1;
+                    float out[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (valid) {
+                        const float4 q4 = *reinterpret_cast<const float4*>(xs_b + size_t(w) * 16);
+                        const float vv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                        for (int i = 0; i < EPW; ++i) {
+                            const DF d = df_scaled_minus(vv[i], Kd, Ld);
+                            int n;
+                            const DF e = df_exp2(d, n);
+                            DF g = df_two_prod(Pd.h, e.h);
+                            g.l = __fmaf_rn(Pd.h, e.l, __fmaf_rn(Pd.l, e.h, g.l));
+                            const float rr = __fadd_rn(g.h, g.l);
+                            out[i] = n >= -126 ? __fmul_rn(rr, df_pow2i(n))
+                                               : (n >= -300 ? ldexpf(rr, n) : 0.f);
+                        }
+                        if (ey >= eb && ey < eb + EPW) {
+                            const int i = int(ey - eb);
+                            const float vy = i == 0 ? vv[0] : i == 1 ? vv[1] : i == 2 ? vv[2] : vv[3];
+                            const float gy =
+                                __double2float_rn(ex2(mul_rn(A(vy), K) - lse2) * pc - bc);
+#pragma unroll
+                            for (int k = 0; k < EPW; ++k)
+                                if (k == i) out[k] = gy;
+                        }
+                    }
+                    if (full) {
+                        *reinterpret_cast<float4*>(gg + eb) = make_float4(out[0], out[1], out[2], out[3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < EPW; ++i)
+                            if (eb + i >= e0 && eb + i < e1) gg[eb + i] = out[i];
+                    }
+                }
+            } else
             for (int w = tid; w < nw; w += nthr) {
                 const int64_t eb = (wf + w) * EPW;
                 const bool full = eb >= e0 && eb + EPW <= e1;

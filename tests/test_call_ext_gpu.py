@@ -32,6 +32,9 @@ CASES = [
     (("ce", "grpo", "grpo_stats", "dist_ce", "rkl", "entropy"), torch.float32, 20.0, None),
     (("ce", "z", "fkl", "rkl", "entropy"), torch.float16, 30.0,
      dict(kernel=STREAM, stages=2, threads=512, chunk_words=1)),
+    # fp32 without teacher, softcap or entropy: the double-float kernel
+    (("ce", "z", "grpo", "grpo_stats"), torch.float32, 0.0, None),
+    (("ce", "grpo"), torch.float32, 0.0, dict(kernel=RESIDENT, cluster=2, stages=1, threads=256)),
 ]
 
 

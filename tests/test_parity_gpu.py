@@ -171,6 +171,61 @@ def test_stream_plan_in_place_takes_resident(words):
                inplace=True)
 
 
+# fp32 logits without a teacher, softcap or entropy gradient take the
+# double-float kernel (fp32 pairs instead of fp64): every loss subset, three
+# scales, ragged rows, structured rows (ramps, +300 offsets, spikes, wide
+# noise: many terms far below the maximum and subnormal gradients), forced
+# cluster plans, and logits far apart (sigma 1e4); same tolerances as fp64
+DF_LOSSES = ("ce", "z", "grpo", "grpo_stats", "entropy")
+DF_SUBSETS = [c for r in range(1, 6) for c in itertools.combinations(DF_LOSSES, r)]
+NO_ENT_GRAD = dict(FULL_W, entropy=0.0)
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.6, 1.7])
+def test_fp32_double_float_every_subset(scale):
+    for losses in DF_SUBSETS:
+        full_check(small(losses, N=40, V=1031, dtype=torch.float32, logits_scale=scale,
+                         sigma=5.0, seed=len(losses), weights=NO_ENT_GRAD))
+
+
+@pytest.mark.parametrize("V", [1, 2, 7, 1023, 1024, 32001])
+def test_fp32_double_float_ragged(V):
+    full_check(small(DF_LOSSES, N=19, V=V, dtype=torch.float32, weights=NO_ENT_GRAD))
+
+
+@pytest.mark.parametrize("plan", [None, dict(kernel=RESIDENT, cluster=2, stages=2, threads=256),
+                                  dict(kernel=RESIDENT, cluster=4, stages=1, threads=512),
+                                  dict(kernel=RESIDENT, cluster=1, stages=1, threads=512)])
+@pytest.mark.parametrize("scale", [1.0, 0.7])
+def test_fp32_double_float_structured_rows(plan, scale):
+    wl = small(DF_LOSSES, N=24, V=4100, dtype=torch.float32, logits_scale=scale,
+               weights=NO_ENT_GRAD)
+    structured_check(wl, plan=plan)
+    structured_check(wl.replace(losses=("ce", "z")), plan=plan)
+
+
+@pytest.mark.parametrize("losses", [("ce", "z"), ("ce", "grpo", "grpo_stats", "entropy")])
+def test_fp32_double_float_confident_rows(losses):
+    """Rows whose label logit leads by 4 .. 36: p(label) up to 1 - 1e-8, so the
+    label element pc p - bc cancels; it is held to the cancellation bound."""
+    wl = small(losses, N=36, V=1000, dtype=torch.float32, sigma=1.0, weights=NO_ENT_GRAD)
+    inp = W.make_inputs(wl, "cuda")
+    lab = inp["labels"]
+    rows = torch.nonzero(lab >= 0)[:, 0]
+    margin = 4.0 + (rows % 10).to(torch.float32) * 3.5
+    inp["logits"][rows, lab[rows]] += margin
+    got, g, _ = H.run_gpu(wl, inp)
+    cfg, rec, ref, gmag = H.oracle_rows(wl, inp)
+    H.check_scalars(wl, got, cfg, rec)
+    H.check_grad(wl, g, ref, gmag, rec)
+
+
+def test_fp32_double_float_far_apart_logits():
+    full_check(small(("ce", "z", "grpo", "grpo_stats", "entropy"), N=8, V=513,
+                     dtype=torch.float32, sigma=1e4, weights=NO_ENT_GRAD))
+    full_check(small(("ce",), N=30, V=2000, dtype=torch.float32, sigma=40.0))
+
+
 def test_large_logits_fp32():
     wl = small(("ce", "z", "entropy", "fkl", "rkl"), N=8, V=513, dtype=torch.float32,
                sigma=1e4)
