@@ -340,6 +340,7 @@ def run_ours(args, rank, world, local):
     if not args.no_lmhead and world == 1:
         line["lm_head_gemm"] = lm_head_gemm(args, dev)
         line["lm_head_loss"] = lm_head_loss(args, dev, peak)
+        line["lm_head_loss_distill"] = lm_head_loss_distill(args, dev, peak)
     if not args.no_e2e:
         del grad
         line["e2e"] = e2e(wl, h, inp, args, dev, world)
@@ -508,6 +509,100 @@ def host_link_bandwidth(dev, gib=2, reps=3):
     return {"h2d_gbs": n / t_h2d / 1e9, "d2h_gbs": n / t_d2h / 1e9,
             "both_directions_gbs": 2 * n / t_both / 1e9,
             "how": f"pinned {gib} GiB copies, best of {reps}, wall clock around a synchronize"}
+
+
+def lm_head_loss_distill(args, dev, peak, steps=6):
+    """The fused LM head with a teacher: the student's GEMM emits its per-tile
+    records and sums at the temperature, the teacher's GEMM its records, and
+    the loss makes one read of both logits and one write of the gradient per
+    row (headloss_forward_backward_rowstats), against the two GEMMs plus the
+    two-pass call on their logits.  Loss set: the all-in set (CE, z, forward KL
+    at T 1.5, GRPO with statistics, entropy; softcap 30, scale 0.5); the
+    single-pass kernel's HBM roofline beside."""
+    import gradient_row_online_gb300 as pkg
+    from gradient_row_online_gb300 import headloss as hlb
+    import torch.nn.functional as F
+
+    N, D, V = (int(v) for v in args.lmhead_shape.split(","))
+    T, softcap, scale = 1.5, 30.0, 0.5
+    g = torch.Generator(device=dev)
+    g.manual_seed(2)
+    hid = torch.randn(N, D, generator=g, device=dev).to(torch.bfloat16)
+    wt = (torch.randn(V, D, generator=g, device=dev) * (9.0 / D) ** 0.5).to(torch.bfloat16)
+    # the teacher: the student's weights plus a perturbation (logit noise ~1)
+    wt_t = (wt.float() + torch.randn(V, D, generator=g, device=dev) * (1.0 / D) ** 0.5).to(
+        torch.bfloat16)
+    labels = torch.randint(0, V, (N,), generator=g, device=dev)
+    labels[torch.rand(N, generator=g, device=dev) < 0.1] = -100
+    adv = torch.randn(N // 1024 + 1, generator=g, device=dev).repeat_interleave(1024)[:N].contiguous()
+    logits = torch.empty(N, V, dtype=torch.bfloat16, device=dev)
+    tlog = torch.empty_like(logits)
+    grad = torch.empty_like(logits)
+    NT = V // 256
+    rs = torch.empty(N, NT, 4, device=dev)
+    rsT = torch.empty(N, NT, device=dev)
+    trs = torch.empty(N, NT, 4, device=dev)
+    st2 = torch.empty(N, NT, 2, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty(16, device=dev)
+    losses = ("ce", "z", "fkl", "grpo", "grpo_stats", "entropy")
+    h = pkg.HeadLoss(pkg.flags_of(losses), hlb.make_weights(ce=1.0, z=1e-4, fkl=0.5, grpo=1.0),
+                     T, 0.2, softcap, scale)
+    s = torch.cuda.current_stream(dev)
+    hlb.headloss_lmhead_logits(hid, wt, N, D, V, logits, st2, err, s)
+    with torch.no_grad():
+        z = scale * softcap * torch.tanh(logits.float() / softcap)
+        lp = F.log_softmax(z, -1).gather(1, labels.clamp(min=0)[:, None])[:, 0]
+        old = (lp + 0.05 * torch.randn(N, generator=g, device=dev)).contiguous()
+        del z, lp
+    dcode = hlb.HEADLOSS_BF16
+
+    def gemms_rs():
+        hlb.headloss_lmhead_logits_rowstats(hid, wt, N, D, V, softcap, scale, logits, rs, err, s,
+                                            temperature=T, row_stats_t=rsT)
+        hlb.headloss_lmhead_logits_rowstats(hid, wt_t, N, D, V, 0.0, 1.0 / T, tlog, trs, err, s)
+
+    def loss_rs():
+        hlb.headloss_forward_backward_rowstats(h.h, logits, N, V, dcode, labels, old, adv, rs,
+                                               grad, out, s, teacher=tlog, row_stats_t=rsT,
+                                               teacher_stats=trs)
+
+    def gemms_plain():
+        hlb.headloss_lmhead_logits(hid, wt, N, D, V, logits, st2, err, s)
+        hlb.headloss_lmhead_logits(hid, wt_t, N, D, V, tlog, st2, err, s)
+
+    def loss_2pass():
+        hlb.headloss_forward_backward(h.h, logits, N, V, dcode, labels, tlog, old, adv, grad,
+                                      out, s)
+
+    fused = lambda: (gemms_rs(), loss_rs())
+    separate = lambda: (gemms_plain(), loss_2pass())
+    for fn in (fused, separate, fused, separate):
+        fn()
+    t_fused = statistics.mean(time_calls(fused, s, steps))
+    t_sep = statistics.mean(time_calls(separate, s, steps))
+    gemms_rs()
+    t_loss1 = statistics.mean(time_calls(loss_rs, s, steps))
+    gemms_plain()
+    t_loss2 = statistics.mean(time_calls(loss_2pass, s, steps))
+    torch.cuda.synchronize()
+    if int(err.item()) != 0 or h.device_error() != hlb.HEADLOSS_OK:
+        raise RuntimeError("LM-head distillation leg: device error")
+    bytes_min = N * V * 2 * 3 + N * 16
+    gbs = bytes_min / (t_loss1 / 1e3) / 1e9
+    res = {"shape": {"N": N, "D": D, "V": V}, "losses": list(losses), "temperature": T,
+           "softcap": softcap, "logits_scale": scale,
+           "fused_ms": t_fused, "separate_ms": t_sep, "speedup": t_sep / t_fused,
+           "loss_one_pass_ms": t_loss1, "loss_two_pass_ms": t_loss2,
+           "loss_one_pass_roofline": {"bound": "hbm", "achieved": gbs, "peak": peak,
+                                      "unit": "GB/s", "frac": gbs / peak,
+                                      "algorithmic_bytes": bytes_min,
+                                      "bytes_with_row_stats": bytes_min + N * NT * 36},
+           "loss_two_pass_plan": h.plan(V, dcode)}
+    h.close()
+    del hid, wt, wt_t, logits, tlog, grad, rs, rsT, trs, st2
+    torch.cuda.empty_cache()
+    return res
 
 
 def lm_head_loss(args, dev, peak, steps=10):

@@ -750,15 +750,19 @@ int headloss_get_device_error(headloss_t h, headloss_stream_t stream, int* err) 
 // LM-head GEMM (include/headloss.h documents the call).
 int headloss_forward_backward_rowstats(headloss_t h, const void* logits, int64_t N, int64_t V,
                                        int dtype, const int64_t* labels,
-                                       const float* old_logprobs, const float* advantages,
-                                       const void* row_stats, void* grad_out, float* scalars_out,
+                                       const void* teacher_logits, const float* old_logprobs,
+                                       const float* advantages, const void* row_stats,
+                                       const float* row_stats_t, const void* teacher_stats,
+                                       void* grad_out, float* scalars_out,
                                        headloss_stream_t stream) {
     const headloss_call_ext none = {nullptr, nullptr, 0, 0.0, nullptr};
     if (!h) return HEADLOSS_ERR_ARG;
     const uint32_t f = h->flags;
-    if (f & (L_DIST_CE | L_FKL | L_RKL)) return HEADLOSS_ERR_ARG;  // no teacher here
+    // reverse KL's coefficient needs a cross sum before the gradient pass
+    if (f & L_RKL) return HEADLOSS_ERR_ARG;
+    const bool teach = (f & (L_DIST_CE | L_FKL)) != 0;
     {
-        const int rc = check_call(h, logits, N, V, dtype, labels, nullptr, old_logprobs,
+        const int rc = check_call(h, logits, N, V, dtype, labels, teacher_logits, old_logprobs,
                                   advantages, grad_out, scalars_out, none);
         if (rc) return rc;
     }
@@ -766,11 +770,18 @@ int headloss_forward_backward_rowstats(headloss_t h, const void* logits, int64_t
     if (V % 256) return HEADLOSS_ERR_ARG;
     if (N > 0 && !row_stats) return HEADLOSS_ERR_ARG;
     if (reinterpret_cast<uintptr_t>(row_stats) & 15u) return HEADLOSS_ERR_ALIGN;
+    if (teach && N > 0) {
+        if (!teacher_stats) return HEADLOSS_ERR_MISSING_INPUT;
+        if (h->T != 1.f && !row_stats_t) return HEADLOSS_ERR_MISSING_INPUT;
+    }
+    if ((reinterpret_cast<uintptr_t>(teacher_stats) & 15u) ||
+        (reinterpret_cast<uintptr_t>(row_stats_t) & 3u))
+        return HEADLOSS_ERR_ALIGN;
     std::lock_guard<std::mutex> g(h->mu);
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return HEADLOSS_ERR_CUDA;
     if (dev != h->device) return HEADLOSS_ERR_ARG;
-    int feat = feature_set(h) & (F_ENT | F_SOFTCAP | F_ENTG);
+    int feat = feature_set(h) & (F_TEACH | F_ENT | F_SOFTCAP | F_ENTG);
     const void* kernel = onepass_kernel_bf16(feat);
     if (!kernel) return HEADLOSS_ERR_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -796,7 +807,7 @@ int headloss_forward_backward_rowstats(headloss_t h, const void* logits, int64_t
         grid = int(want < cap ? want : cap);
         Params p = {};
         p.x = logits;
-        p.t = nullptr;
+        p.t = teach ? teacher_logits : nullptr;
         p.g = grad_out;
         p.labels = labels;
         p.old_lp = (f & (L_GRPO | L_GRPO_STATS)) ? old_logprobs : nullptr;
@@ -813,6 +824,8 @@ int headloss_forward_backward_rowstats(headloss_t h, const void* logits, int64_t
         p.w_z = h->w.z;
         p.w_grpo = h->w.grpo;
         p.w_ent = h->w.entropy;
+        p.w_dce = h->w.dist_ce;
+        p.w_fkl = h->w.fkl;
         p.grad_scale = h->w.grad_scale;
         p.partials = h->partials;
         p.n_valid = h->n_valid;
@@ -822,7 +835,9 @@ int headloss_forward_backward_rowstats(headloss_t h, const void* logits, int64_t
         p.drop_row = -1;
         int nt = int(V / 256);
         const void* rs = row_stats;
-        void* args[] = {&p, &rs, &nt};
+        const void* rsT = teach ? static_cast<const void*>(row_stats_t) : nullptr;
+        const void* rst = teach ? teacher_stats : nullptr;
+        void* args[] = {&p, &rs, &rsT, &rst, &nt};
         if (cudaLaunchKernel(kernel, dim3(grid), dim3(256), args, size_t(smem), s) !=
             cudaSuccess)
             return HEADLOSS_ERR_CUDA;
@@ -831,9 +846,9 @@ int headloss_forward_backward_rowstats(headloss_t h, const void* logits, int64_t
     fa.flags = f;
     fa.w_ce = h->w.ce;
     fa.w_z = h->w.z;
-    fa.w_dce = 0.f;
-    fa.w_fkl = 0.f;
-    fa.w_rkl = 0.f;
+    fa.w_dce = h->w.dist_ce;
+    fa.w_fkl = h->w.fkl;
+    fa.w_rkl = 0.f;  // refused above
     fa.w_grpo = h->w.grpo;
     fa.w_ent = h->w.entropy;
     fa.divisor = 0.0;

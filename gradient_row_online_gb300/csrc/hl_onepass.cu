@@ -9,11 +9,16 @@
 // the row's softmax statistics; the loss then needs a single read of the
 // logits and a single write of the gradient: no statistics pass, no second
 // read.  The statistics it consumes are, per (row, 256-column tile), the base-2
-// record (m2, S, E) of zs = s c tanh(x / c) log2(e) (c = 0: s x log2(e)):
-// m2 = max zs, S = sum 2^(zs - m2), E = sum 2^(zs - m2) (zs - m2).  These
-// cover every label-based loss (CE, z-loss, GRPO and its statistics,
-// entropy); the distillation losses pair the row with a teacher row element
-// by element and are not supported here.
+// record (m2, S, E, X) of zs = s c tanh(x / c) log2(e) (c = 0: s x log2(e)):
+// m2 = max zs, S = sum 2^(zs - m2), E = sum 2^(zs - m2) (zs - m2), X = max |x|.
+// These cover the label-based losses (CE, z-loss, GRPO and its statistics,
+// entropy).  With a teacher (from-distribution CE, forward KL) two more come
+// in: the student tile's S_T = sum 2^((zs - m2) / T) and the teacher GEMM's
+// record of ut = t log2(e) / T.  The gradient then needs no cross sum, and the
+// two losses' values are sums of q (log q - log pT) and q log pT the pass
+// accumulates as it goes (q, pT: the teacher's and the student's softmax at T),
+// added to the row's losses after the pass.  Reverse KL is not covered: its
+// coefficient needs the cross sum sum pT (log pT - log q) before the pass.
 //
 // Four warps per row, each a quarter of its words (a unit), units strided
 // over the grid:
@@ -21,11 +26,11 @@
 //             (running max, rescaled sums), exchange them through shared
 //             memory, and each takes the 32 lane records through the row
 //             epilogue shared with the other kernels (losses, coefficients);
-//   gradient  the unit's words arrive through the warp's own ring of 4 KB
-//             bulk copies, which runs ahead across units; each lane computes
-//             the combined gradient of its 16-byte words in fp32 and stores
-//             it once; the lane whose word holds the label column patches
-//             that element before the store.
+//   gradient  the unit's words (and the teacher's) arrive through the warp's
+//             own ring of 4 KB bulk copies, which runs ahead across units;
+//             each lane computes the combined gradient of its 16-byte words
+//             in fp32 and stores it once; the lane whose word holds the label
+//             column patches that element before the store.
 // Per-warp compensated sums of the row losses are added in warp order into
 // one fp64 partial record per CTA, which the finalize kernel reduces.
 #include "hl_rows16.cuh"
@@ -34,45 +39,54 @@ namespace hl {
 
 constexpr int OP_THREADS = 256;
 constexpr int OP_WARPS = OP_THREADS / 32;
-constexpr int OP_PARTS = 4;         // warps per row, each a quarter of the row's words
-constexpr int OP_SLOTS = 3;         // chunk slots of each warp's ring
-constexpr int OP_CHUNK_WORDS = 256; // 16-byte words per chunk (8 per lane, 4 KB)
+constexpr int OP_PARTS = 4;           // warps per row, each a quarter of the row's words
+constexpr int OP_SLOTS = 3;           // chunk slots of each warp's ring
+constexpr int OP_SLOT_BYTES = 4096;   // a slot: 256 student words, or 128 student + 128 teacher
 // dynamic shared memory: the warps' rings and their mbarriers
-constexpr int OP_SMEM = OP_WARPS * OP_SLOTS * OP_CHUNK_WORDS * 16 + OP_WARPS * OP_SLOTS * 8;
+constexpr int OP_SMEM = OP_WARPS * OP_SLOTS * OP_SLOT_BYTES + OP_WARPS * OP_SLOTS * 8;
 
 template <int FEAT>
-__global__ void __launch_bounds__(OP_THREADS, 2) onepass_kernel16(const __grid_constant__ Params p,
-                                                               const float4* __restrict__ rs,
-                                                               int NT) {
+__global__ void __launch_bounds__(OP_THREADS, 2)
+    onepass_kernel16(const __grid_constant__ Params p, const float4* __restrict__ rs,
+                     const float* __restrict__ rsT, const float4* __restrict__ rst, int NT) {
     using P16 = Pack16<__nv_bfloat16>;
+    constexpr bool TEACH = (FEAT & F_TEACH) != 0;
     constexpr bool ENT = (FEAT & F_ENT) != 0;
     constexpr bool CAP = (FEAT & F_SOFTCAP) != 0;
     constexpr bool ENTG = ENT && (FEAT & F_ENTG) != 0;
     constexpr int EPW = 8;
+    constexpr int CW = TEACH ? 128 : 256;  // words of each operand in a chunk
+    constexpr int NF = TEACH ? 6 : 3;      // merged fields the part warps exchange
+    static_assert(CW * 16 * (TEACH ? 2 : 1) == OP_SLOT_BYTES, "slot size");
 
     __shared__ float recs[OP_WARPS][32 * NREC];
-    // the four part warps' merged tile records (m2, S, E) per lane:
-    // [group][part][field][lane]
-    __shared__ float mrg[OP_WARPS / OP_PARTS][OP_PARTS][3][32];
     __shared__ float accs[OP_WARPS][2 * NACC];
     __shared__ RowLoss rls[OP_WARPS];
+    __shared__ float xq[OP_WARPS][2];  // a unit's teacher cross sums, per warp
     extern __shared__ __align__(128) unsigned char ring_smem[];
+    // the part warps' merged records, [part][field][lane], live in the
+    // group's record area between the two merge barriers
+    static_assert(OP_PARTS * NF * 32 <= OP_PARTS * 32 * NREC, "exchange area");
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t N = p.N, V = p.V;
     const int64_t nwords = V / EPW;
     const __nv_bfloat16* __restrict__ xg = static_cast<const __nv_bfloat16*>(p.x);
+    const __nv_bfloat16* __restrict__ tg = static_cast<const __nv_bfloat16*>(p.t);
     __nv_bfloat16* gg = static_cast<__nv_bfloat16*>(p.g);
     const bool has_labels = p.labels != nullptr;
     const bool need_side = (p.flags & (L_GRPO | L_GRPO_STATS)) != 0;
     const float kk = *p.kscale;
 
     const float LOG2E = 1.4426950408889634f;
+    const float LN2 = 0.6931471805599453f;
     const float s = p.s;
     const float K1 = s * LOG2E;
     const float invc = CAP ? 1.f / p.softcap : 0.f;
     const float A2 = CAP ? 2.f * LOG2E * invc : 0.f;
     const float Kc = CAP ? s * p.softcap * LOG2E : 0.f;
+    const float invT = TEACH ? 1.f / p.T : 1.f;
+    const float KT = LOG2E * invT;  // teacher: ut = t log2(e) / T
     // softcap: tanh by tiers, picked per chunk from the records' largest |x|:
     // A = degree-3 odd polynomial on |x| <= 0.45 c (only while Kc <= 48,
     // where its fit error stays below fp32 rounding of the exponentials),
@@ -97,6 +111,7 @@ __global__ void __launch_bounds__(OP_THREADS, 2) onepass_kernel16(const __grid_c
     // 1 - tanh^2 = 1 - (zs / Kc)^2 on the polynomial tiers (|tanh| <= 0.67)
     const f2 mKc2 = pk1(CAP ? -1.f / (Kc * Kc) : 0.f), one2 = pk1(1.f);
     const f2 K2 = pk1(K1), A22 = pk1(A2), Kc2 = pk1(Kc);
+    const f2 invT2 = pk1(invT), KinvT2 = pk1(K1 * invT), KT2 = pk1(KT);
     auto zs1 = [&](float v, float* om) -> float {
         return CAP ? __fmul_rn(tanh_a2x_1(__fmul_rn(v, A2), om), Kc) : __fmul_rn(v, K1);
     };
@@ -111,11 +126,12 @@ __global__ void __launch_bounds__(OP_THREADS, 2) onepass_kernel16(const __grid_c
     // shared memory by bulk copies (lane 0 issues, an mbarrier per slot
     // counts the bytes), refilled as soon as the warp has used a chunk and
     // running on across units, so the copies OP_SLOTS chunks ahead are always
-    // in flight whatever the arithmetic is doing.
-    unsigned char* ring = ring_smem + size_t(warp) * OP_SLOTS * OP_CHUNK_WORDS * 16;
-    uint64_t* fullb = reinterpret_cast<uint64_t*>(ring_smem + size_t(OP_WARPS) * OP_SLOTS *
-                                                                  OP_CHUNK_WORDS * 16) +
-                      warp * OP_SLOTS;
+    // in flight whatever the arithmetic is doing.  A slot holds CW student
+    // words and, with a teacher, the teacher's CW words behind them.
+    unsigned char* ring = ring_smem + size_t(warp) * OP_SLOTS * OP_SLOT_BYTES;
+    uint64_t* fullb =
+        reinterpret_cast<uint64_t*>(ring_smem + size_t(OP_WARPS) * OP_SLOTS * OP_SLOT_BYTES) +
+        warp * OP_SLOTS;
     auto unit_range = [&](int64_t uu, int64_t& rr, int64_t& b0, int64_t& b1) {
         rr = uu / OP_PARTS;
         const int pt = int(uu - rr * OP_PARTS);
@@ -129,13 +145,14 @@ __global__ void __launch_bounds__(OP_THREADS, 2) onepass_kernel16(const __grid_c
         if (iu >= nunits) return;
         int64_t rr, b0, b1;
         unit_range(iu, rr, b0, b1);
-        const int64_t c0 = b0 + ic * OP_CHUNK_WORDS;
-        const int64_t cw = (b1 - c0) < OP_CHUNK_WORDS ? (b1 - c0) : OP_CHUNK_WORDS;
+        const int64_t c0 = b0 + ic * CW;
+        const int64_t cw = (b1 - c0) < CW ? (b1 - c0) : CW;
         const uint32_t bar = smem_addr(&fullb[sl]);
-        mbar_arrive_expect_tx(bar, uint32_t(cw * 16));
-        bulk_g2s(smem_addr(ring + size_t(sl) * OP_CHUNK_WORDS * 16), xg + rr * V + c0 * EPW,
-                 uint32_t(cw * 16), bar);
-        if (c0 + OP_CHUNK_WORDS >= b1) {
+        const uint32_t dst = smem_addr(ring + size_t(sl) * OP_SLOT_BYTES);
+        mbar_arrive_expect_tx(bar, uint32_t(cw * 16) * (TEACH ? 2u : 1u));
+        bulk_g2s(dst, xg + rr * V + c0 * EPW, uint32_t(cw * 16), bar);
+        if (TEACH) bulk_g2s(dst + CW * 16, tg + rr * V + c0 * EPW, uint32_t(cw * 16), bar);
+        if (c0 + CW >= b1) {
             iu += nw;
             ic = 0;
         } else {
@@ -158,7 +175,7 @@ __global__ void __launch_bounds__(OP_THREADS, 2) onepass_kernel16(const __grid_c
             lost_par = (lost_par & ~(1u << slot)) | (phase << slot);
             if (lane == 0) atomicOr(p.err, E_TIMEOUT);
         }
-        return ring + size_t(slot) * OP_CHUNK_WORDS * 16;
+        return ring + size_t(slot) * OP_SLOT_BYTES;
     };
     // the warp is done with the chunk: refill its slot, step the ring
     auto release = [&]() {
@@ -172,13 +189,20 @@ __global__ void __launch_bounds__(OP_THREADS, 2) onepass_kernel16(const __grid_c
             phase ^= 1u;
         }
     };
+    // the row's four warps (warps 0-3 or 4-7 of the CTA) take the same rows
+    // in the same iterations: a named barrier of the four orders their
+    // exchanges
+    const uint32_t gbar = 1 + (warp >> 2);
+    auto group_sync = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(gbar) : "memory"); };
+    float* mg = recs[(warp / OP_PARTS) * OP_PARTS];  // [part][field][lane]
+
     // unit u: row u / OP_PARTS, part u % OP_PARTS (a range of the row's words);
     // every part merges the row's records itself, part 0 adds the row's losses
     for (int64_t u = gw; u < nunits; u += nw) {
         const int64_t r = u / OP_PARTS;
         const int part = int(u - r * OP_PARTS);
         const int64_t wb = nwords * part / OP_PARTS, we = nwords * (part + 1) / OP_PARTS;
-        const int64_t nch = (we - wb + OP_CHUNK_WORDS - 1) / OP_CHUNK_WORDS;
+        const int64_t nch = (we - wb + CW - 1) / CW;
         int64_t y = 0;
         float old_lp = 0.f, adv = 0.f;
         if (lane == 0) {
@@ -208,74 +232,109 @@ __global__ void __launch_bounds__(OP_THREADS, 2) onepass_kernel16(const __grid_c
         }
 
         // ---- merge the tiles' records: part warp pt, lane k takes tiles
-        // pt 32 + k + 128 j (four loads in flight per lane), then lane k of
-        // every part warp merges the four parts' records of lane k ----
-        float M = -CUDART_INF_F, S = 0.f, E = 0.f;
-        auto merge_in = [&](float qm, float qs, float qe) {
+        // pt 32 + k + 128 j (four tiles' loads in flight per lane), then lane
+        // k of every part warp merges the four parts' records of lane k ----
+        // student (M, S, E; S_T at the temperature), teacher (Mu, Sq)
+        float M = -CUDART_INF_F, S = 0.f, E = 0.f, ST = 0.f, Mu = -CUDART_INF_F, Sq = 0.f;
+        auto merge_s = [&](float qm, float qs, float qe, float qt) {
             if (!(qs > 0.f)) return;
             if (qm > M) {
                 const float d = M == -CUDART_INF_F ? 0.f : M - qm;  // <= 0
                 const float al = exp2f(d);
                 if (ENT) E = al * (E + d * S) + qe;
                 S = al * S + qs;
+                if (TEACH) ST = exp2f(d * invT) * ST + qt;
                 M = qm;
             } else {
                 const float d = qm - M;
                 const float al = exp2f(d);
                 if (ENT) E += al * (qe + d * qs);
                 S += al * qs;
+                if (TEACH) ST += exp2f(d * invT) * qt;
+            }
+        };
+        auto merge_t = [&](float qm, float qs) {
+            if (!(qs > 0.f)) return;
+            if (qm > Mu) {
+                Sq = (Mu == -CUDART_INF_F ? 0.f : exp2f(Mu - qm) * Sq) + qs;
+                Mu = qm;
+            } else {
+                Sq += exp2f(qm - Mu) * qs;
             }
         };
         const float4* rrow = rs + r * NT;
+        const float* trow = TEACH && rsT != nullptr ? rsT + r * NT : nullptr;
+        const float4* urow = TEACH ? rst + r * NT : nullptr;
         for (int tb = part * 32 + lane; tb < NT; tb += 4 * 128) {
-            float4 q[4];
+            float4 q[4], qu[4];
+            float qt[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                q[j] = tb + 128 * j < NT ? rrow[tb + 128 * j] : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < 4; ++j) {
+                const bool in = tb + 128 * j < NT;
+                q[j] = in ? rrow[tb + 128 * j] : make_float4(0.f, 0.f, 0.f, 0.f);
+                if (TEACH) {
+                    qu[j] = in ? urow[tb + 128 * j] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    qt[j] = in && trow != nullptr ? trow[tb + 128 * j] : q[j].y;  // T = 1: S
+                }
+            }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) merge_in(q[j].x, q[j].y, q[j].z);
+            for (int j = 0; j < 4; ++j) {
+                merge_s(q[j].x, q[j].y, q[j].z, TEACH ? qt[j] : 0.f);
+                if (TEACH) merge_t(qu[j].x, qu[j].y);
+            }
         }
         float zy = 0.f, hasy = 0.f;
         if (lane == 0 && has_labels) {
             zy = zs1(P16::to_f(reinterpret_cast<const uint16_t*>(xg)[r * V + y]), nullptr);
             hasy = 1.f;
         }
-        float(*mg)[3][32] = mrg[warp / OP_PARTS];
-        mg[part][0][lane] = M;
-        mg[part][1][lane] = S;
-        mg[part][2][lane] = E;
-        // the row's four warps (warps 0-3 or 4-7 of the CTA: the same rows in
-        // the same iterations) have all read the label logit and stored their
-        // records before any of them writes the gradient (in place, one of
-        // them overwrites the label logit), and all have read the records
-        // before any stores the next row's
-        const uint32_t gbar = 1 + (warp >> 2);
-        asm volatile("bar.sync %0, 128;" ::"r"(gbar) : "memory");
+        {
+            float* m = mg + part * NF * 32 + lane;
+            m[0] = M;
+            m[32] = S;
+            m[64] = E;
+            if (TEACH) {
+                m[96] = ST;
+                m[128] = Mu;
+                m[160] = Sq;
+            }
+        }
+        // all four warps have read the label logit and stored their records
+        // before any of them writes the gradient (in place, one of them
+        // overwrites the label logit) or the merged records (next)
+        group_sync();
         M = -CUDART_INF_F;
-        S = 0.f;
-        E = 0.f;
+        S = E = ST = Sq = 0.f;
+        Mu = -CUDART_INF_F;
 #pragma unroll
-        for (int pt = 0; pt < OP_PARTS; ++pt)
-            merge_in(mg[pt][0][lane], mg[pt][1][lane], mg[pt][2][lane]);
-        asm volatile("bar.sync %0, 128;" ::"r"(gbar) : "memory");
+        for (int pt = 0; pt < OP_PARTS; ++pt) {
+            const float* m = mg + pt * NF * 32 + lane;
+            merge_s(m[0], m[32], m[64], TEACH ? m[96] : 0.f);
+            if (TEACH) merge_t(m[128], m[160]);
+        }
+        // all have read the exchanged records before the area takes the
+        // lane records below
+        group_sync();
         float* rec = recs[warp] + lane * NREC;
         rec[R_ZM] = M;
-        rec[R_UM] = 0.f;
+        rec[R_UM] = Mu;
         rec[R_S] = S;
         rec[R_E] = E;
-        rec[R_ST] = 0.f;
-        rec[R_SQ] = 0.f;
-        rec[R_EQ] = 0.f;
+        rec[R_ST] = ST;
+        rec[R_SQ] = Sq;
+        rec[R_EQ] = 0.f;  // the distillation values come from the pass (below)
         rec[R_XP] = 0.f;
         rec[R_Y] = 0.f;
         rec[R_ZY] = zy;
         rec[R_HASY] = hasy;
         __syncwarp();
-        const RowCoef k = row_epilogue16<false, false, ENT, CAP, true>(
+        const RowCoef k = row_epilogue16<TEACH, false, ENT, CAP, true>(
             p, recs[warp], 32, false, old_lp, adv, accs[warp], lane, r, kk, &rls[warp]);
-        __syncwarp();
-        if (lane == 0 && part == 0) row_accumulate(p, rls[warp], accs[warp], r);
-        if (grow == nullptr) {
+        // all have read their lane records before the next row's exchange
+        // reuses the area
+        group_sync();
+        if (!TEACH && lane == 0 && part == 0) row_accumulate(p, rls[warp], accs[warp], r);
+        if (!TEACH && grow == nullptr) {
             for (int64_t c = 0; c < nch; ++c) {
                 acquire();
                 release();
@@ -286,37 +345,46 @@ __global__ void __launch_bounds__(OP_THREADS, 2) onepass_kernel16(const __grid_c
         // ---- the gradient, one read and one write of the row ----
         const ShiftCoef h = shift_coefs(k, ENTG);
         const f2 nlse2 = pk1(h.nlse), pc2 = pk1(h.pc), ps2 = pk1(h.ps);
+        const f2 nlseT2 = pk1(h.nlseT), nlsq2 = pk1(h.nlsq), tc2 = pk1(h.tc), qc2 = pk1(h.qc);
         const int64_t ywd = has_labels ? y / EPW : -1;  // the label's word
         const int iyw = has_labels ? int(y - ywd * EPW) : 0;
+        // teacher cross sums of this unit, in units of 2^sg (the exponent
+        // shift shared by every exponential): B1 = sum 2^sg q (log2 q -
+        // log2 pT), B2 = sum 2^sg q (log2 pT + sg)
+        f2 B1 = pk1(0.f), B2 = pk1(0.f);
         // softcap: the tier of chunk c of this unit (c < 32; later chunks take
         // tier X): lane c takes the largest |x| of the tiles the chunk spans
         uint32_t mA = 0u, mB = 0u;
         if (CAP) {
             float cx = 0.f;
             if (lane < nch) {
-                const int64_t c0 = wb + int64_t(lane) * OP_CHUNK_WORDS;
-                const int64_t c1 = c0 + OP_CHUNK_WORDS < we ? c0 + OP_CHUNK_WORDS : we;
+                const int64_t c0 = wb + int64_t(lane) * CW;
+                const int64_t c1 = c0 + CW < we ? c0 + CW : we;
                 const int64_t t0 = c0 / 32, t1 = (c1 - 1) / 32;  // 32 words a tile
                 const float* xr = reinterpret_cast<const float*>(rrow) + 3;
 #pragma unroll
-                for (int i = 0; i <= OP_CHUNK_WORDS / 32; ++i)
+                for (int i = 0; i <= CW / 32; ++i)
                     if (t0 + i <= t1) cx = fmaxf(cx, xr[4 * (t0 + i)]);
             }
             mA = __ballot_sync(0xffffffffu, cx <= XA);
             mB = __ballot_sync(0xffffffffu, cx <= XB);
         }
-        // one word's gradient in tier TI (-1: no softcap)
-        auto word = [&](const uint4& a, const uint4& ow, auto tierc) -> uint4 {
+        // one word's gradient in tier TI (-1: no softcap); b: the teacher's
+        // word; live: a word of the unit (the cross sums take only those)
+        auto word = [&](const uint4& a, const uint4& b, const uint4& ow, bool live,
+                        auto tierc) -> uint4 {
             constexpr int TI = decltype(tierc)::value;
             const uint32_t xa[4] = {a.x, a.y, a.z, a.w};
+            const uint32_t ta[4] = {b.x, b.y, b.z, b.w};
             const uint32_t oa[4] = {ow.x, ow.y, ow.z, ow.w};
             uint32_t out[4];
 #pragma unroll
             for (int kq = 0; kq < 4; ++kq) {
                 const f2 xv = P16::unpack(xa[kq]);
-                f2 arg, omt = one2;
+                f2 arg, argT = pk1(0.f), omt = one2;
                 if constexpr (TI < 0) {
                     arg = fma2(xv, K2, nlse2);
+                    if (TEACH) argT = fma2(xv, KinvT2, nlseT2);
                 } else if constexpr (TI <= 1) {
                     const f2 u = mul2(xv, xv);
                     f2 q;
@@ -334,12 +402,25 @@ __global__ void __launch_bounds__(OP_THREADS, 2) onepass_kernel16(const __grid_c
                     const f2 zs = mul2(xv, q);
                     omt = fma2(zs, mul2(zs, mKc2), one2);
                     arg = add2(zs, nlse2);
+                    if (TEACH) argT = fma2(zs, invT2, nlseT2);
                 } else {
                     const TanhD2 td = tanh_from_ex2_arg(mul2(xv, A22));
                     omt = td.omt;
-                    arg = fma2(td.th, Kc2, nlse2);
+                    const f2 zs = mul2(td.th, Kc2);
+                    arg = add2(zs, nlse2);
+                    if (TEACH) argT = fma2(zs, invT2, nlseT2);
                 }
-                const f2 g = mul2(ex2p(arg), ENTG ? fma2(ps2, arg, pc2) : pc2);
+                f2 g = mul2(ex2p(arg), ENTG ? fma2(ps2, arg, pc2) : pc2);
+                if (TEACH) {
+                    const f2 argq = fma2(P16::unpack(ta[kq]), KT2, nlsq2);
+                    const f2 pT = ex2p(argT), q = ex2p(argq);
+                    g = fma2(pT, tc2, g);
+                    g = fma2(q, qc2, g);
+                    if (live) {
+                        B1 = fma2(q, sub2(argq, argT), B1);
+                        B2 = fma2(q, argT, B2);
+                    }
+                }
                 const f2 gw = CAP ? mul2(g, omt) : g;
                 out[kq] = P16::pack(p.accumulate ? add2(P16::unpack(oa[kq]), gw) : gw);
             }
@@ -347,23 +428,31 @@ __global__ void __launch_bounds__(OP_THREADS, 2) onepass_kernel16(const __grid_c
         };
         // the label column's element again, with the label term (halves
         // picked by selects, so the words stay in registers)
-        auto patch = [&](const uint4& o, const uint4& a, const uint4& ow) -> uint4 {
+        auto patch = [&](const uint4& o, const uint4& a, const uint4& b,
+                         const uint4& ow) -> uint4 {
             const uint32_t xa[4] = {a.x, a.y, a.z, a.w};
+            const uint32_t ta[4] = {b.x, b.y, b.z, b.w};
             const uint32_t oa[4] = {ow.x, ow.y, ow.z, ow.w};
             uint32_t out[4] = {o.x, o.y, o.z, o.w};
             const int qy = iyw >> 1, sh = (iyw & 1) * 16;
-            uint32_t xw = xa[0], owd = oa[0];
+            uint32_t xw = xa[0], tw = ta[0], owd = oa[0];
 #pragma unroll
             for (int kq = 1; kq < 4; ++kq)
                 if (kq == qy) {
                     xw = xa[kq];
+                    tw = ta[kq];
                     owd = oa[kq];
                 }
             const float xv1 = P16::to_f(uint16_t(xw >> sh));
             float om1 = 1.f;
             const float zs = zs1(xv1, &om1);
             const float arg = zs + h.nlse;
-            float g1 = ex2f(arg) * (ENTG ? fmaf(h.ps, arg, h.pc) : h.pc) - k.bc;
+            float g1 = ex2f(arg) * (ENTG ? fmaf(h.ps, arg, h.pc) : h.pc);
+            if (TEACH) {
+                g1 = fmaf(ex2f(fmaf(zs, invT, h.nlseT)), h.tc, g1);
+                g1 = fmaf(ex2f(fmaf(P16::to_f(uint16_t(tw >> sh)), KT, h.nlsq)), h.qc, g1);
+            }
+            g1 -= k.bc;
             if (CAP) g1 *= om1;
             if (p.accumulate) g1 += P16::to_f(uint16_t(owd >> sh));
             const uint32_t hv = uint32_t(P16::from_f(g1)) << sh;
@@ -373,26 +462,30 @@ __global__ void __launch_bounds__(OP_THREADS, 2) onepass_kernel16(const __grid_c
                 if (kq == qy) out[kq] = (out[kq] & keep) | hv;
             return make_uint4(out[0], out[1], out[2], out[3]);
         };
-        // one chunk from the ring: eight words a lane, unrolled; the words
-        // past a short chunk's end are computed and not stored
+        // one chunk from the ring: CW / 32 words a lane, unrolled; the words
+        // past a short chunk's end are computed and neither stored nor summed
+        const bool store = grow != nullptr;
         auto chunk = [&](const unsigned char* sb, __nv_bfloat16* gc, int cw, int jy, auto tierc) {
 #pragma unroll
-            for (int i = 0; i < OP_CHUNK_WORDS / 32; ++i) {
+            for (int i = 0; i < CW / 32; ++i) {
                 const int j = lane + 32 * i;
                 const uint4 a = *reinterpret_cast<const uint4*>(sb + size_t(j) * 16);
+                uint4 b = make_uint4(0, 0, 0, 0);
+                if (TEACH) b = *reinterpret_cast<const uint4*>(sb + CW * 16 + size_t(j) * 16);
                 uint4 ow = make_uint4(0, 0, 0, 0);
-                if (p.accumulate && j < cw) ow = *reinterpret_cast<const uint4*>(gc + size_t(j) * EPW);
-                uint4 o = word(a, ow, tierc);
-                if (j == jy) o = patch(o, a, ow);
-                if (j < cw) *reinterpret_cast<uint4*>(gc + size_t(j) * EPW) = o;
+                if (p.accumulate && j < cw)
+                    ow = *reinterpret_cast<const uint4*>(gc + size_t(j) * EPW);
+                uint4 o = word(a, b, ow, j < cw, tierc);
+                if (j == jy) o = patch(o, a, b, ow);
+                if (store && j < cw) *reinterpret_cast<uint4*>(gc + size_t(j) * EPW) = o;
             }
         };
         for (int64_t c = 0; c < nch; ++c) {
             const unsigned char* sb = acquire();
-            const int64_t c0 = wb + c * OP_CHUNK_WORDS;
-            const int cw = int((we - c0) < OP_CHUNK_WORDS ? (we - c0) : OP_CHUNK_WORDS);
+            const int64_t c0 = wb + c * CW;
+            const int cw = int((we - c0) < CW ? (we - c0) : CW);
             const int jy = (ywd >= c0 && ywd < c0 + cw) ? int(ywd - c0) : -1;
-            __nv_bfloat16* gc = grow + c0 * EPW;
+            __nv_bfloat16* gc = store ? grow + c0 * EPW : nullptr;
             if (!CAP) {
                 chunk(sb, gc, cw, jy, std::integral_constant<int, -1>{});
             } else {
@@ -402,6 +495,34 @@ __global__ void __launch_bounds__(OP_THREADS, 2) onepass_kernel16(const __grid_c
                 else chunk(sb, gc, cw, jy, std::integral_constant<int, 2>{});
             }
             release();
+        }
+        if (TEACH) {
+            // the row's distillation values from the four warps' cross sums:
+            // forward KL = ln2 sum q (log2 q - log2 pT), from-distribution
+            // CE = -ln2 sum q log2 pT (sum q = 1)
+            float b1 = hsum(B1), b2 = hsum(B2);
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                b1 += __shfl_xor_sync(0xffffffffu, b1, o);
+                b2 += __shfl_xor_sync(0xffffffffu, b2, o);
+            }
+            if (lane == 0) {
+                xq[warp][0] = b1;
+                xq[warp][1] = b2;
+            }
+            group_sync();
+            if (lane == 0 && part == 0) {
+                float s1 = 0.f, s2 = 0.f;
+                for (int pt = 0; pt < OP_PARTS; ++pt) {
+                    s1 += xq[warp + pt][0];
+                    s2 += xq[warp + pt][1];
+                }
+                const float sg = rintf(h.nlsq + k.lsq2);  // the shift: nlsq = sg - lsq2
+                const float sc = __uint_as_float(uint32_t(127 - int(sg)) << 23);  // 2^-sg
+                rls[warp].fkl = LN2 * s1 * sc;
+                rls[warp].dce = -LN2 * fmaf(s2, sc, -sg);
+                row_accumulate(p, rls[warp], accs[warp], r);
+            }
         }
     }
 
@@ -433,6 +554,12 @@ const void* onepass_kernel_bf16(int feat) {
         HL_CASE(F_SOFTCAP)
         HL_CASE(F_SOFTCAP | F_ENT)
         HL_CASE(F_SOFTCAP | F_ENT | F_ENTG)
+        HL_CASE(F_TEACH)
+        HL_CASE(F_TEACH | F_ENT)
+        HL_CASE(F_TEACH | F_ENT | F_ENTG)
+        HL_CASE(F_TEACH | F_SOFTCAP)
+        HL_CASE(F_TEACH | F_SOFTCAP | F_ENT)
+        HL_CASE(F_TEACH | F_SOFTCAP | F_ENT | F_ENTG)
         default: return nullptr;
     }
 }

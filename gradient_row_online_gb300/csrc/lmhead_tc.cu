@@ -200,9 +200,12 @@ __device__ __forceinline__ void tile_of(int i, int MT, int NT, int& m, int& n) {
 // record of the capped, scaled logits zs = s c tanh(x / c) log2(e) (c = 0:
 // s x log2(e)), base 2: (m2, S, E, X) with m2 = max zs, S = sum 2^(zs - m2),
 // E = sum 2^(zs - m2) (zs - m2) and X = max |x| (which picks the loss
-// kernel's tanh form).
+// kernel's tanh form).  MODE 2: MODE 1's record and, apart, the tile's sum at
+// the distillation temperature T, S_T = sum 2^((zs - m2) / T).
 struct Xform {
     float c, invc, k;  // softcap (0: off), 1 / c, s * c * log2(e) (c = 0: s * log2(e))
+    float invT;        // MODE 2: 1 / T
+    float* st_out;     // MODE 2: N x NT sums at temperature T
 };
 
 template <int MODE>
@@ -327,7 +330,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!wait_phase(su32(&tfull[acc]), uint32_t(j >> 1) & 1u, abort, err)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const uint32_t tbase = tmem + (uint32_t(32 * q) << 16) + uint32_t(acc * BN);
-            float mx = -INFINITY, ssum = 0.f, esum = 0.f, ax = 0.f;
+            float mx = -INFINITY, ssum = 0.f, esum = 0.f, ax = 0.f, tsum = 0.f;
             for (int g = 0; g < BN / OUT_COLS; ++g, ++step) {
                 unsigned char* ob = outb + (step & 1) * OUT_BYTES;
                 // the store that last read this buffer has finished reading it
@@ -345,7 +348,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         pk[t] = *reinterpret_cast<const uint32_t*>(&b2);
                         v[2 * t] = __low2float(b2);
                         v[2 * t + 1] = __high2float(b2);
-                        if (MODE == 1) {  // zs of the bf16 logits, their largest |x|
+                        if (MODE >= 1) {  // zs of the bf16 logits, their largest |x|
                             ax = fmaxf(ax, fmaxf(fabsf(v[2 * t]), fabsf(v[2 * t + 1])));
                             v[2 * t] = xf.c > 0.f ? xf.k * tanhf(v[2 * t] * xf.invc) : xf.k * v[2 * t];
                             v[2 * t + 1] = xf.c > 0.f ? xf.k * tanhf(v[2 * t + 1] * xf.invc)
@@ -364,12 +367,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const float al = exp2f(dm);
                         esum = al * (esum + dm * ssum);
                         ssum *= al;
+                        if (MODE == 2) tsum *= exp2f(dm * xf.invT);
 #pragma unroll
                         for (int t = 0; t < 32; ++t) {
                             const float d = v[t] - nm;
                             const float e = exp2f(d);
                             ssum += e;
                             esum = fmaf(e, d, esum);
+                            if (MODE == 2) tsum += exp2f(d * xf.invT);
                         }
                     }
                     mx = nm;
@@ -397,6 +402,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const size_t si = size_t(m * BM + 32 * q + lane) * NT + n;
             if (MODE == 0) static_cast<float2*>(stats_out)[si] = make_float2(mx, ssum);
             else static_cast<float4*>(stats_out)[si] = make_float4(mx, ssum, esum, ax);
+            if (MODE == 2) xf.st_out[si] = tsum;
         }
         if (lane == 0) bulk_wait_all();  // stores complete before shared memory is released
         __syncwarp();
@@ -444,7 +450,8 @@ int make_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows,
 namespace hl_lmhead {
 
 int launch(int mode, const void* hidden, const void* weight, int N, int D, int V, float softcap,
-           float logits_scale, void* logits, void* stats, int* err, void* stream) {
+           float logits_scale, void* logits, void* stats, int* err, void* stream,
+           float temperature = 1.f, float* stats_t = nullptr) {
     if (N <= 0 || D <= 0 || V <= 0 || N % BM || V % BN || D % BK) return HEADLOSS_ERR_ARG;
     if (!hidden || !weight || !logits || !stats || !err) return HEADLOSS_ERR_ARG;
     if (!(softcap >= 0.f) || !isfinite(softcap) || !(logits_scale > 0.f) || !isfinite(logits_scale))
@@ -454,6 +461,9 @@ int launch(int mode, const void* hidden, const void* weight, int N, int D, int V
         return HEADLOSS_ERR_ALIGN;
     if (reinterpret_cast<uintptr_t>(stats) & (mode == 0 ? 7 : 15)) return HEADLOSS_ERR_ALIGN;
     if (reinterpret_cast<uintptr_t>(err) & 3) return HEADLOSS_ERR_ALIGN;
+    if (mode == 2 && (!stats_t || !(temperature > 0.f) || !isfinite(temperature)))
+        return HEADLOSS_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(stats_t) & 3) return HEADLOSS_ERR_ALIGN;
     CUtensorMap mh, mw, mo;
     if (make_map(&mh, hidden, N, D, BM, BK) || make_map(&mw, weight, V, D, BN, BK) ||
         make_map(&mo, logits, N, V, 32, OUT_COLS))
@@ -462,8 +472,9 @@ int launch(int mode, const void* hidden, const void* weight, int N, int D, int V
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return HEADLOSS_ERR_CUDA;
-    const void* fn = mode == 0 ? reinterpret_cast<const void*>(&lmhead_gemm_kernel<0>)
-                               : reinterpret_cast<const void*>(&lmhead_gemm_kernel<1>);
+    const void* fn = mode == 0   ? reinterpret_cast<const void*>(&lmhead_gemm_kernel<0>)
+                     : mode == 1 ? reinterpret_cast<const void*>(&lmhead_gemm_kernel<1>)
+                                 : reinterpret_cast<const void*>(&lmhead_gemm_kernel<2>);
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
         cudaSuccess)
         return HEADLOSS_ERR_CUDA;
@@ -474,12 +485,17 @@ int launch(int mode, const void* hidden, const void* weight, int N, int D, int V
     xf.c = softcap;
     xf.invc = softcap > 0.f ? 1.f / softcap : 0.f;
     xf.k = (softcap > 0.f ? logits_scale * softcap : logits_scale) * 1.4426950408889634f;
+    xf.invT = 1.f / temperature;
+    xf.st_out = stats_t;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (mode == 0)
         lmhead_gemm_kernel<0><<<grid, THREADS, SMEM_BYTES, s>>>(mh, mw, mo, D, MT, NT, stats, xf,
                                                                  err);
-    else
+    else if (mode == 1)
         lmhead_gemm_kernel<1><<<grid, THREADS, SMEM_BYTES, s>>>(mh, mw, mo, D, MT, NT, stats, xf,
+                                                                 err);
+    else
+        lmhead_gemm_kernel<2><<<grid, THREADS, SMEM_BYTES, s>>>(mh, mw, mo, D, MT, NT, stats, xf,
                                                                  err);
     return cudaGetLastError() == cudaSuccess ? HEADLOSS_OK : HEADLOSS_ERR_CUDA;
 }
@@ -494,8 +510,8 @@ extern "C" int headloss_lmhead_logits(const void* hidden, const void* weight, in
 
 extern "C" int headloss_lmhead_logits_rowstats(const void* hidden, const void* weight, int N,
                                                int D, int V, float softcap, float logits_scale,
-                                               void* logits, void* row_stats, int* err,
-                                               void* stream) {
-    return hl_lmhead::launch(1, hidden, weight, N, D, V, softcap, logits_scale, logits, row_stats,
-                             err, stream);
+                                               float temperature, void* logits, void* row_stats,
+                                               float* row_stats_t, int* err, void* stream) {
+    return hl_lmhead::launch(row_stats_t ? 2 : 1, hidden, weight, N, D, V, softcap, logits_scale,
+                             logits, row_stats, err, stream, temperature, row_stats_t);
 }

@@ -129,11 +129,11 @@ def load_library(path: str = LIB_PATH):
     lib.headloss_gspo_seam.argtypes = [vp, vp, vp, vp, i64, i64, vp, i32, f32, f32, f32, vp, vp,
                                        vp]
     lib.headloss_gspo_seam.restype = i32
-    lib.headloss_lmhead_logits_rowstats.argtypes = [vp, vp, i32, i32, i32, f32, f32, vp, vp, vp,
-                                                    vp]
+    lib.headloss_lmhead_logits_rowstats.argtypes = [vp, vp, i32, i32, i32, f32, f32, f32, vp, vp,
+                                                    vp, vp, vp]
     lib.headloss_lmhead_logits_rowstats.restype = i32
     lib.headloss_forward_backward_rowstats.argtypes = [vp, vp, i64, i64, i32, vp, vp, vp, vp, vp,
-                                                       vp, vp]
+                                                       vp, vp, vp, vp, vp]
     lib.headloss_forward_backward_rowstats.restype = i32
     _lib = lib
     return lib
@@ -248,22 +248,28 @@ def headloss_lmhead_logits(hidden, weight, N, D, V, logits, stats, err, stream=N
 
 
 def headloss_lmhead_logits_rowstats(hidden, weight, N, D, V, softcap, logits_scale, logits,
-                                    row_stats, err, stream=None) -> None:
-    """The LM-head GEMM with the loss's per-tile first-pass records
-    (include/headloss_lmhead.h); raises HeadlossError on a bad status."""
+                                    row_stats, err, stream=None, temperature=1.0,
+                                    row_stats_t=None) -> None:
+    """The LM-head GEMM with the loss's per-tile first-pass records, and with
+    row_stats_t the tiles' sums at `temperature` (include/headloss_lmhead.h);
+    raises HeadlossError on a bad status."""
     _check(load_library().headloss_lmhead_logits_rowstats(
         _ptr(hidden), _ptr(weight), int(N), int(D), int(V), float(softcap), float(logits_scale),
-        _ptr(logits), _ptr(row_stats), _ptr(err), _stream(stream)),
-        "headloss_lmhead_logits_rowstats")
+        float(temperature), _ptr(logits), _ptr(row_stats), _ptr(row_stats_t), _ptr(err),
+        _stream(stream)), "headloss_lmhead_logits_rowstats")
 
 
 def headloss_forward_backward_rowstats(h, logits, N, V, dtype, labels, old_logprobs, advantages,
-                                       row_stats, grad_out, scalars_out, stream=None) -> None:
-    """The loss's gradient pass alone from the GEMM's row statistics
-    (include/headloss.h); raises HeadlossError on a bad status."""
+                                       row_stats, grad_out, scalars_out, stream=None,
+                                       teacher=None, row_stats_t=None,
+                                       teacher_stats=None) -> None:
+    """The loss's gradient pass alone from the GEMMs' row statistics (the
+    student's, its sums at the temperature, the teacher's; include/headloss.h);
+    raises HeadlossError on a bad status."""
     _check(load_library().headloss_forward_backward_rowstats(
-        h, _ptr(logits), int(N), int(V), int(dtype), _ptr(labels), _ptr(old_logprobs),
-        _ptr(advantages), _ptr(row_stats), _ptr(grad_out), _ptr(scalars_out), _stream(stream)),
+        h, _ptr(logits), int(N), int(V), int(dtype), _ptr(labels), _ptr(teacher),
+        _ptr(old_logprobs), _ptr(advantages), _ptr(row_stats), _ptr(row_stats_t),
+        _ptr(teacher_stats), _ptr(grad_out), _ptr(scalars_out), _stream(stream)),
         "headloss_forward_backward_rowstats")
 
 

@@ -347,27 +347,38 @@ int headloss_gspo_seam(const float* new_logprobs, const float* old_logprobs,
  * headloss_forward_backward_rowstats -- the loss of headloss_forward_backward
  * from logits whose first-pass statistics the LM-head GEMM already produced
  * (headloss_lmhead_logits_rowstats in include/headloss_lmhead.h): one read of
- * the logits and one write of the gradient per row, no statistics pass.  The
- * fused LM head of ServiceNow Fast-LLM PR #549 ("Correctness": the LM head
- * and tied embeddings) computes the head GEMM and the loss back to back; on
- * GB300 the GEMM's epilogue emits each output tile's share of the softmax
- * statistics from TMEM.
+ * the logits (and the teacher's) and one write of the gradient per row, no
+ * statistics pass.  The fused LM head of ServiceNow Fast-LLM PR #549
+ * ("Correctness": the LM head and tied embeddings) computes the head GEMM and
+ * the loss back to back; on GB300 the GEMM's epilogue emits each output
+ * tile's share of the softmax statistics from TMEM.
  *
- * Arguments as headloss_forward_backward, with no teacher, plus:
- * row_stats:  N x (V / 256) records of 4 fp32 (device, 16-byte aligned) from
- *             headloss_lmhead_logits_rowstats called with this handle's
- *             softcap and logits_scale on the same logits.
- * The handle's losses must be label-based (CE, Z, GRPO, GRPO_STATS,
- * ENTROPY): the distillation losses pair each logit with the teacher's and
- * are not covered by the statistics (ERR_ARG).  dtype must be HEADLOSS_BF16
- * (ERR_DTYPE) and V a multiple of 256 (ERR_ARG).  In place is allowed (each
+ * Arguments as headloss_forward_backward, plus:
+ * row_stats:     N x (V / 256) records of 4 fp32 (device, 16-byte aligned)
+ *                from headloss_lmhead_logits_rowstats called with this
+ *                handle's softcap and logits_scale on the same logits.
+ * row_stats_t:   with a teacher and temperature T != 1: the same call's
+ *                N x (V / 256) sums at T (row_stats_t there, 4-byte aligned);
+ *                null otherwise (at T = 1 the records' S serve).
+ * teacher_stats: with a teacher: N x (V / 256) records from
+ *                headloss_lmhead_logits_rowstats on the teacher's logits with
+ *                softcap 0 and logits_scale 1 / T (16-byte aligned); null
+ *                otherwise.
+ * Losses: CE, Z, GRPO, GRPO_STATS, ENTROPY, and with a teacher DIST_CE and
+ * FKL (their values are summed during the pass: the gradient needs no cross
+ * sum).  REVERSE KL is refused (ERR_ARG): its coefficient needs the cross sum
+ * of pT (log pT - log q) before the pass.  dtype must be HEADLOSS_BF16
+ * (ERR_DTYPE) and V a multiple of 256 (ERR_ARG); a missing teacher_stats, or
+ * row_stats_t at T != 1, is ERR_MISSING_INPUT.  In place is allowed (each
  * word is read before its gradient replaces it).  Three launches; results as
  * headloss_forward_backward, within the same tolerances.
  */
 int headloss_forward_backward_rowstats(headloss_t h, const void* logits, int64_t N, int64_t V,
                                        int dtype, const int64_t* labels,
-                                       const float* old_logprobs, const float* advantages,
-                                       const void* row_stats, void* grad_out, float* scalars_out,
+                                       const void* teacher_logits, const float* old_logprobs,
+                                       const float* advantages, const void* row_stats,
+                                       const float* row_stats_t, const void* teacher_stats,
+                                       void* grad_out, float* scalars_out,
                                        headloss_stream_t stream);
 
 /* Kernel launches one headloss_forward_backward call enqueues (constant). */

@@ -59,19 +59,30 @@ int headloss_lmhead_logits(const void* hidden, const void* weight, int N, int D,
  * statistics headloss_forward_backward_rowstats (include/headloss.h) consumes.
  *
  * softcap, logits_scale: those of the loss handle that will consume the
- *            statistics (softcap c >= 0, 0 = off; logits_scale s > 0).
+ *            statistics (softcap c >= 0, 0 = off; logits_scale s > 0).  For a
+ *            teacher's logits: softcap 0 and logits_scale 1 / T (the teacher
+ *            enters the loss as t / T).
+ * temperature: the distillation temperature T > 0 of the consuming handle;
+ *            read only when row_stats_t is non-null.
  * row_stats: N x (V / 256) records of 4 fp32, device, 16-byte aligned
  *            (written): for the bf16 logits x of row i and tile k, with
  *            zs = s c tanh(x / c) log2(e) (c = 0: zs = s x log2(e)),
  *            (m2, S, E, X): m2 = max zs, S = sum 2^(zs - m2),
  *            E = sum 2^(zs - m2) (zs - m2), X = max |x| (exact: the largest
  *            magnitude among the tile's bf16 logits).
+ * row_stats_t: null, or N x (V / 256) fp32 (device, 4-byte aligned,
+ *            written): S_T = sum 2^((zs - m2) / T) per tile, which a student
+ *            row needs for the distillation losses when T != 1 (one more
+ *            exponential per logit in the epilogue).
  * Other arguments, checks and errors as headloss_lmhead_logits (ERR_ARG also
- * for a negative or non-finite softcap, a non-positive logits_scale).
+ * for a negative or non-finite softcap, a non-positive logits_scale, or a
+ * non-positive or non-finite temperature with row_stats_t; ERR_ALIGN for a
+ * misaligned row_stats_t).
  */
 int headloss_lmhead_logits_rowstats(const void* hidden, const void* weight, int N, int D, int V,
-                                    float softcap, float logits_scale, void* logits,
-                                    void* row_stats, int* err, void* stream);
+                                    float softcap, float logits_scale, float temperature,
+                                    void* logits, void* row_stats, float* row_stats_t, int* err,
+                                    void* stream);
 
 #ifdef __cplusplus
 }

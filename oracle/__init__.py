@@ -238,7 +238,8 @@ def gspo_forward_backward(x, labels, old_logprobs, advantages, seg_offsets, clip
     return scalars, coeff, grad
 
 
-def tile_records(x, softcap: float = 0.0, logits_scale: float = 1.0, tile: int = 256):
+def tile_records(x, softcap: float = 0.0, logits_scale: float = 1.0, tile: int = 256,
+                 temperature: float | None = None):
     """The first-pass statistics of each (row, tile of ``tile`` columns), written out
     plainly in fp64: the record the fused LM head's GEMM epilogue emits for the loss
     (ServiceNow Fast-LLM PR #549, "Approach": the row's softmax statistics built up
@@ -247,14 +248,18 @@ def tile_records(x, softcap: float = 0.0, logits_scale: float = 1.0, tile: int =
 
     With z = s c tanh(x / c) (c = 0: z = s x) and zs = z log2(e) (base 2):
       m2 = max zs, S = sum 2^(zs - m2), E = sum 2^(zs - m2) (zs - m2), X = max |x|,
-    per tile.  Returns an N x (V / tile) x 4 array (m2, S, E, X)."""
+    per tile, and with a temperature T also S_T = sum 2^((zs - m2) / T) (the
+    student's sums at T, which the distillation losses' normaliser needs).
+    Returns an N x (V / tile) x 4 array (m2, S, E, X), or x 5 with S_T last.
+    A teacher's records are those of its logits with softcap 0 and
+    logits_scale 1 / T (the teacher enters the losses as t / T)."""
     x = _f64(x)
     n, V = x.shape
     if V % tile:
         raise ValueError("V must be a multiple of the tile width")
     z = logits_scale * (softcap * np.tanh(x / softcap) if softcap > 0 else x)
     zs = z / math.log(2.0)
-    out = np.zeros((n, V // tile, 4))
+    out = np.zeros((n, V // tile, 4 if temperature is None else 5))
     for t in range(V // tile):
         blk = zs[:, t * tile:(t + 1) * tile]
         m2 = blk.max(axis=1)
@@ -264,4 +269,6 @@ def tile_records(x, softcap: float = 0.0, logits_scale: float = 1.0, tile: int =
         out[:, t, 1] = e.sum(axis=1)
         out[:, t, 2] = (e * d).sum(axis=1)
         out[:, t, 3] = np.abs(x[:, t * tile:(t + 1) * tile]).max(axis=1)
+        if temperature is not None:
+            out[:, t, 4] = np.exp2(d / temperature).sum(axis=1)
     return out

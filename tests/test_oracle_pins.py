@@ -480,3 +480,29 @@ def test_tile_records_closed_forms():
                                rtol=1e-14)
     assert rec[1, 1, 3] == 4.0
     assert rec[1, 1, 0] == 0.0  # the largest zs of tile 1 is a zero logit
+
+
+@pytest.mark.parametrize("T", [1.0, 1.5, 0.5])
+def test_tile_records_at_temperature(T):
+    """S_T merged over a row's tiles (weights 2^((m2_k - M) / T)) is the base-2
+    sum of 2^(zs / T) (scipy's logsumexp); at T = 1 it is S; a constant tile
+    gives 256 and a one-spike tile 1 + 255 2^(-m2 / T)."""
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(5)
+    x = rng.normal(0.0, 3.0, (3, 768))
+    x[0, 256:512] = 0.0
+    x[0, 300] = 4.0
+    rec = orc.tile_records(x, 30.0, 0.5, temperature=T)
+    assert rec.shape == (3, 3, 5)
+    zs = 0.5 * 30.0 * np.tanh(x / 30.0) / math.log(2.0)
+    for i in range(3):
+        M = rec[i, :, 0].max()
+        tot = np.sum(np.exp2((rec[i, :, 0] - M) / T) * rec[i, :, 4])
+        ref = logsumexp(zs[i] * math.log(2.0) / T) / math.log(2.0)
+        assert abs(M / T + math.log2(tot) - ref) < 1e-12
+    if T == 1.0:
+        np.testing.assert_allclose(rec[..., 4], rec[..., 1], rtol=1e-15)
+    m2 = rec[0, 1, 0]
+    assert abs(rec[0, 1, 4] - (1 + 255 * 2 ** (-m2 / T))) < 1e-12
+    c = orc.tile_records(np.full((1, 256), -2.0), 0.0, 1.0, temperature=T)
+    assert c[0, 0, 4] == 256.0
