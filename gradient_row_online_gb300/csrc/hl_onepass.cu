@@ -14,10 +14,11 @@
 // These cover the label-based losses (CE, z-loss, GRPO and its statistics,
 // entropy).  With a teacher (from-distribution CE, forward KL) two more come
 // in: the student tile's S_T = sum 2^((zs - m2) / T) and the teacher GEMM's
-// record of ut = t log2(e) / T.  The gradient then needs no cross sum, and the
-// two losses' values are sums of q (log q - log pT) and q log pT the pass
-// accumulates as it goes (q, pT: the teacher's and the student's softmax at T),
-// added to the row's losses after the pass.  Reverse KL is not covered: its
+// record of ut = t log2(e) / T.  The gradient then needs no cross sum; the
+// forward KL's value, sum q (log q - log pT) (q, pT: the teacher's and the
+// student's softmax at T), is summed as the pass goes and added to the row's
+// losses after it, and the from-distribution CE is that plus the teacher's
+// entropy (from its records).  Reverse KL is not covered: its
 // coefficient needs the cross sum sum pT (log pT - log q) before the pass.
 //
 // Four warps per row, each a quarter of its words (a unit), units strided
@@ -56,13 +57,13 @@ __global__ void __launch_bounds__(OP_THREADS, 2)
     constexpr bool ENTG = ENT && (FEAT & F_ENTG) != 0;
     constexpr int EPW = 8;
     constexpr int CW = TEACH ? 128 : 256;  // words of each operand in a chunk
-    constexpr int NF = TEACH ? 6 : 3;      // merged fields the part warps exchange
+    constexpr int NF = TEACH ? 7 : 3;      // merged fields the part warps exchange
     static_assert(CW * 16 * (TEACH ? 2 : 1) == OP_SLOT_BYTES, "slot size");
 
     __shared__ float recs[OP_WARPS][32 * NREC];
     __shared__ float accs[OP_WARPS][2 * NACC];
     __shared__ RowLoss rls[OP_WARPS];
-    __shared__ float xq[OP_WARPS][2];  // a unit's teacher cross sums, per warp
+    __shared__ float xq[OP_WARPS];  // a unit's forward-KL sum, per warp
     extern __shared__ __align__(128) unsigned char ring_smem[];
     // the part warps' merged records, [part][field][lane], live in the
     // group's record area between the two merge barriers
@@ -234,8 +235,9 @@ __global__ void __launch_bounds__(OP_THREADS, 2)
         // ---- merge the tiles' records: part warp pt, lane k takes tiles
         // pt 32 + k + 128 j (four tiles' loads in flight per lane), then lane
         // k of every part warp merges the four parts' records of lane k ----
-        // student (M, S, E; S_T at the temperature), teacher (Mu, Sq)
-        float M = -CUDART_INF_F, S = 0.f, E = 0.f, ST = 0.f, Mu = -CUDART_INF_F, Sq = 0.f;
+        // student (M, S, E; S_T at the temperature), teacher (Mu, Sq, Eq)
+        float M = -CUDART_INF_F, S = 0.f, E = 0.f, ST = 0.f, Mu = -CUDART_INF_F, Sq = 0.f,
+              Eq = 0.f;
         auto merge_s = [&](float qm, float qs, float qe, float qt) {
             if (!(qs > 0.f)) return;
             if (qm > M) {
@@ -253,13 +255,19 @@ __global__ void __launch_bounds__(OP_THREADS, 2)
                 if (TEACH) ST += exp2f(d * invT) * qt;
             }
         };
-        auto merge_t = [&](float qm, float qs) {
+        auto merge_t = [&](float qm, float qs, float qe) {
             if (!(qs > 0.f)) return;
             if (qm > Mu) {
-                Sq = (Mu == -CUDART_INF_F ? 0.f : exp2f(Mu - qm) * Sq) + qs;
+                const float d = Mu == -CUDART_INF_F ? 0.f : Mu - qm;  // <= 0
+                const float al = exp2f(d);
+                Eq = al * (Eq + d * Sq) + qe;
+                Sq = al * Sq + qs;
                 Mu = qm;
             } else {
-                Sq += exp2f(qm - Mu) * qs;
+                const float d = qm - Mu;
+                const float al = exp2f(d);
+                Eq += al * (qe + d * qs);
+                Sq += al * qs;
             }
         };
         const float4* rrow = rs + r * NT;
@@ -280,7 +288,7 @@ __global__ void __launch_bounds__(OP_THREADS, 2)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 merge_s(q[j].x, q[j].y, q[j].z, TEACH ? qt[j] : 0.f);
-                if (TEACH) merge_t(qu[j].x, qu[j].y);
+                if (TEACH) merge_t(qu[j].x, qu[j].y, qu[j].z);
             }
         }
         float zy = 0.f, hasy = 0.f;
@@ -297,6 +305,7 @@ __global__ void __launch_bounds__(OP_THREADS, 2)
                 m[96] = ST;
                 m[128] = Mu;
                 m[160] = Sq;
+                m[192] = Eq;
             }
         }
         // all four warps have read the label logit and stored their records
@@ -304,13 +313,13 @@ __global__ void __launch_bounds__(OP_THREADS, 2)
         // overwrites the label logit) or the merged records (next)
         group_sync();
         M = -CUDART_INF_F;
-        S = E = ST = Sq = 0.f;
+        S = E = ST = Sq = Eq = 0.f;
         Mu = -CUDART_INF_F;
 #pragma unroll
         for (int pt = 0; pt < OP_PARTS; ++pt) {
             const float* m = mg + pt * NF * 32 + lane;
             merge_s(m[0], m[32], m[64], TEACH ? m[96] : 0.f);
-            if (TEACH) merge_t(m[128], m[160]);
+            if (TEACH) merge_t(m[128], m[160], m[192]);
         }
         // all have read the exchanged records before the area takes the
         // lane records below
@@ -322,8 +331,8 @@ __global__ void __launch_bounds__(OP_THREADS, 2)
         rec[R_E] = E;
         rec[R_ST] = ST;
         rec[R_SQ] = Sq;
-        rec[R_EQ] = 0.f;  // the distillation values come from the pass (below)
-        rec[R_XP] = 0.f;
+        rec[R_EQ] = Eq;
+        rec[R_XP] = 0.f;  // the forward KL comes from the pass (below)
         rec[R_Y] = 0.f;
         rec[R_ZY] = zy;
         rec[R_HASY] = hasy;
@@ -348,10 +357,10 @@ __global__ void __launch_bounds__(OP_THREADS, 2)
         const f2 nlseT2 = pk1(h.nlseT), nlsq2 = pk1(h.nlsq), tc2 = pk1(h.tc), qc2 = pk1(h.qc);
         const int64_t ywd = has_labels ? y / EPW : -1;  // the label's word
         const int iyw = has_labels ? int(y - ywd * EPW) : 0;
-        // teacher cross sums of this unit, in units of 2^sg (the exponent
-        // shift shared by every exponential): B1 = sum 2^sg q (log2 q -
-        // log2 pT), B2 = sum 2^sg q (log2 pT + sg)
-        f2 B1 = pk1(0.f), B2 = pk1(0.f);
+        // the forward KL's sum over this unit, in units of 2^sg (the
+        // exponent shift shared by every exponential): B1 = sum 2^sg q
+        // (log2 q - log2 pT)
+        f2 B1 = pk1(0.f);
         // softcap: the tier of chunk c of this unit (c < 32; later chunks take
         // tier X): lane c takes the largest |x| of the tiles the chunk spans
         uint32_t mA = 0u, mB = 0u;
@@ -416,10 +425,7 @@ __global__ void __launch_bounds__(OP_THREADS, 2)
                     const f2 pT = ex2p(argT), q = ex2p(argq);
                     g = fma2(pT, tc2, g);
                     g = fma2(q, qc2, g);
-                    if (live) {
-                        B1 = fma2(q, sub2(argq, argT), B1);
-                        B2 = fma2(q, argT, B2);
-                    }
+                    if (live) B1 = fma2(q, sub2(argq, argT), B1);
                 }
                 const f2 gw = CAP ? mul2(g, omt) : g;
                 out[kq] = P16::pack(p.accumulate ? add2(P16::unpack(oa[kq]), gw) : gw);
@@ -464,21 +470,31 @@ __global__ void __launch_bounds__(OP_THREADS, 2)
         };
         // one chunk from the ring: CW / 32 words a lane, unrolled; the words
         // past a short chunk's end are computed and neither stored nor summed
+        // (with a teacher a full chunk, the common case, tests no word)
         const bool store = grow != nullptr;
-        auto chunk = [&](const unsigned char* sb, __nv_bfloat16* gc, int cw, int jy, auto tierc) {
+        auto chunk = [&](const unsigned char* sb, __nv_bfloat16* gc, int cw, int jy, auto tierc,
+                         auto fullc) {
+            constexpr bool FULL = decltype(fullc)::value;
 #pragma unroll
             for (int i = 0; i < CW / 32; ++i) {
                 const int j = lane + 32 * i;
+                const bool in = FULL || j < cw;
                 const uint4 a = *reinterpret_cast<const uint4*>(sb + size_t(j) * 16);
                 uint4 b = make_uint4(0, 0, 0, 0);
                 if (TEACH) b = *reinterpret_cast<const uint4*>(sb + CW * 16 + size_t(j) * 16);
                 uint4 ow = make_uint4(0, 0, 0, 0);
-                if (p.accumulate && j < cw)
-                    ow = *reinterpret_cast<const uint4*>(gc + size_t(j) * EPW);
-                uint4 o = word(a, b, ow, j < cw, tierc);
+                if (p.accumulate && in) ow = *reinterpret_cast<const uint4*>(gc + size_t(j) * EPW);
+                uint4 o = word(a, b, ow, in, tierc);
                 if (j == jy) o = patch(o, a, b, ow);
-                if (store && j < cw) *reinterpret_cast<uint4*>(gc + size_t(j) * EPW) = o;
+                if (store && in) *reinterpret_cast<uint4*>(gc + size_t(j) * EPW) = o;
             }
+        };
+        // (the split pays only where a word's test guards the cross sum: with
+        // a teacher; without, the doubled code measured slower)
+        auto chunk_t = [&](const unsigned char* sb, __nv_bfloat16* gc, int cw, int jy,
+                           auto tierc) {
+            if (TEACH && cw == CW) chunk(sb, gc, cw, jy, tierc, std::true_type{});
+            else chunk(sb, gc, cw, jy, tierc, std::false_type{});
         };
         for (int64_t c = 0; c < nch; ++c) {
             const unsigned char* sb = acquire();
@@ -487,40 +503,34 @@ __global__ void __launch_bounds__(OP_THREADS, 2)
             const int jy = (ywd >= c0 && ywd < c0 + cw) ? int(ywd - c0) : -1;
             __nv_bfloat16* gc = store ? grow + c0 * EPW : nullptr;
             if (!CAP) {
-                chunk(sb, gc, cw, jy, std::integral_constant<int, -1>{});
+                chunk_t(sb, gc, cw, jy, std::integral_constant<int, -1>{});
             } else {
                 const bool inA = c < 32 && ((mA >> c) & 1u), inB = c < 32 && ((mB >> c) & 1u);
-                if (inA) chunk(sb, gc, cw, jy, std::integral_constant<int, 0>{});
-                else if (inB) chunk(sb, gc, cw, jy, std::integral_constant<int, 1>{});
-                else chunk(sb, gc, cw, jy, std::integral_constant<int, 2>{});
+                if (inA) chunk_t(sb, gc, cw, jy, std::integral_constant<int, 0>{});
+                else if (inB) chunk_t(sb, gc, cw, jy, std::integral_constant<int, 1>{});
+                else chunk_t(sb, gc, cw, jy, std::integral_constant<int, 2>{});
             }
             release();
         }
         if (TEACH) {
-            // the row's distillation values from the four warps' cross sums:
-            // forward KL = ln2 sum q (log2 q - log2 pT), from-distribution
-            // CE = -ln2 sum q log2 pT (sum q = 1)
-            float b1 = hsum(B1), b2 = hsum(B2);
+            // the row's distillation values: forward KL = ln2 sum q (log2 q -
+            // log2 pT) from the four warps' sums; the epilogue's values, with
+            // the cross sum left out, differ by the teacher's entropy
+            // (from-distribution CE = forward KL + H(q)), which holds for the
+            // true values as well
+            float b1 = hsum(B1);
 #pragma unroll
-            for (int o = 16; o; o >>= 1) {
-                b1 += __shfl_xor_sync(0xffffffffu, b1, o);
-                b2 += __shfl_xor_sync(0xffffffffu, b2, o);
-            }
-            if (lane == 0) {
-                xq[warp][0] = b1;
-                xq[warp][1] = b2;
-            }
+            for (int o = 16; o; o >>= 1) b1 += __shfl_xor_sync(0xffffffffu, b1, o);
+            if (lane == 0) xq[warp] = b1;
             group_sync();
             if (lane == 0 && part == 0) {
-                float s1 = 0.f, s2 = 0.f;
-                for (int pt = 0; pt < OP_PARTS; ++pt) {
-                    s1 += xq[warp + pt][0];
-                    s2 += xq[warp + pt][1];
-                }
+                float s1 = 0.f;
+                for (int pt = 0; pt < OP_PARTS; ++pt) s1 += xq[warp + pt];
                 const float sg = rintf(h.nlsq + k.lsq2);  // the shift: nlsq = sg - lsq2
                 const float sc = __uint_as_float(uint32_t(127 - int(sg)) << 23);  // 2^-sg
-                rls[warp].fkl = LN2 * s1 * sc;
-                rls[warp].dce = -LN2 * fmaf(s2, sc, -sg);
+                const float fkl = LN2 * s1 * sc;
+                rls[warp].dce = fkl + (rls[warp].dce - rls[warp].fkl);
+                rls[warp].fkl = fkl;
                 row_accumulate(p, rls[warp], accs[warp], r);
             }
         }
