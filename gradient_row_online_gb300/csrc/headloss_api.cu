@@ -177,9 +177,18 @@ int feature_set(const headloss* h) {
     return f;
 }
 
+// fp32 rows in double-float arithmetic where fp32 pairs carry the precision:
+// no teacher, no softcap, no entropy gradient term, and no accumulation (each
+// term is good to ~2^-26 of itself, which an existing value of the opposite
+// sign could leave exposed).
+bool uses_df(int dtype, int feat) {
+    return dtype == HEADLOSS_FP32 && !(feat & (F_ACC | F_TEACH | F_SOFTCAP | F_ENTG));
+}
+
 // The kernel of `kind` for `dtype` and the feature set `feat` (F_ACC selects
 // the accumulating instantiation; the fp32 kernel reads the flag at run time).
 const void* kernel_for(int kind, int dtype, int feat) {
+    const bool df = uses_df(dtype, feat);
     const bool acc = (feat & F_ACC) != 0;
     feat &= ~F_ACC;
     if (kind == HEADLOSS_KERNEL_STREAM) {
@@ -194,14 +203,7 @@ const void* kernel_for(int kind, int dtype, int feat) {
     switch (dtype) {
         case HEADLOSS_BF16: return rows_kernel_bf16(feat & F_BASE);
         case HEADLOSS_FP16: return rows_kernel_fp16(feat & F_BASE);
-        case HEADLOSS_FP32:
-            // double-float arithmetic where fp32 pairs carry the precision: no
-            // teacher, no softcap, no entropy gradient term, and no
-            // accumulation (each term is good to ~2^-26 of itself, which an
-            // existing value of the opposite sign could leave exposed)
-            return rows_kernel_fp32(
-                (feat & F_BASE) |
-                ((acc || (feat & (F_TEACH | F_SOFTCAP | F_ENTG))) ? 0 : int(F_DF)));
+        case HEADLOSS_FP32: return rows_kernel_fp32((feat & F_BASE) | (df ? int(F_DF) : 0));
         default: return nullptr;
     }
 }
@@ -242,6 +244,7 @@ int resident_candidates(headloss* h, int64_t V, int dtype, int feat, Plan* cand,
     const int epw = 16 / es;
     const int ops = (feat & F_TEACH) ? 2 : 1;
     const int acc_bytes = dtype == HEADLOSS_FP32 ? 8 : 4;
+    const bool df = uses_df(dtype, feat);
     const int budget = h->smem_optin - smem_fixed_bytes(acc_bytes);
     // the attribute is a per-kernel cap shared by every handle: always the device maximum
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -255,8 +258,12 @@ int resident_candidates(headloss* h, int64_t V, int dtype, int feat, Plan* cand,
         if (C > 1 && (C - 1) * L >= V && !h->forced.cluster) continue;  // an idle CTA
         const int64_t words = L / epw + 2;
         const int64_t stage = words * 16 * ops;
+        // double-float: the low parts of the stored exponentials, bf16, one
+        // set per CTA after the fixed area (16-byte aligned)
+        const int64_t extra = df ? words * 8 + 16 : 0;
+        const int64_t room = budget - extra;
         const int64_t max_nbuf =
-            budget / stage < MAX_RESIDENT_STAGES ? budget / stage : MAX_RESIDENT_STAGES;
+            room / stage < MAX_RESIDENT_STAGES ? room / stage : MAX_RESIDENT_STAGES;
         for (int ti = 0; ti < 2; ++ti) {
             const int T = kThreads[ti];
             if (!wants(h->forced.threads, T)) continue;
@@ -270,7 +277,7 @@ int resident_candidates(headloss* h, int64_t V, int dtype, int feat, Plan* cand,
                 pl.words = int(words);
                 pl.nbuf = int(nbuf);
                 pl.threads = T;
-                pl.smem = int(stage * nbuf) + smem_fixed_bytes(acc_bytes);
+                pl.smem = int(stage * nbuf + extra) + smem_fixed_bytes(acc_bytes);
                 int ncl = 0;
                 const int rc = active_clusters(kernel, C, T, pl.smem, h->num_sms, &ncl);
                 if (rc) return rc;

@@ -32,6 +32,13 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
     A* xch = reinterpret_cast<A*>(acc + NACC);          // [2][MAX_CLUSTER][NREC]
     A* red = xch + 2 * MAX_CLUSTER * NREC;              // [NWARPS][NREC]
     A* coef = red + NWARPS * NREC;                      // [16]
+    // double-float path: coef[13] the slice's raw maximum, coef[12] the label
+    // logit (its shared-memory copy is overwritten by 2^d); the low parts of
+    // the stored 2^d, as bf16, after the fixed area
+    constexpr int DF_VMAX = 13, DF_VY = 12;
+    float* const df_vy = reinterpret_cast<float*>(coef + DF_VY);  // fp32: no conversion per element
+    __nv_bfloat16* elb = reinterpret_cast<__nv_bfloat16*>(
+        smem + ((size_t(stage_bytes) * p.nbuf + smem_fixed_bytes(sizeof(A)) + 15) & ~size_t(15)));
 
     const int C = p.C;
     uint32_t rank, cid, ncl;
@@ -204,7 +211,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
             if (tid == 0) {
                 coef[0] = nonempty ? zs_of(mx[0]) : A(-CUDART_INF);
                 coef[1] = (TEACH && nonempty) ? mul_rn(mx[1], KT) : A(-CUDART_INF);
-                if (DFM) coef[2] = mx[0];  // the raw maximum, for the double-float shift
+                if (DFM) coef[DF_VMAX] = mx[0];  // the raw maximum, for the double-float shift
             }
             __syncthreads();
             const A zm = coef[0], um = coef[1];
@@ -220,23 +227,34 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
                 // maximum, whose product is formed the same way: a one-column
                 // row's CE is then exactly 0), summed by two-sums; terms below
                 // 2^-126 (beside the maximum's 1) are dropped.  The shift
-                // differs from the record's fp64 zm by ~2^-48 |zm|.
-                const float vmax = float(coef[2]);
+                // differs from the record's fp64 zm by ~2^-48 |zm|.  Each
+                // 2^d, times 2^64, replaces its logit in shared memory (high
+                // part; the low part as bf16 beside) for the gradient pass,
+                // which then only scales it; the label logit is kept apart.
+                const float vmax = float(coef[DF_VMAX]);
                 DF Zd = df_two_prod(vmax, Kd.h);
                 Zd.l = __fmaf_rn(vmax, Kd.l, Zd.l);
+                const bool keep = gg != nullptr && !p.accumulate;
+                const int64_t eyl = (has_labels && y >= col0 && y < col1) ? r * V + y : -1;
                 float Sh = 0.f, Sl = 0.f, Eh = 0.f, El = 0.f;
                 for (int w = tid; w < nw; w += nthr) {
                     const int64_t eb = (wf + w) * EPW;
                     const bool full = eb >= e0 && eb + EPW <= e1;
                     const float4 q4 = *reinterpret_cast<const float4*>(xs_b + size_t(w) * 16);
                     const float vv[4] = {q4.x, q4.y, q4.z, q4.w};
+                    float kh[4], kl[4];
 #pragma unroll
                     for (int i = 0; i < EPW; ++i) {
-                        if (!(full || (eb + i >= e0 && eb + i < e1))) continue;
+                        const bool in = full || (eb + i >= e0 && eb + i < e1);
+                        if (eb + i == eyl) *df_vy = vv[i];
                         const DF d = df_scaled_minus(vv[i], Kd, Zd);
                         int n;
                         const DF e = df_exp2(d, n);
-                        if (n < -126) continue;
+                        const bool big = n + 64 >= -126;  // 2^d 2^64 normal
+                        const float s64 = big ? df_pow2i(n + 64) : 0.f;
+                        kh[i] = __fmul_rn(e.h, s64);
+                        kl[i] = __fmul_rn(e.l, s64);
+                        if (!in || n < -126) continue;
                         const float sc = df_pow2i(n);
                         const float eh = __fmul_rn(e.h, sc), el = __fmul_rn(e.l, sc);
                         const DF s2 = df_two_sum(Sh, eh);
@@ -249,6 +267,15 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
                             Eh = e2.h;
                             El = __fadd_rn(El, __fadd_rn(e2.l, pe.l));
                         }
+                    }
+                    if (keep) {
+                        *reinterpret_cast<float4*>(xs_b + size_t(w) * 16) =
+                            make_float4(kh[0], kh[1], kh[2], kh[3]);
+                        __nv_bfloat162 l01 = __floats2bfloat162_rn(kl[0], kl[1]);
+                        __nv_bfloat162 l23 = __floats2bfloat162_rn(kl[2], kl[3]);
+                        *reinterpret_cast<uint2*>(elb + size_t(w) * 4) =
+                            make_uint2(*reinterpret_cast<uint32_t*>(&l01),
+                                       *reinterpret_cast<uint32_t*>(&l23));
                     }
                 }
                 // block sums in double-float (fp32 shuffles and two-sums),
@@ -338,7 +365,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
                 rec[R_HASY] = A(0);
                 if (has_labels && y >= col0 && y < col1) {
                     const int64_t ey = r * V + y;
-                    rec[R_ZY] = zs_of(Tr::to_acc(xs[ey - wf * EPW]));
+                    rec[R_ZY] = DFM ? zs_of(A(*df_vy)) : zs_of(Tr::to_acc(xs[ey - wf * EPW]));
                     rec[R_HASY] = A(1);
                 }
                 if (C > 1) {
@@ -391,36 +418,53 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
             const A dlse = lseT2 - lsq2;
             const int64_t ey = (has_labels && valid && y >= col0 && y < col1) ? r * V + y : -1;
             if (DFM && !p.accumulate) {
-                // double-float kernel: fp32 words in and out.  Non-label
-                // elements: pc 2^(v K - lse2) in double-float, rounded once
-                // (then scaled by 2^n, exactly while normal); the label
+                // double-float kernel: fp32 words out.  Non-label elements:
+                // pc 2^(zs - lse2) = pc 2^(Z - lse2) 2^d with 2^d (times
+                // 2^64) stored by the statistics pass: P = pc 2^(Z - lse2)
+                // once per row in double-float, then P (hi + lo) rounded once
+                // and scaled by 2^-64 (exactly while normal); the label
                 // element in fp64 (it subtracts bc and may cancel).
                 // (Accumulating calls take the fp64 kernel; this branch never
                 // sees one.)
-                const DF Ld = split(double(lse2)), Pd = split(double(pc));
+                DF Pp = {0.f, 0.f};
+                int nsc = 0;
+                if (valid) {
+                    const float vmax = float(coef[DF_VMAX]);
+                    DF Zd = df_two_prod(vmax, Kd.h);
+                    Zd.l = __fmaf_rn(vmax, Kd.l, Zd.l);
+                    const double cz = (double(Zd.h) + double(Zd.l)) - double(lse2);  // <= ~0
+                    int nc;
+                    const DF Cd = df_exp2(split(cz), nc);
+                    const DF Pd = split(double(pc));
+                    Pp = df_two_prod(Pd.h, Cd.h);
+                    Pp.l = __fmaf_rn(Pd.h, Cd.l, __fmaf_rn(Pd.l, Cd.h, Pp.l));
+                    nsc = nc - 64;
+                }
+                const bool scale_exact = nsc >= -126;
+                const float psc = scale_exact ? df_pow2i(nsc) : 0.f;
                 for (int w = tid; w < nw; w += nthr) {
                     const int64_t eb = (wf + w) * EPW;
                     const bool full = eb >= e0 && eb + EPW <= e1;
                     float out[4] = {0.f, 0.f, 0.f, 0.f};
                     if (valid) {
-                        const float4 q4 = *reinterpret_cast<const float4*>(xs_b + size_t(w) * 16);
-                        const float vv[4] = {q4.x, q4.y, q4.z, q4.w};
+                        const float4 k4 = *reinterpret_cast<const float4*>(xs_b + size_t(w) * 16);
+                        const uint2 l4 = *reinterpret_cast<const uint2*>(elb + size_t(w) * 4);
+                        const float kh[4] = {k4.x, k4.y, k4.z, k4.w};
+                        const float kl[4] = {__uint_as_float(l4.x << 16),
+                                             __uint_as_float(l4.x & 0xffff0000u),
+                                             __uint_as_float(l4.y << 16),
+                                             __uint_as_float(l4.y & 0xffff0000u)};
 #pragma unroll
                         for (int i = 0; i < EPW; ++i) {
-                            const DF d = df_scaled_minus(vv[i], Kd, Ld);
-                            int n;
-                            const DF e = df_exp2(d, n);
-                            DF g = df_two_prod(Pd.h, e.h);
-                            g.l = __fmaf_rn(Pd.h, e.l, __fmaf_rn(Pd.l, e.h, g.l));
+                            DF g = df_two_prod(Pp.h, kh[i]);
+                            g.l = __fmaf_rn(Pp.h, kl[i], __fmaf_rn(Pp.l, kh[i], g.l));
                             const float rr = __fadd_rn(g.h, g.l);
-                            out[i] = n >= -126 ? __fmul_rn(rr, df_pow2i(n))
-                                               : (n >= -300 ? ldexpf(rr, n) : 0.f);
+                            out[i] = scale_exact ? __fmul_rn(rr, psc) : ldexpf(rr, nsc);
                         }
                         if (ey >= eb && ey < eb + EPW) {
                             const int i = int(ey - eb);
-                            const float vy = i == 0 ? vv[0] : i == 1 ? vv[1] : i == 2 ? vv[2] : vv[3];
-                            const float gy =
-                                __double2float_rn(ex2(mul_rn(A(vy), K) - lse2) * pc - bc);
+                            const float gy = __double2float_rn(
+                                ex2(mul_rn(A(*df_vy), K) - lse2) * pc - bc);
 #pragma unroll
                             for (int k = 0; k < EPW; ++k)
                                 if (k == i) out[k] = gy;
