@@ -202,6 +202,25 @@ __device__ __forceinline__ void tile_of(int i, int MT, int NT, int& m, int& n) {
 // E = sum 2^(zs - m2) (zs - m2) and X = max |x| (which picks the loss
 // kernel's tanh form).  MODE 2: MODE 1's record and, apart, the tile's sum at
 // the distillation temperature T, S_T = sum 2^((zs - m2) / T).
+// The statistics modes' per-logit arithmetic, one MUFU op each (relative
+// error ~2^-22): the records feed the loss's normalisers, which the 16-bit
+// gradient needs to ~2^-9 only.
+__device__ __forceinline__ float ex2_mufu(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float rcp_mufu(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+// tanh(y) = sign(y) (1 - w) / (1 + w), w = 2^(-2 log2(e) |y|) in (0, 1]
+__device__ __forceinline__ float tanh_mufu(float y) {
+    const float w = ex2_mufu(-2.8853900817779268f * fabsf(y));
+    return copysignf((1.f - w) * rcp_mufu(1.f + w), y);
+}
+
 struct Xform {
     float c, invc, k;  // softcap (0: off), 1 / c, s * c * log2(e) (c = 0: s * log2(e))
     float invT;        // MODE 2: 1 / T
@@ -350,8 +369,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                         v[2 * t + 1] = __high2float(b2);
                         if (MODE >= 1) {  // zs of the bf16 logits, their largest |x|
                             ax = fmaxf(ax, fmaxf(fabsf(v[2 * t]), fabsf(v[2 * t + 1])));
-                            v[2 * t] = xf.c > 0.f ? xf.k * tanhf(v[2 * t] * xf.invc) : xf.k * v[2 * t];
-                            v[2 * t + 1] = xf.c > 0.f ? xf.k * tanhf(v[2 * t + 1] * xf.invc)
+                            v[2 * t] = xf.c > 0.f ? xf.k * tanh_mufu(v[2 * t] * xf.invc)
+                                                  : xf.k * v[2 * t];
+                            v[2 * t + 1] = xf.c > 0.f ? xf.k * tanh_mufu(v[2 * t + 1] * xf.invc)
                                                       : xf.k * v[2 * t + 1];
                         }
                         cm = fmaxf(cm, fmaxf(v[2 * t], v[2 * t + 1]));
@@ -364,17 +384,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                     } else {
                         // rescale the running sums to the new max, then add the chunk
                         const float dm = mx == -INFINITY ? 0.f : mx - nm;
-                        const float al = exp2f(dm);
+                        const float al = ex2_mufu(dm);
                         esum = al * (esum + dm * ssum);
                         ssum *= al;
-                        if (MODE == 2) tsum *= exp2f(dm * xf.invT);
+                        if (MODE == 2) tsum *= ex2_mufu(dm * xf.invT);
 #pragma unroll
                         for (int t = 0; t < 32; ++t) {
                             const float d = v[t] - nm;
-                            const float e = exp2f(d);
+                            const float e = ex2_mufu(d);
                             ssum += e;
                             esum = fmaf(e, d, esum);
-                            if (MODE == 2) tsum += exp2f(d * xf.invT);
+                            if (MODE == 2) tsum += ex2_mufu(d * xf.invT);
                         }
                     }
                     mx = nm;
