@@ -84,8 +84,8 @@ def run_gpu(wl, inp, grad=True, inplace=False, plan=None, handle=None):
 def oracle_rows(wl, inp, rows=None, want_grad=True, want_gmag=True, chunk=1024):
     """Oracle records (and gradient / magnitude) of the selected rows (default all)."""
     cfg = oracle_cfg(wl)
-    labels_all = host_i64(inp["labels"])
-    n_valid = orc.count_valid(labels_all, labels_all.shape[0])
+    labels_all = host_i64(inp["labels"])  # None: no mask, every row valid
+    n_valid = orc.count_valid(labels_all, inp["logits"].shape[0])
     idx = np.arange(inp["logits"].shape[0]) if rows is None else np.asarray(rows)
     recs, grads, gmags = [], [], []
     for c0 in range(0, len(idx), chunk):

@@ -226,6 +226,26 @@ def test_fp32_double_float_far_apart_logits():
     full_check(small(("ce",), N=30, V=2000, dtype=torch.float32, sigma=40.0))
 
 
+# no labels (no mask, every row valid): the losses that need none, both kernels
+@pytest.mark.parametrize("plan", [dict(kernel=RESIDENT, cluster=2, stages=1, threads=256),
+                                  dict(kernel=STREAM, stages=3, threads=256, chunk_words=4)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_without_labels(plan, dtype):
+    if dtype == torch.float32 and plan["kernel"] == STREAM:
+        pytest.skip("the streaming kernel takes 16-bit rows")
+    # fp32 rows without softcap and entropy gradient take the double-float kernel
+    for losses, w in ((("dist_ce", "fkl", "rkl", "entropy"), FULL_W), (("z", "entropy"), NO_ENT_GRAD),
+                      (("fkl",), FULL_W)):
+        wl = small(losses, N=29, V=4104, dtype=dtype, logits_scale=0.7, weights=dict(w),
+                   softcap=20.0 if dtype == torch.bfloat16 else 0.0)
+        inp = dict(W.make_inputs(wl, "cuda"), labels=None)
+        got, g, _ = H.run_gpu(wl, inp, plan=plan)
+        cfg, rec, ref, gmag = H.oracle_rows(wl, inp)
+        assert got[14] == wl.N
+        H.check_scalars(wl, got, cfg, rec)
+        H.check_grad(wl, g, ref, gmag, rec)
+
+
 def test_large_logits_fp32():
     wl = small(("ce", "z", "entropy", "fkl", "rkl"), N=8, V=513, dtype=torch.float32,
                sigma=1e4)

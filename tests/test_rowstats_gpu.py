@@ -116,6 +116,20 @@ def test_rowstats_with_teacher_against_oracle(losses, softcap, scale, T):
     H.check_grad(wl, g, ref, gmag, rec)
 
 
+@pytest.mark.parametrize("losses", [("dist_ce", "fkl", "entropy"), ("z", "entropy")])
+def test_rowstats_without_labels(losses):
+    """No labels (every row valid): the losses that need none, with and without a
+    teacher."""
+    wl = W.Workload("rowstats", 256, 4096, torch.bfloat16, losses, dict(W_DIST), softcap=30.0,
+                    logits_scale=0.5, temperature=1.5, teacher_noise=1.0, seed=3)
+    inp = dict(W.make_inputs(wl, "cuda"), labels=None)
+    got, g, ref_inp = _run(wl, inp)
+    cfg, rec, ref, gmag = H.oracle_rows(wl, ref_inp)
+    assert got[14] == 256
+    H.check_scalars(wl, got, cfg, rec)
+    H.check_grad(wl, g, ref, gmag, rec)
+
+
 def _oracle_stats(inp, wl):
     """Per-tile records from the oracle's plain definition (for rows too wide
     for an identity-weight GEMM), as the kernel takes them."""
