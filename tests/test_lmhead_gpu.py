@@ -130,3 +130,29 @@ def test_lmhead_host_checks():
         with pytest.raises(hlb.HeadlossError) as e:
             call(*args)
         assert e.value.status == status
+
+
+def test_lmhead_rowstats_host_checks():
+    """The statistics call's own checks: softcap, scale and (with sums at a
+    temperature) the temperature and the sums' alignment."""
+    hid, wt = _inputs(128, 64, 256)
+    out = torch.empty(128, 256, dtype=torch.bfloat16, device="cuda")
+    rs = torch.empty(128, 1, 4, device="cuda")
+    rsT = torch.empty(128, 2, device="cuda")
+    err = torch.zeros(2, dtype=torch.int32, device="cuda")
+    call = hlb.headloss_lmhead_logits_rowstats
+    base = (hid, wt, 128, 64, 256)
+    for kw, status in [(dict(softcap=-1.0), hlb.HEADLOSS_ERR_ARG),
+                       (dict(scale=0.0), hlb.HEADLOSS_ERR_ARG),
+                       (dict(temperature=0.0, row_stats_t=rsT), hlb.HEADLOSS_ERR_ARG),
+                       (dict(temperature=float("inf"), row_stats_t=rsT), hlb.HEADLOSS_ERR_ARG),
+                       (dict(row_stats_t=rsT.data_ptr() + 2), hlb.HEADLOSS_ERR_ALIGN),
+                       (dict(row_stats=rs.data_ptr() + 8), hlb.HEADLOSS_ERR_ALIGN)]:
+        a = dict(softcap=0.0, scale=1.0, temperature=1.5, row_stats_t=None, row_stats=rs)
+        a.update(kw)
+        with pytest.raises(hlb.HeadlossError) as e:
+            call(*base, a["softcap"], a["scale"], out, a["row_stats"], err,
+                 temperature=a["temperature"], row_stats_t=a["row_stats_t"])
+        assert e.value.status == status
+    torch.cuda.synchronize()
+    assert int(err[0].item()) == 0  # nothing ran
