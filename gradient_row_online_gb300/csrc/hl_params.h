@@ -22,8 +22,9 @@ enum : int {
     // pairs) instead of fp64; for student-only rows without softcap whose
     // gradient has no entropy term (the entropy may still be a metric)
     F_DF = 128,
-    // streaming kernel only: L2 cache hints on the row copies (first pass
-    // evict-last, second pass evict-first) and streaming gradient stores; for
+    // streaming kernel only: L2 cache hints on the row copies (the teacher's
+    // first pass evict-last, second pass evict-first) and streaming gradient
+    // stores; for
     // teacher rows without softcap, where it measured faster (the second read
     // then hits L2 more often)
     F_L2P = 256,

@@ -219,14 +219,17 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
 #endif
         const uint32_t dst = smem_addr(smem + size_t(sl) * slot_bytes);
         if constexpr ((FEAT & F_L2P) != 0) {
-            // first-pass copies stay in L2 for the second pass's re-read,
-            // second-pass copies (their last use) go first
+            // the teacher's first-pass copies stay in L2 for the second
+            // pass's re-read; second-pass copies (their last use) go first
+            // (the student's first pass as well was measured slower)
             uint64_t pol;
-            if (jl < K)
+            if (jl < K) {
                 asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-            else
+                bulk_g2s(dst, xg + r * V + c0, bytes, bar);
+            } else {
                 asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-            bulk_g2s_hint(dst, xg + r * V + c0, bytes, bar, pol);
+                bulk_g2s_hint(dst, xg + r * V + c0, bytes, bar, pol);
+            }
             if (TEACH) bulk_g2s_hint(dst + opbytes, tg + r * V + c0, bytes, bar, pol);
         } else {
             bulk_g2s(dst, xg + r * V + c0, bytes, bar);
