@@ -336,8 +336,8 @@ def run_ours(args, rank, world, local):
     if not args.no_per_loss and world == 1:
         line["per_loss_loop"] = per_loss_loop(wl, inp, grad, dev)
     # the end-to-end steps next, on the main workload's tensors, before the
-    # other legs' allocations (measured: after them, the same steps ran up to
-    # 1.75x slower on the host link)
+    # other legs' allocations (the host link's speed varies from run to run;
+    # this keeps the other legs out of it)
     if not args.no_e2e:
         del grad
         line["e2e"] = e2e(wl, h, inp, args, dev, world)
