@@ -35,6 +35,9 @@ __global__ void __launch_bounds__(1024) count_valid_kernel(const int64_t* labels
                                                            float grad_scale, double divisor,
                                                            float* kscale) {
     __shared__ long long part[32];
+    // the row kernel may start now; it waits for this grid before it reads
+    // the count
+    asm volatile("griddepcontrol.launch_dependents;");
     long long c = 0;
     int bad = 0;
     if (labels) {
@@ -75,6 +78,7 @@ __global__ void __launch_bounds__(32 * NACC) finalize_kernel(const double* parti
                                                              const long long* n_valid,
                                                              FinalizeArgs a, float* out) {
     __shared__ double tot[NACC];
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the row kernel has completed
     const int t = threadIdx.x >> 5, lane = threadIdx.x & 31;
     double s = 0.0;
     for (int c = lane; c < nclusters; c += 32) s += partials[size_t(c) * NACC + t];
@@ -703,18 +707,24 @@ int headloss_forward_backward_ext(headloss_t h, const void* logits, int64_t N, i
         p.accumulate = x.accumulate;
         p.tok = x.token_coeff;
 
+        // programmatic dependent launch: the row kernel's CTAs start while
+        // the count kernel runs and wait for it before they read the count
+        // (griddepcontrol.wait); the finalize kernel likewise after the row
+        // kernel (measured: CE + z 0.206 -> 0.202 ms, the larger sets ~0.2%)
         cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = pl.C;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = pl.C;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
         cfg.gridDim = dim3(ncl * pl.C, 1, 1);
         cfg.blockDim = dim3(pl.threads, 1, 1);
         cfg.dynamicSmemBytes = pl.smem;
         cfg.stream = s;
         cfg.attrs = attr;
-        cfg.numAttrs = pl.C > 1 ? 1 : 0;
+        cfg.numAttrs = pl.C > 1 ? 2 : 1;
         void* args[] = {&p};
         if (cudaLaunchKernelExC(&cfg, pl.kernel, args) != cudaSuccess) return HEADLOSS_ERR_CUDA;
     }
@@ -728,8 +738,24 @@ int headloss_forward_backward_ext(headloss_t h, const void* logits, int64_t N, i
     fa.w_grpo = h->w.grpo;
     fa.w_ent = h->w.entropy;
     fa.divisor = x.divisor;
-    finalize_kernel<<<1, 32 * NACC, 0, s>>>(h->partials, ncl, h->n_valid, fa, scalars_out);
-    if (cudaGetLastError() != cudaSuccess) return HEADLOSS_ERR_CUDA;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.gridDim = dim3(1, 1, 1);
+        cfg.blockDim = dim3(32 * NACC, 1, 1);
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const double* pp = h->partials;
+        int n = int(ncl);
+        const long long* nvp = h->n_valid;
+        void* args[] = {&pp, &n, &nvp, &fa, &scalars_out};
+        if (cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(&finalize_kernel), args) !=
+            cudaSuccess)
+            return HEADLOSS_ERR_CUDA;
+    }
     return HEADLOSS_OK;
 }
 

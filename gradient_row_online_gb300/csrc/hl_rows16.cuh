@@ -390,6 +390,7 @@ __device__ __forceinline__ void rows_body16(const Params& p) {
     }
     // grad_scale / n, read once; held in a register (measured faster here
     // than a shared-memory read per row)
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the count kernel has completed
     const float kk = *p.kscale;
     __syncthreads();
     if (C > 1) cluster_barrier();  // every peer has started before any DSMEM store
@@ -814,6 +815,7 @@ __device__ __forceinline__ void rows_body16(const Params& p) {
     }
     if (rank == 0 && tid == 0) {
         store_partials(acc, p.partials + size_t(cid) * NACC);
+        asm volatile("griddepcontrol.launch_dependents;");  // the finalize kernel may launch
     }
     if (C > 1) cluster_barrier();
 }

@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
     };
     const DF Kd = split(double(K));
 
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the count kernel has completed
     if (tid == 0) {
         for (int b = 0; b < p.nbuf; ++b) mbar_init(smem_addr(&bars[b]), 1);
         fence_mbar_init();
@@ -550,6 +551,7 @@ __global__ void __launch_bounds__(THREADS, 1) rows_kernel(const __grid_constant_
             if (lost & (1u << b)) (void)mbar_wait_bounded(smem_addr(&bars[b]), (lost_par >> b) & 1u, p.wait_ns);
     }
     if (rank == 0 && tid == 0) {
+        asm volatile("griddepcontrol.launch_dependents;");
         double* out = p.partials + size_t(cid) * NACC;
 #pragma unroll
         for (int i = 0; i < NACC; ++i) out[i] = acc[i];

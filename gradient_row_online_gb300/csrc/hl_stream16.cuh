@@ -252,6 +252,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         }
         fence_mbar_init();
         for (int i = 0; i < 2 * NACC; ++i) acc[i] = 0.f;
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // the count kernel has completed
         coefs[KK_SLOT] = *p.kscale;
 #pragma unroll
         for (int i = 0; i < 6; ++i) rare[i] = QB[i];
@@ -724,6 +725,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
     }
     if (tid == 0) {
         store_partials(acc, p.partials + size_t(blockIdx.x) * NACC);
+        asm volatile("griddepcontrol.launch_dependents;");  // the finalize kernel may launch
     }
 }
 
