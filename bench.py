@@ -700,6 +700,25 @@ def e2e(wl, h, inp, args, dev, world):
     from gradient_row_online_gb300 import headloss as hlb
 
     names = ["logits", "labels", "teacher", "old_logprobs", "advantages"]
+    # pinned host memory: the inputs and two gradient buffers, per rank (71 GB
+    # for the all-in batch); the rows are cut, if need be, until every local
+    # rank's buffers fit in 70% of the host's available memory (several ranks
+    # on one host), and the line reports the rows used
+    per_row = sum(inp[k][0].numel() * inp[k].element_size() for k in names
+                  if inp[k] is not None) + 2 * inp["logits"][0].numel() * inp["logits"].element_size()
+    rows = wl.N
+    try:
+        with open("/proc/meminfo") as f:
+            avail = next(int(l.split()[1]) * 1024 for l in f if l.startswith("MemAvailable:"))
+        local = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+        fit = int(0.7 * avail / max(1, local) / per_row)
+        if fit < rows:
+            rows = max(1024, fit // 1024 * 1024)
+    except (OSError, StopIteration, ValueError):
+        pass
+    if rows < wl.N:
+        inp = {k: (None if inp[k] is None else inp[k][:rows]) for k in inp}
+        wl = wl.replace(N=rows)
     host = {k: (None if inp[k] is None else torch.empty(inp[k].shape, dtype=inp[k].dtype,
                                                         pin_memory=True)) for k in names}
     for k in names:
@@ -764,6 +783,7 @@ def e2e(wl, h, inp, args, dev, world):
     bound_ms = 1e3 * max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9))
     return {"value": wl.N * world * n / (total / 1e3), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "rows_per_rank": wl.N,
             "ms_per_step": total / n, "pipelined": "2 buffer sets, copy-in / compute / copy-out streams",
             "link": link, "link_bound_ms_per_step": bound_ms,
             "frac_of_link_bound": bound_ms / (total / n)}
