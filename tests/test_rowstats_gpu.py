@@ -137,8 +137,10 @@ def _oracle_stats(inp, wl):
     T = float(np.float32(wl.temperature))
     st = orc.tile_records(inp["logits"].float().cpu().numpy(), wl.softcap, wl.logits_scale,
                           temperature=T)
-    tt = orc.tile_records(inp["teacher"].float().cpu().numpy(), 0.0, 1.0 / T)
     f = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+    if inp["teacher"] is None:
+        return f(st[..., :4]), f(st[..., 4]), None
+    tt = orc.tile_records(inp["teacher"].float().cpu().numpy(), 0.0, 1.0 / T)
     return f(st[..., :4]), f(st[..., 4]), f(tt)
 
 
@@ -250,3 +252,33 @@ def test_gemm_tile_records_against_oracle(softcap, scale):
     np.testing.assert_allclose(got[..., 0], ref[..., 0], rtol=2e-5, atol=2e-5)
     np.testing.assert_allclose(got[..., 1], ref[..., 1], rtol=2e-5, atol=0)
     assert np.all(np.abs(got[..., 2] - ref[..., 2]) <= 2e-5 * (ref[..., 1] + np.abs(ref[..., 2])))
+
+
+@pytest.mark.parametrize("N,V", [(1, 256), (3, 512), (130, 256), (5, 4352)])
+@pytest.mark.parametrize("losses", [("ce", "z", "grpo", "grpo_stats", "entropy"), TEACH_SETS[0]])
+def test_rowstats_small_and_ragged_batches(N, V, losses):
+    """Batches below one CTA's eight warps, a ragged count of units, the
+    smallest vocabulary (one tile, a partial chunk per unit), with and without
+    a teacher; records from the oracle's definition (the GEMM takes 128-row
+    multiples only)."""
+    wl = W.Workload("rowstats", N, V, torch.bfloat16, losses, dict(W_DIST), softcap=30.0,
+                    logits_scale=0.5, temperature=1.5, teacher_noise=1.0, mask_frac=0.2,
+                    seed=N + V)
+    inp = W.make_inputs(wl, "cuda")
+    rs, rsT, trs = _oracle_stats(inp, wl)
+    h = pkg.headloss_for(wl)
+    g = torch.empty_like(inp["logits"])
+    out = torch.full((16,), float("nan"), device="cuda")
+    teach = "fkl" in losses
+    hlb.headloss_forward_backward_rowstats(h.h, inp["logits"], N, V, hlb.HEADLOSS_BF16,
+                                           inp["labels"], inp["old_logprobs"],
+                                           inp["advantages"], rs, g, out,
+                                           teacher=inp["teacher"] if teach else None,
+                                           row_stats_t=rsT if teach else None,
+                                           teacher_stats=trs if teach else None)
+    torch.cuda.synchronize()
+    assert h.device_error() == hlb.HEADLOSS_OK
+    h.close()
+    cfg, rec, ref, gmag = H.oracle_rows(wl, inp)
+    H.check_scalars(wl, out.double().cpu().numpy(), cfg, rec)
+    H.check_grad(wl, g, ref, gmag, rec)
