@@ -792,8 +792,9 @@ int headloss_forward_backward_rowstats(headloss_t h, const void* logits, int64_t
                                        const float* advantages, const void* row_stats,
                                        const float* row_stats_t, const void* teacher_stats,
                                        void* grad_out, float* scalars_out,
-                                       headloss_stream_t stream) {
-    const headloss_call_ext none = {nullptr, nullptr, 0, 0.0, nullptr};
+                                       const headloss_call_ext* ext, headloss_stream_t stream) {
+    headloss_call_ext x = {nullptr, nullptr, 0, 0.0, nullptr};
+    if (ext) x = *ext;
     if (!h) return HEADLOSS_ERR_ARG;
     const uint32_t f = h->flags;
     // reverse KL's coefficient needs a cross sum before the gradient pass
@@ -801,7 +802,7 @@ int headloss_forward_backward_rowstats(headloss_t h, const void* logits, int64_t
     const bool teach = (f & (L_DIST_CE | L_FKL)) != 0;
     {
         const int rc = check_call(h, logits, N, V, dtype, labels, teacher_logits, old_logprobs,
-                                  advantages, grad_out, scalars_out, none);
+                                  advantages, grad_out, scalars_out, x);
         if (rc) return rc;
     }
     if (dtype != HEADLOSS_BF16) return HEADLOSS_ERR_DTYPE;
@@ -823,8 +824,8 @@ int headloss_forward_backward_rowstats(headloss_t h, const void* logits, int64_t
     const void* kernel = onepass_kernel_bf16(feat);
     if (!kernel) return HEADLOSS_ERR_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    count_valid_kernel<<<1, 1024, 0, s>>>(labels, N, V, h->n_valid, h->err, h->w.grad_scale, 0.0,
-                                          h->kscale);
+    count_valid_kernel<<<1, 1024, 0, s>>>(labels, N, V, h->n_valid, h->err, h->w.grad_scale,
+                                          x.divisor, h->kscale);
     int grid = 0;
     if (N > 0) {
         // four warps per row (each a quarter of its words), eight warps per
@@ -871,6 +872,11 @@ int headloss_forward_backward_rowstats(headloss_t h, const void* logits, int64_t
         p.err = h->err;
         p.wait_ns = h->wait_ns;
         p.drop_row = -1;
+        p.lp_out = x.new_logprobs;
+        p.rl_out = x.row_loss;
+        p.divisor = x.divisor;
+        p.accumulate = x.accumulate;
+        p.tok = x.token_coeff;
         int nt = int(V / 256);
         const void* rs = row_stats;
         const void* rsT = teach ? static_cast<const void*>(row_stats_t) : nullptr;
@@ -889,7 +895,7 @@ int headloss_forward_backward_rowstats(headloss_t h, const void* logits, int64_t
     fa.w_rkl = 0.f;  // refused above
     fa.w_grpo = h->w.grpo;
     fa.w_ent = h->w.entropy;
-    fa.divisor = 0.0;
+    fa.divisor = x.divisor;
     finalize_kernel<<<1, 32 * NACC, 0, s>>>(h->partials, grid, h->n_valid, fa, scalars_out);
     if (cudaGetLastError() != cudaSuccess) return HEADLOSS_ERR_CUDA;
     return HEADLOSS_OK;

@@ -337,8 +337,15 @@ __global__ void __launch_bounds__(OP_THREADS, 2)
         rec[R_ZY] = zy;
         rec[R_HASY] = hasy;
         __syncwarp();
-        const RowCoef k = row_epilogue16<TEACH, false, ENT, CAP, true>(
+        RowCoef k = row_epilogue16<TEACH, false, ENT, CAP, true>(
             p, recs[warp], 32, false, old_lp, adv, accs[warp], lane, r, kk, &rls[warp]);
+        if (p.tok != nullptr) {
+            // a per-token coefficient c = d(total)/d(log p(label)) (GSPO's):
+            // c (delta_label - p), scaled like every coefficient
+            const float c = p.tok[r] * p.s;
+            k.pc -= c;
+            k.bc -= c;
+        }
         // all have read their lane records before the next row's exchange
         // reuses the area
         group_sync();

@@ -133,7 +133,7 @@ def load_library(path: str = LIB_PATH):
                                                     vp, vp, vp]
     lib.headloss_lmhead_logits_rowstats.restype = i32
     lib.headloss_forward_backward_rowstats.argtypes = [vp, vp, i64, i64, i32, vp, vp, vp, vp, vp,
-                                                       vp, vp, vp, vp, vp]
+                                                       vp, vp, vp, vp, vp, vp]
     lib.headloss_forward_backward_rowstats.restype = i32
     _lib = lib
     return lib
@@ -261,16 +261,20 @@ def headloss_lmhead_logits_rowstats(hidden, weight, N, D, V, softcap, logits_sca
 
 def headloss_forward_backward_rowstats(h, logits, N, V, dtype, labels, old_logprobs, advantages,
                                        row_stats, grad_out, scalars_out, stream=None,
-                                       teacher=None, row_stats_t=None,
-                                       teacher_stats=None) -> None:
+                                       teacher=None, row_stats_t=None, teacher_stats=None,
+                                       new_logprobs=None, row_loss=None, accumulate=False,
+                                       divisor=0.0, token_coeff=None) -> None:
     """The loss's gradient pass alone from the GEMMs' row statistics (the
-    student's, its sums at the temperature, the teacher's; include/headloss.h);
-    raises HeadlossError on a bad status."""
+    student's, its sums at the temperature, the teacher's; include/headloss.h),
+    with the extras of headloss_forward_backward_ext; raises HeadlossError on a
+    bad status."""
+    ext = headloss_call_ext(_ptr(new_logprobs), _ptr(row_loss), int(bool(accumulate)),
+                            float(divisor), _ptr(token_coeff))
     _check(load_library().headloss_forward_backward_rowstats(
         h, _ptr(logits), int(N), int(V), int(dtype), _ptr(labels), _ptr(teacher),
         _ptr(old_logprobs), _ptr(advantages), _ptr(row_stats), _ptr(row_stats_t),
-        _ptr(teacher_stats), _ptr(grad_out), _ptr(scalars_out), _stream(stream)),
-        "headloss_forward_backward_rowstats")
+        _ptr(teacher_stats), _ptr(grad_out), _ptr(scalars_out), ctypes.byref(ext),
+        _stream(stream)), "headloss_forward_backward_rowstats")
 
 
 def headloss_gspo_seam(new_logprobs, old_logprobs, advantages, labels, N, V, seg_offsets, n_seg,

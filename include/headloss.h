@@ -372,6 +372,13 @@ int headloss_gspo_seam(const float* new_logprobs, const float* old_logprobs,
  * row_stats_t at T != 1, is ERR_MISSING_INPUT.  In place is allowed (each
  * word is read before its gradient replaces it).  Three launches; results as
  * headloss_forward_backward, within the same tolerances.
+ * ext:           NULL, or the extras of headloss_forward_backward_ext with
+ *                the same meaning and errors: per-row log p(label) and total
+ *                loss, accumulation into grad_out (not in place), the
+ *                divisor of a split batch, and GSPO's per-token coefficient.
+ *                With ext, GSPO runs on the GEMM's records as well: this call
+ *                with new_logprobs (grad_out may be NULL), headloss_gspo_seam,
+ *                then this call with token_coeff.
  */
 int headloss_forward_backward_rowstats(headloss_t h, const void* logits, int64_t N, int64_t V,
                                        int dtype, const int64_t* labels,
@@ -379,7 +386,7 @@ int headloss_forward_backward_rowstats(headloss_t h, const void* logits, int64_t
                                        const float* advantages, const void* row_stats,
                                        const float* row_stats_t, const void* teacher_stats,
                                        void* grad_out, float* scalars_out,
-                                       headloss_stream_t stream);
+                                       const headloss_call_ext* ext, headloss_stream_t stream);
 
 /* Kernel launches one headloss_forward_backward call enqueues (constant). */
 int headloss_launches_per_call(void);
