@@ -389,13 +389,20 @@ bool pick_resident(const headloss* h, const Plan* cand, int ncand, Plan* best) {
 // one of 512: one CTA's row merge and barriers hide behind the other's
 // arithmetic); then the most slots that still keep them co-resident (a
 // deeper ring rides out DRAM latency: three slots beat two by ~1%).
-bool pick_stream(const headloss* h, const Plan* cand, int ncand, Plan* best) {
+// Except for teacher rows without softcap (`fewer_rows`): there one CTA of
+// 512 threads per SM halves the rows in flight, so that with the gradient
+// stores kept out of L2 a row's second read finds nearly all of it still
+// there (DRAM bytes 1.34x -> 1.06x the minimum on the distillation set,
+// 2.625 -> 2.602 ms); with softcap the arithmetic is heavier and two CTAs per
+// SM still win (all-in 11.75 against 12.06 ms).
+bool pick_stream(const headloss* h, const Plan* cand, int ncand, bool fewer_rows, Plan* best) {
     Plan b;
     double bscore = -1.0;
     for (int i = 0; i < ncand; ++i) {
         const Plan& c = cand[i];
         if (c.kind != HEADLOSS_KERNEL_STREAM) continue;
-        const double score = c.chunk_words * 1e6 + double(c.ncl) * 1e2 + c.nbuf;
+        const double score = c.chunk_words * 1e6 + (fewer_rows ? c.threads * 1e3 : 0.0) +
+                             double(c.ncl) * 1e2 + c.nbuf;
         if (score > bscore) {
             b = c;
             bscore = score;
@@ -438,7 +445,9 @@ int make_plan(headloss* h, int64_t V, int dtype, Plan* out, int acc = 0, int inp
     if (rc) return rc;
     Plan res, str, best;
     const bool have_res = pick_resident(h, cand, ncand, &res);
-    const bool have_str = pick_stream(h, cand, ncand, &str);
+    // the rows the hinted streaming instantiation takes (kernel_for)
+    const bool fewer_rows = !acc && (feat & F_TEACH) && !(feat & F_SOFTCAP);
+    const bool have_str = pick_stream(h, cand, ncand, fewer_rows, &str);
     if (fk == HEADLOSS_KERNEL_STREAM) {
         if (!have_str) return HEADLOSS_ERR_SIZE;
         best = str;

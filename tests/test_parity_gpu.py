@@ -89,7 +89,8 @@ def test_forced_resident_plans(cluster, stages, threads):
 # the streaming kernel: aligned rows only (V a multiple of 8), several chunks
 # per row plus a partial last chunk, every feature set, both tanh paths
 @pytest.mark.parametrize("stages,threads,words", [(2, 256, 1), (3, 512, 1), (4, 256, 2),
-                                                   (6, 256, 4), (6, 512, 2), (8, 256, 1)])
+                                                   (6, 256, 4), (6, 512, 2), (8, 256, 1),
+                                                   (3, 512, 4)])
 @pytest.mark.parametrize("V", [8, 1000, 20008])
 def test_forced_stream_plans(stages, threads, words, V):
     plan = dict(kernel=STREAM, stages=stages, threads=threads, chunk_words=words)
