@@ -23,10 +23,10 @@ enum : int {
     // gradient has no entropy term (the entropy may still be a metric)
     F_DF = 128,
     // streaming kernel only: L2 cache hints on the row copies (the teacher's
-    // first pass evict-last, second pass evict-first) and streaming gradient
-    // stores; for
-    // teacher rows without softcap, where it measured faster (the second read
-    // then hits L2 more often)
+    // first pass evict-last, second pass evict-first); for teacher rows
+    // without softcap, where it measured faster (the second read then hits L2
+    // more often).  Every teacher instantiation stores its gradient with the
+    // streaming hint.
     F_L2P = 256,
 };
 
