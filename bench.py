@@ -325,7 +325,9 @@ def run_ours(args, rank, world, local):
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "peak_kind": peak_kind,
             "frac_of_nominal_8000": achieved / 8000.0,
-            "traffic": recorded_traffic(wl.name),
+            # the recorded counters describe the full workload in its automatic plan
+            "traffic": (recorded_traffic(wl.name)
+                        if wl.N == W.WORKLOADS[args.workload].N and not args.plan else None),
             "algorithmic_bytes_per_launch": bytes_per_launch,
             "kernel": kernel_label(plan, wl),
         },
