@@ -238,7 +238,9 @@ static void oracle_row(const oracle_cfg* cfg, int64_t V, const double* x, int64_
         const double delta = (has_labels && j == label) ? 1.0 : 0.0;
         /* terms[i]: one loss's contribution; mags[i]: the size of the
          * quantities it is computed from (a factor that is itself a
-         * difference, like log pT - log q - RKL, counts its parts) */
+         * difference, like log pT - log q - RKL, counts its parts, down to
+         * the logits and row log-sum-exps a log-probability is formed from:
+         * log pT_j = zT_j - lse_T) */
         double terms[8], mags[8];
         int nt = 0;
         /* CE: d(lse - z_y)/dz_j = p_j - delta */
@@ -268,7 +270,7 @@ static void oracle_row(const oracle_cfg* cfg, int64_t V, const double* x, int64_
             const double log_pT = zT[j] - lse_T, log_q = u[j] - lsq;
             terms[nt] = k * cfg->w_rkl * pT[j] * (log_pT - log_q - rkl) / T;
             mags[nt++] = fabs(k * cfg->w_rkl * pT[j] / T) *
-                         (fabs(log_pT) + fabs(log_q) + fabs(rkl));
+                         (fabs(zT[j]) + fabs(lse_T) + fabs(u[j]) + fabs(lsq) + fabs(rkl));
         }
         /* GRPO: d loss/d rho = -A (unclipped branch) or 0; d rho/d lp = rho;
          * d lp/dz_j = delta - p_j */
@@ -279,7 +281,7 @@ static void oracle_row(const oracle_cfg* cfg, int64_t V, const double* x, int64_
         /* entropy: dH/dz_j = -p_j (log p_j + H) */
         if (f & OR_ENTROPY) {
             terms[nt] = k * cfg->w_entropy * (-p[j] * ((z[j] - lse) + H));
-            mags[nt++] = fabs(k * cfg->w_entropy * p[j]) * (fabs(z[j] - lse) + fabs(H));
+            mags[nt++] = fabs(k * cfg->w_entropy * p[j]) * (fabs(z[j]) + fabs(lse) + fabs(H));
         }
 
         const double dzdx = transform_deriv(cfg, x[j]);
