@@ -178,6 +178,7 @@ int feature_set(const headloss* h) {
     if (h->softcap > 0.f) f |= F_SOFTCAP;
     if (h->flags & L_DIST_CE) f |= F_DCE;
     if ((h->flags & L_ENTROPY) && h->w.entropy != 0.f) f |= F_ENTG;
+    if ((f & F_TEACH) && h->T == 2.f) f |= F_T2;
     return f;
 }
 
@@ -199,6 +200,8 @@ const void* kernel_for(int kind, int dtype, int feat) {
         // L2 hints on the copies of teacher rows without softcap (measured:
         // distillation 2.77 -> 2.68 ms; with softcap, the all-in set, slower)
         if (!acc && (feat & F_TEACH) && !(feat & F_SOFTCAP)) feat |= F_L2P;
+        // the T = 2 form: hinted bf16 instantiations without entropy only
+        if (!((feat & F_L2P) && dtype == HEADLOSS_BF16 && !(feat & F_ENT))) feat &= ~F_T2;
         switch (dtype) {
             case HEADLOSS_BF16: return acc ? stream_kernel_bf16_acc(feat) : stream_kernel_bf16(feat);
             case HEADLOSS_FP16: return acc ? stream_kernel_fp16_acc(feat) : stream_kernel_fp16(feat);

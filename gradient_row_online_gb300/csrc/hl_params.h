@@ -28,6 +28,10 @@ enum : int {
     // more often).  Every teacher instantiation stores its gradient with the
     // streaming hint.
     F_L2P = 256,
+    // streaming kernel only: the distillation temperature is exactly 2, so
+    // a logit's probabilities at T = 1 and at T share one exponential:
+    // 2^d = (2^(d/2))^2 (bf16 teacher rows without softcap or entropy)
+    F_T2 = 512,
 };
 
 // Loss / metric bits (values match enum headloss_flag).

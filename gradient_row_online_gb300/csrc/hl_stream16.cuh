@@ -83,6 +83,9 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
     constexpr bool CAP = (FEAT & F_SOFTCAP) != 0;
     constexpr bool DCE = TEACH && (FEAT & F_DCE) != 0;
     constexpr bool ENTG = ENT && (FEAT & F_ENTG) != 0;
+    // T = 2 exactly (no softcap, no entropy): 2^d = (2^(d/2))^2, so the
+    // probabilities at T = 1 and at T come from one exponential
+    constexpr bool T2 = TEACH && !CAP && !ENT && (FEAT & F_T2) != 0;
     constexpr int OPS = TEACH ? 2 : 1;
 
     extern __shared__ __align__(128) unsigned char smem[];
@@ -144,6 +147,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         }
     }
     const f2 K2 = pk1(K1), A22 = pk1(A2), Kc2 = pk1(Kc), invT2 = pk1(invT), KT2 = pk1(KT);
+    const f2 K2h = pk1(T2 ? 0.5f * K1 : 0.f);  // T = 2: the first pass forms d / 2 directly
     const f2 KinvT2 = pk1(K1 * invT);
     const f2 m2 = pk1(CAP ? -1.f / (Kc * Kc) : 0.f), one2 = pk1(1.f);
     const f2 z2 = pk1(0.f);
@@ -386,12 +390,21 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         const bool need_sx = !CAP || !fixed_shift;
         // one pair's contribution to the sums, given its shifted logit d
         auto accum = [&](f2 d, uint32_t tbits, f2 num2) {
-            const f2 e = ex2p(d);
+            f2 e, dT, eT;
+            if constexpr (T2) {
+                dT = d;  // the caller passes d / 2
+                eT = ex2p(dT);
+                e = mul2(eT, eT);
+            } else {
+                e = ex2p(d);
+            }
             S2 = add2(S2, e);
             if (ENT) E2 = fma2(e, d, E2);
             if (TEACH) {
-                const f2 dT = mul2(d, invT2);
-                const f2 eT = ex2p(dT);
+                if constexpr (!T2) {
+                    dT = mul2(d, invT2);
+                    eT = ex2p(dT);
+                }
                 ST2 = add2(ST2, eT);
                 const f2 du = fma2(P16::unpack(tbits), KT2, num2);
                 const f2 eq = ex2p(du);
@@ -506,6 +519,7 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                 else tier_hi = tier > tier_hi ? tier : tier_hi;
             }
             const f2 nzm2 = pk1(-zm), num2 = pk1(-um);
+            const f2 nzmh2 = pk1(T2 ? -0.5f * zm : 0.f);
             if (full && tier == 0) {
                 // hot path: four words, the narrow tier (or no softcap), unrolled
 #pragma unroll
@@ -514,7 +528,10 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                     const uint32_t tb[4] = {tw[i].x, tw[i].y, tw[i].z, tw[i].w};
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        accum(shifted(P16::unpack(xa[kk]), nzm2, IntC<0>{}), tb[kk], num2);
+                        if constexpr (T2)
+                            accum(fma2(P16::unpack(xa[kk]), K2h, nzmh2), tb[kk], num2);
+                        else
+                            accum(shifted(P16::unpack(xa[kk]), nzm2, IntC<0>{}), tb[kk], num2);
                 }
             } else {
                 // cold path: a partial chunk or a wider tier, one word at a time
@@ -531,7 +548,8 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
                     for (int kk = 0; kk < 4; ++kk) {
                         const f2 xv = P16::unpack(xa[kk]);
                         f2 d;
-                        if (!CAP || tier == 0) d = shifted(xv, nzm2, IntC<0>{});
+                        if (T2) d = fma2(xv, K2h, nzmh2);
+                        else if (!CAP || tier == 0) d = shifted(xv, nzm2, IntC<0>{});
                         else if (tier == 1) d = shifted(xv, nzm2, IntC<1>{});
                         else d = shifted(xv, nzm2, IntC<2>{});
                         accum(d, tb[kk], num2);
@@ -594,6 +612,16 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
         const f2 pc2 = pk1(h.pc), ps2 = pk1(h.ps), tc2 = pk1(h.tc), ts2 = pk1(h.ts);
         const f2 qc2 = pk1(h.qc), s2 = pk1(s), ndlse2 = pk1(-dlse);
         const f2 nKT2 = pk1(-KT);
+        // T = 2: hh = 2^((x K1 + nlse) / 2), so p 2^sg = hh^2 and pT 2^sg = hh cT
+        // with cT = 2^(nlseT - nlse / 2) (a row constant, from the library
+        // exp2); the gradient is hh (hh pc + cT tco) + q qc, and with reverse
+        // KL cT tco = cT (ts (dxu - dlse) + tc), dxu = (x s - t) KT, is
+        // x A + (t B + C)
+        const float cT = T2 ? exp2f(h.nlseT - 0.5f * h.nlse) : 0.f;
+        const f2 Kh2 = pk1(T2 ? 0.5f * K1 : 0.f), nlseh2 = pk1(T2 ? 0.5f * h.nlse : 0.f);
+        const f2 rA2 = pk1(T2 && RKL ? cT * h.ts * s * KT : 0.f);
+        const f2 rB2 = pk1(T2 && RKL ? -cT * h.ts * KT : 0.f);
+        const f2 rC2 = pk1(T2 ? cT * (RKL ? fmaf(-h.ts, dlse, h.tc) : h.tc) : 0.f);
         // accumulating: the label element's existing value, read before this
         // row's word stores overwrite it
         float old_y = 0.f;
@@ -608,29 +636,39 @@ __global__ void __launch_bounds__(THREADS, 1) stream_kernel16(const __grid_const
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const f2 xv = P16::unpack(xa[kk]);
-                f2 zs = z2, omt = z2, arg, argT = z2;
-                if constexpr (CAP) {
-                    zs_omt(xv, zs, omt, tierc);
-                    arg = add2(zs, nlse2);
-                    if (TEACH) argT = fma2(zs, invT2, nlseT2);
-                } else {
-                    arg = fma2(xv, K2, nlse2);
-                    if (TEACH) argT = fma2(xv, KinvT2, nlseT2);
-                }
-                f2 g = mul2(ex2p(arg), ENTG ? fma2(ps2, arg, pc2) : pc2);
-                if (TEACH) {
+                f2 omt = z2, g;
+                if constexpr (T2) {
                     const f2 tv = P16::unpack(tb[kk]);
-                    const f2 pT = ex2p(argT);
+                    const f2 hh = ex2p(fma2(xv, Kh2, nlseh2));
                     const f2 q = ex2p(fma2(tv, KT2, nlsq2));
-                    f2 tco = tc2;
-                    if (RKL) {
-                        // log pT - log q from the logit difference
-                        const f2 dxu = CAP ? fma2(zs, invT2, mul2(tv, nKT2))
-                                           : mul2(fma2(xv, s2, sub2(z2, tv)), KT2);
-                        tco = fma2(ts2, add2(dxu, ndlse2), tc2);
+                    f2 tcoT = rC2;
+                    if constexpr (RKL) tcoT = fma2(xv, rA2, fma2(tv, rB2, rC2));
+                    g = fma2(hh, fma2(hh, pc2, tcoT), mul2(q, qc2));
+                } else {
+                    f2 zs = z2, arg, argT = z2;
+                    if constexpr (CAP) {
+                        zs_omt(xv, zs, omt, tierc);
+                        arg = add2(zs, nlse2);
+                        if (TEACH) argT = fma2(zs, invT2, nlseT2);
+                    } else {
+                        arg = fma2(xv, K2, nlse2);
+                        if (TEACH) argT = fma2(xv, KinvT2, nlseT2);
                     }
-                    g = fma2(pT, tco, g);
-                    g = fma2(q, qc2, g);
+                    g = mul2(ex2p(arg), ENTG ? fma2(ps2, arg, pc2) : pc2);
+                    if (TEACH) {
+                        const f2 tv = P16::unpack(tb[kk]);
+                        const f2 pT = ex2p(argT);
+                        const f2 q = ex2p(fma2(tv, KT2, nlsq2));
+                        f2 tco = tc2;
+                        if (RKL) {
+                            // log pT - log q from the logit difference
+                            const f2 dxu = CAP ? fma2(zs, invT2, mul2(tv, nKT2))
+                                               : mul2(fma2(xv, s2, sub2(z2, tv)), KT2);
+                            tco = fma2(ts2, add2(dxu, ndlse2), tc2);
+                        }
+                        g = fma2(pT, tco, g);
+                        g = fma2(q, qc2, g);
+                    }
                 }
                 // dz/dx = s (1 - tanh^2); s is already in the coefficients
                 const f2 gw = CAP ? mul2(g, omt) : g;

@@ -21,6 +21,7 @@ const void* stream_kernel_bf16(int feat) {
         HL_ENT_SET(0)
         HL_ENT_SET(F_SOFTCAP)
         HL_L2P_SET(0)
+        HL_L2P_SET(F_T2)
         HL_L2P_SET(F_ENT)
         HL_L2P_SET(F_ENT | F_ENTG)
         default: return nullptr;

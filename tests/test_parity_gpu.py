@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import oracle as orc
+import gradient_row_online_gb300 as pkg
 from gradient_row_online_gb300 import headloss as hlb
 from gradient_row_online_gb300 import workloads as W
 from tests import _harness as H
@@ -371,3 +372,50 @@ def test_full_size_workload(name):
     H.check_grad(wl, g.index_select(0, sel), ref, gmag, srec)
     del inp, g
     torch.cuda.empty_cache()
+
+
+# distillation at T = 2 exactly: bf16 teacher rows without softcap or entropy
+# take the one-exponential form (2^d = (2^(d/2))^2) on the streaming kernel;
+# every teacher loss combination, several chunk shapes with a partial last
+# chunk, structured rows (large offsets, spikes, ramps), and the same call at
+# T = 2 where that form does not apply (fp16 logits, accumulation, entropy)
+T2_SETS = [("ce", "fkl", "rkl"), ("dist_ce", "fkl"), ("rkl",),
+           ("ce", "z", "dist_ce", "rkl", "grpo", "grpo_stats")]
+
+
+@pytest.mark.parametrize("losses", T2_SETS)
+@pytest.mark.parametrize("plan", [None, dict(kernel=STREAM, stages=3, threads=512, chunk_words=4),
+                                  dict(kernel=STREAM, stages=3, threads=256, chunk_words=1)])
+@pytest.mark.parametrize("V", [1000, 20008, 70000])
+def test_temperature_two_streaming(losses, plan, V):
+    wl = small(losses, N=23, V=V, temperature=2.0, sigma=4.0, logits_scale=0.8)
+    full_check(wl, plan=plan)
+    structured_check(wl.replace(N=24, seed=3), plan=plan or dict(kernel=STREAM, stages=3,
+                                                                  threads=256, chunk_words=4))
+
+
+@pytest.mark.parametrize("kw", [dict(dtype=torch.float16), dict(losses=("ce", "fkl", "entropy")),
+                                dict(softcap=30.0)])
+def test_temperature_two_general_path(kw):
+    losses = kw.pop("losses", ("ce", "fkl", "rkl"))
+    wl = small(losses, N=23, V=20008, temperature=2.0, **kw)
+    full_check(wl, plan=dict(kernel=STREAM, stages=3, threads=256, chunk_words=4))
+
+
+def test_temperature_two_accumulating():
+    wl = small(("ce", "fkl", "rkl"), N=23, V=20008, temperature=2.0)
+    inp = W.make_inputs(wl, "cuda")
+    h = pkg.headloss_for(wl)
+    h.force_plan(kernel=STREAM, stages=3, threads=256, chunk_words=4)
+    g0 = (torch.randn(inp["logits"].shape, device="cuda") * 1e-4).to(wl.dtype)
+    g = g0.clone()
+    h(inp["logits"], inp["labels"], inp["teacher"], inp["old_logprobs"], inp["advantages"], g,
+      accumulate=True)
+    torch.cuda.synchronize()
+    assert h.device_error() == hlb.HEADLOSS_OK
+    cfg, rec, ref, gmag = H.oracle_rows(wl, inp)
+    valid = rec[:, orc.RF["valid"]] > 0
+    sel = torch.from_numpy(np.nonzero(valid)[0]).cuda()
+    g0h = g0.double().cpu().numpy()
+    H.check_grad(wl, g.index_select(0, sel), (g0h + ref)[valid], (gmag + np.abs(g0h))[valid],
+                 rec[valid])
