@@ -110,7 +110,11 @@ enum headloss_slot {
  *               A weight of a loss whose flag is not set is ignored.
  * temperature:  T > 0, divides student AND teacher logits for the three
  *               distillation losses only (PR #549 "Bundled fix": the
- *               distillation temperature is honoured).
+ *               distillation temperature is honoured).  At T = 2 exactly,
+ *               streamed bf16 teacher rows without softcap or entropy take
+ *               the probabilities at T = 1 and at T from one exponential
+ *               (2^d = (2^(d/2))^2): the same results within the stated
+ *               tolerances, fewer operations per element.
  * clip_eps:     GRPO epsilon >= 0 (symmetric clip).
  * softcap:      c >= 0; c > 0 applies z = c * tanh(x / c) before the scale.
  * logits_scale: s > 0; the student softmax sees z = s * softcap(x) (PR #549
