@@ -419,3 +419,54 @@ def test_temperature_two_accumulating():
     g0h = g0.double().cpu().numpy()
     H.check_grad(wl, g.index_select(0, sel), (g0h + ref)[valid], (gmag + np.abs(g0h))[valid],
                  rec[valid])
+
+
+def test_temperature_two_without_labels():
+    """The temperature-2 form with no labels (every row valid, no label term)."""
+    plan = dict(kernel=STREAM, stages=3, threads=512, chunk_words=4)
+    for losses in (("dist_ce", "fkl"), ("fkl", "rkl"), ("rkl",)):
+        wl = small(losses, N=29, V=20008, temperature=2.0, logits_scale=0.7)
+        inp = dict(W.make_inputs(wl, "cuda"), labels=None)
+        got, g, _ = H.run_gpu(wl, inp, plan=plan)
+        cfg, rec, ref, gmag = H.oracle_rows(wl, inp)
+        assert got[14] == wl.N
+        H.check_scalars(wl, got, cfg, rec)
+        H.check_grad(wl, g, ref, gmag, rec)
+
+
+def test_temperature_two_per_row_outputs_and_divisor():
+    """The temperature-2 form with the call's per-row outputs and a batch split
+    over two calls that share one divisor."""
+    from tests import test_call_ext_gpu as CX
+    wl = small(("ce", "fkl", "rkl"), N=40, V=20008, temperature=2.0)
+    inp = W.make_inputs(wl, "cuda")
+    cfg, rec, ref, gmag = H.oracle_rows(wl, inp)
+    whole = orc.reduce(cfg, rec)
+    valid = rec[:, orc.RF["valid"]] > 0
+    lp_ref, rl_ref = CX.expected_rows(wl, rec)
+    h = pkg.headloss_for(wl)
+    h.force_plan(kernel=STREAM, stages=3, threads=512, chunk_words=4)
+    g = torch.empty_like(inp["logits"])
+    lp = torch.full((wl.N,), float("nan"), device="cuda")
+    rl = torch.full((wl.N,), float("nan"), device="cuda")
+    sums = np.zeros(16)
+    for sl in (slice(0, 13), slice(13, 40)):
+        pick = lambda t: None if t is None else t[sl].contiguous()
+        gp = torch.empty_like(inp["logits"][sl])
+        lpp = torch.empty(sl.stop - sl.start, device="cuda")
+        rlp = torch.empty(sl.stop - sl.start, device="cuda")
+        out = h(pick(inp["logits"]), pick(inp["labels"]), pick(inp["teacher"]), None, None, gp,
+                new_logprobs=lpp, row_loss=rlp, divisor=float(whole[14]))
+        torch.cuda.synchronize()
+        assert h.device_error() == hlb.HEADLOSS_OK
+        g[sl] = gp
+        lp[sl] = lpp
+        rl[sl] = rlp
+        sums += out.double().cpu().numpy()
+    tol = H.SCALAR_TOL[wl.dtype]
+    CX.close_rows(lp.double().cpu().numpy(), lp_ref, valid, tol)
+    CX.close_rows(rl.double().cpu().numpy(), rl_ref, valid, tol)
+    for slot in (0, 1, 4, 5):  # total, CE, forward KL, reverse KL
+        assert abs(sums[slot] - whole[slot]) <= tol * max(1.0, abs(whole[slot])), (slot, sums,
+                                                                                   whole)
+    H.check_grad(wl, g, ref, gmag, rec)
