@@ -470,3 +470,20 @@ def test_temperature_two_per_row_outputs_and_divisor():
         assert abs(sums[slot] - whole[slot]) <= tol * max(1.0, abs(whole[slot])), (slot, sums,
                                                                                    whole)
     H.check_grad(wl, g, ref, gmag, rec)
+
+
+def test_planner_choices_on_the_benchmarked_sets():
+    """The plans the measured figures come from: streamed teacher rows without
+    softcap on one 512-thread CTA per SM (half the rows in flight), streamed
+    teacher rows with softcap on two 256-thread CTAs per SM, student-only rows
+    resident (GRPO rows in 6-CTA clusters), fp32 rows resident in 3-CTA clusters."""
+    want = {"ce_distill_bf16": ("stream", 1, 512, 4), "all_in_bf16": ("stream", 1, 256, 4),
+            "grpo_z_entropy_bf16": ("resident", 6, 256, 0), "ce_z_bf16": ("resident", 1, 256, 0),
+            "ce_z_fp32": ("resident", 3, 256, 0)}
+    for name, (kernel, cluster, threads, words) in want.items():
+        wl = W.WORKLOADS[name]
+        h = pkg.headloss_for(wl)
+        p = h.plan(wl.V, hlb.dtype_code(wl.dtype))
+        h.close()
+        assert (p["kernel"], p["cluster"], p["threads"], p["chunk_words"]) == \
+            (kernel, cluster, threads, words), (name, p)
